@@ -1,0 +1,378 @@
+"""Benchmark: fused Hadamard rotation + NVFP4 quantization on GB300.
+
+One step = the whole hot path over one activation tensor already resident in HBM:
+hq_rot_amax (pass 1: rotate, global amax) then hq_rotate_quant_nvfp4 (pass 2: rotate, block
+scales, codes).  The metric is GB/s of algorithmic bytes in + out per step:
+    bytes = M*K*sizeof(x)  (x read)  +  M*K/2 (codes)  +  M*K/16 (E4M3 scales).
+Default workload: x bf16 [32768, 28672] (1.88 GB, larger than L2, so no flush is needed
+between steps), N(0,1) with 0.5% outlier channels x100, seed 3, rotation group 16.
+
+Also reported on the same JSON line:
+  roofline      pass 2 (the dominant kernel): its algorithmic bytes / its average launch time
+                (CUDA events around every launch in the timed region), against the measured
+                HBM copy bandwidth;
+  e2e           the same metric through the public API with host buffers: pinned host x ->
+                device, both passes, codes + scales + s_global -> pinned host, every step;
+  cpu_baseline  the CPU oracle on a bounded sample of the workload, on this host's cores;
+  clocks        nvidia-smi samples taken during the timed region.
+
+--impl reference times the CPU oracle (the definition the kernels are checked against) as the
+reference arm; it uses no GPU.
+
+Multi-GPU: --gpus N under torchrun runs N independent replicas (one tensor per GPU, weak
+scaling, no collective on the data path); the barrier and max-over-ranks time are host-side.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "bf16_32768x28672"
+METRIC = "rotate+NVFP4-quant GB/s (bytes in+out) and % of GB300 HBM peak"
+L2_BYTES = 126 * 1024 * 1024
+
+# Pass-2 DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the kernel source it was taken on.  Captured on the
+# bf16 [16384, 8192] G=16 tensor and scaled by element count to the bench workload; the
+# capture and its command are summarised under profiles/.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("hadamard_rotation_gb300/csrc/hq_kernels.cuh", "hadamard_rotation_gb300/csrc/hq.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--group", type=int, default=None, help="rotation group (default: the workload's first)")
+    ap.add_argument("--e2e-steps", type=int, default=None, help="steps of the host-buffer run (default: min(steps, 200))")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------- clocks ------
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and not (parts[1].endswith(self.uuid) or self.uuid.endswith(parts[1])):
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        pw = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def device_uuid(dev) -> str | None:
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u.replace("GPU-", "")
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------- CPU oracle ------
+
+def oracle_sample_run(w, rows: int, reps: int, warm: int = 1):
+    """Time the CPU oracle (both passes) on the first `rows` rows of the workload."""
+    import oracle
+    from hadamard_rotation_gb300 import synth
+
+    oracle.build()
+    x = synth.as_oracle_array(synth.generate(w, rows=slice(0, rows)))
+    group = w.groups[0]
+    threads = os.cpu_count() or 1
+    for _ in range(warm):
+        oracle.quantize(x, group, nthreads=threads)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.quantize(x, group, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    nbytes = rows * w.K * w.elem_bytes + rows * w.K // 2 + rows * w.K // 16
+    return nbytes, times, threads
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0  # the reference arm runs on rank 0 only; other ranks exit without work
+    # Size the per-step sample so the whole run (warm-up + steps) takes about two minutes:
+    # calibrate the oracle's rate on 64 rows first.
+    _, t_cal, _ = oracle_sample_run(w, min(w.M, 64), reps=1, warm=1)
+    per_row = max(t_cal[0] / min(w.M, 64), 1e-7)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(min(w.M, max(1, budget / per_row)))
+    nbytes, times, threads = oracle_sample_run(w, rows, reps=args.steps, warm=args.warmup)
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    sample = f"rows 0..{rows - 1} of {w.name} ({rows}x{w.K}), both passes per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.describe(), "group": w.groups[0], "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------- GPU arm -----
+
+def run_ours(args, w):
+    import torch
+
+    import hadamard_rotation_gb300 as hq
+    from hadamard_rotation_gb300 import build as hq_build
+    from hadamard_rotation_gb300 import synth
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU path)")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        # control plane only (barrier, max of the timings): replicas exchange no data
+        dist.init_process_group("gloo")
+        pg = dist
+    hq_build.build()
+    hq.load()
+    group = args.group if args.group is not None else w.groups[0]
+
+    x_host = synth.generate(w).pin_memory()
+    x = x_host.to(dev)
+    bytes_in = x.numel() * x.element_size()
+    bytes_out = w.numel // 2 + w.numel // 16
+    step_bytes = bytes_in + bytes_out
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    q = torch.empty((w.M, w.K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((w.M, w.K // 16), dtype=torch.uint8, device=dev)
+    sg = torch.empty(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None
+    if bytes_in + bytes_out < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        hq.hq_rot_amax(x, group, amax=amax, stream=stream)
+        hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(device_uuid(dev))
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    t_start.record(stream)
+    for i in range(K):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        hq.hq_rot_amax(x, group, amax=amax, stream=stream)
+        e1.record(stream)
+        hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
+        e2.record(stream)
+        if flush is not None:
+            flush.fill_(1.0)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    pass1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    pass2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    region_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        # steps are timed launch to launch; the L2 flush between them is not part of a step
+        region_ms = sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(K))
+    step_ms = region_ms / K
+    if pg:
+        t = torch.tensor([region_ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        region_ms = float(t.item())
+    value = step_bytes * K * world / (region_ms / 1e3) / 1e9
+
+    # ---- end to end through the public API, host buffers ----
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
+    hqz = hq.HostQuantizer(w.M, w.K, x.dtype, group, device=dev, stream=stream)
+    for _ in range(max(3, min(args.warmup, 10))):
+        hqz.enqueue(x_host)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        hqz.enqueue(x_host)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = step_bytes * e2e_steps * world / (e2e_ms / 1e3) / 1e9
+
+    # ---- roofline of the dominant kernel (pass 2) ----
+    peak, peak_kind = load_peaks()
+    p2 = sum(pass2) / K
+    p1 = sum(pass1) / K
+    achieved = step_bytes / (p2 / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get((src_hash, w.name, group))
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": "k_rotate_quant_nvfp4",
+                "peak_source": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.describe(), "M": w.M, "K": w.K, "input_dtype": w.dtype,
+                   "group": group, "bytes_per_step": step_bytes,
+                   "l2": ("inputs larger than L2, no flush" if flush is None
+                          else "L2 flushed between steps (256 MB write, outside the step time)"),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "passes": {"pass1_ms": p1, "pass2_ms": p2,
+                   "pass1_gbs_read": bytes_in / (p1 / 1e3) / 1e9,
+                   "pass2_gbs": achieved,
+                   "pass2_frac_of_nominal_8000": achieved / 8000.0},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": hqz.h2d_bytes,
+                "d2h_bytes_per_step": hqz.d2h_bytes, "steps": e2e_steps,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "kernel_source": src_hash,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = min(w.M, max(1, (8192 * 28672) // w.K))
+        nbytes, times, threads = oracle_sample_run(w, rows, reps=2)
+        line["cpu_baseline"] = {
+            "value": nbytes * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of {w.name} ({rows}x{w.K}), both passes, 2 timed runs"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from hadamard_rotation_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

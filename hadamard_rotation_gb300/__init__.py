@@ -1,1 +1,24 @@
-"""Fused Hadamard rotation + NVFP4 quantization for GB300 (sm_103a)."""
+"""Fused Hadamard rotation + NVFP4 quantization for GB300 (sm_103a).
+
+The compute path is libhq.so (hand-written CUDA, C ABI in include/hq.h); this package
+is its Python binding.  ``synth`` draws the seeded synthetic activations.
+"""
+from ._lib import HQError, lib_path, load  # noqa: F401
+from .api import (  # noqa: F401
+    HostQuantizer,
+    hq_dequant_nvfp4,
+    hq_rot_amax,
+    hq_rotate_quant_nvfp4,
+    quantize_nvfp4,
+)
+
+__all__ = [
+    "HQError",
+    "HostQuantizer",
+    "hq_dequant_nvfp4",
+    "hq_rot_amax",
+    "hq_rotate_quant_nvfp4",
+    "lib_path",
+    "load",
+    "quantize_nvfp4",
+]

@@ -1,0 +1,254 @@
+// hq.cu -- C ABI of libhq (declared in include/hq.h) and the launch logic.
+//
+// Every entry point validates its arguments on the host, picks the kernel
+// instance for (rotation group, element type, contiguous/strided rows), sizes a
+// persistent grid (resident CTAs per SM x SM count, capped by the work), and
+// enqueues on the caller's stream.  Nothing here allocates, synchronises or
+// waits on the device.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "hq.h"
+#include "hq_kernels.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+hq_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return HQ_ERR_CUDA;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size(hq_dtype dt) { return dt == HQ_BF16 ? 2 : 4; }
+
+// Divider constants for hq::fast_div (Granlund & Montgomery 1994, Figure 4.1).
+hq::FastDiv make_fast_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+  hq::FastDiv f;
+  f.m = static_cast<uint32_t>(m);
+  f.s1 = l ? 1u : 0u;
+  f.s2 = l ? l - 1 : 0u;
+  return f;
+}
+
+// Resident CTAs per SM for a kernel, and the SM count, cached per device.
+struct GridCache {
+  std::mutex mu;
+  static constexpr int kSlots = 128;
+  const void* fn[kSlots] = {};
+  int dev[kSlots] = {};
+  int ctas[kSlots] = {};
+  int n = 0;
+  int sms[64] = {};
+};
+GridCache g_grid;
+
+cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, unsigned* grid) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0, sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_grid.mu);
+    for (int i = 0; i < g_grid.n; ++i)
+      if (g_grid.fn[i] == fn && g_grid.dev[i] == dev) per_sm = g_grid.ctas[i];
+    if (dev >= 0 && dev < 64) sms = g_grid.sms[dev];
+  }
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_grid.mu);
+    if (dev >= 0 && dev < 64) g_grid.sms[dev] = sms;
+  }
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, hq::kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    std::lock_guard<std::mutex> lock(g_grid.mu);
+    if (g_grid.n < GridCache::kSlots) {
+      g_grid.fn[g_grid.n] = fn;
+      g_grid.dev[g_grid.n] = dev;
+      g_grid.ctas[g_grid.n] = per_sm;
+      ++g_grid.n;
+    }
+  }
+  const uint64_t want = (n_tiles + hq::kWarpsPerCta - 1) / hq::kWarpsPerCta;
+  const uint64_t cap = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+  *grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (*grid == 0) *grid = 1;
+  return cudaSuccess;
+}
+
+template <typename Kernel>
+hq_status launch(Kernel kernel, const hq::Params& p, hq_stream stream) {
+  unsigned grid = 0;
+  cudaError_t e = persistent_grid(reinterpret_cast<const void*>(kernel), p.n_tiles, &grid);
+  if (e != cudaSuccess) return cuda_fail(e);
+  kernel<<<grid, hq::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HQ_OK;
+}
+
+// Shape checks shared by the two quantization passes.
+// An empty tensor (M == 0 or K == 0) may come with NULL data pointers.
+hq_status check_x(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx, int group) {
+  if (dt != HQ_F32 && dt != HQ_BF16) return HQ_ERR_DTYPE;
+  if (group != 0 && group != 16 && group != 256) return HQ_ERR_GROUP;
+  if (M < 0 || K < 0 || ldx < K) return HQ_ERR_SHAPE;
+  const int64_t unit = group > 16 ? group : 16;
+  if (K % unit != 0) return HQ_ERR_SHAPE;
+  if (K > 0 && M > INT64_MAX / K) return HQ_ERR_SHAPE;
+  const int64_t es = elem_size(dt);
+  if (ldx > INT64_MAX / es) return HQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!x) return HQ_ERR_NULL;
+  if (!aligned(x, 16)) return HQ_ERR_ALIGN;
+  if (M > 1 && (ldx * es) % 16 != 0) return HQ_ERR_ALIGN;
+  return HQ_OK;
+}
+
+hq::Params base_params(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx) {
+  hq::Params p = {};
+  p.x = static_cast<const uint8_t*>(x);
+  p.ldx_bytes = ldx * elem_size(dt);
+  p.nb = static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 16);
+  p.nbr = static_cast<uint32_t>(K / 16 > 0xFFFFFFFFll ? 0xFFFFFFFFu : K / 16);
+  if (p.nbr > 0) p.div_nbr = make_fast_div(p.nbr);
+  p.n_tiles = (p.nb + hq::kTileBlocks - 1) / hq::kTileBlocks;
+  return p;
+}
+
+// Rows are read as a flat array when they are back to back.
+bool is_strided(int64_t M, int64_t K, int64_t ldx) { return M > 1 && ldx != K; }
+
+template <int G>
+hq_status dispatch_rot_amax(const hq::Params& p, bool bf16, bool strided, bool write_y,
+                            hq_stream s) {
+  using namespace hq;
+  if (bf16) {
+    if (strided)
+      return write_y ? launch(k_rot_amax<G, true, true, true>, p, s)
+                     : launch(k_rot_amax<G, true, true, false>, p, s);
+    return write_y ? launch(k_rot_amax<G, true, false, true>, p, s)
+                   : launch(k_rot_amax<G, true, false, false>, p, s);
+  }
+  if (strided)
+    return write_y ? launch(k_rot_amax<G, false, true, true>, p, s)
+                   : launch(k_rot_amax<G, false, true, false>, p, s);
+  return write_y ? launch(k_rot_amax<G, false, false, true>, p, s)
+                 : launch(k_rot_amax<G, false, false, false>, p, s);
+}
+
+template <int G>
+hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream s) {
+  using namespace hq;
+  if (bf16)
+    return strided ? launch(k_rotate_quant_nvfp4<G, true, true>, p, s)
+                   : launch(k_rotate_quant_nvfp4<G, true, false>, p, s);
+  return strided ? launch(k_rotate_quant_nvfp4<G, false, true>, p, s)
+                 : launch(k_rotate_quant_nvfp4<G, false, false>, p, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                      int group, float* amax, float* y, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (!amax) return HQ_ERR_NULL;
+  if (!aligned(amax, 4) || (y && !aligned(y, 16))) return HQ_ERR_ALIGN;
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (M == 0 || K == 0) return HQ_OK;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.amax_out = amax;
+  p.y = y;
+  const bool bf16 = dtype == HQ_BF16;
+  const bool strided = is_strided(M, K, ldx);
+  switch (group) {
+    case 0: return dispatch_rot_amax<0>(p, bf16, strided, y != nullptr, stream);
+    case 16: return dispatch_rot_amax<16>(p, bf16, strided, y != nullptr, stream);
+    default: return dispatch_rot_amax<256>(p, bf16, strided, y != nullptr, stream);
+  }
+}
+
+hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                int64_t ldx, int group, const float* amax, uint8_t* q,
+                                uint8_t* scales, float* s_global, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!amax || !q || !scales) return HQ_ERR_NULL;
+  if (!aligned(amax, 4) || !aligned(q, 16) || !aligned(scales, 4) ||
+      (s_global && !aligned(s_global, 4)))
+    return HQ_ERR_ALIGN;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.amax_in = amax;
+  p.q = q;
+  p.s = scales;
+  p.sglobal_out = s_global;
+  const bool bf16 = dtype == HQ_BF16;
+  const bool strided = is_strided(M, K, ldx);
+  switch (group) {
+    case 0: return dispatch_quant<0>(p, bf16, strided, stream);
+    case 16: return dispatch_quant<16>(p, bf16, strided, stream);
+    default: return dispatch_quant<256>(p, bf16, strided, stream);
+  }
+}
+
+hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float* s_global,
+                           int64_t M, int64_t K, int group, int unrotate, float* out,
+                           hq_stream stream) {
+  if (unrotate && group != 16 && group != 256) return HQ_ERR_GROUP;
+  if (!unrotate && group != 0 && group != 16 && group != 256) return HQ_ERR_GROUP;
+  if (M < 0 || K < 0) return HQ_ERR_SHAPE;
+  const int64_t unit = (unrotate && group > 16) ? group : 16;
+  if (K % unit != 0) return HQ_ERR_SHAPE;
+  if (K > 0 && M > INT64_MAX / K) return HQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!q || !scales || !s_global || !out) return HQ_ERR_NULL;
+  if (!aligned(q, 8) || !aligned(s_global, 4) || !aligned(out, 16)) return HQ_ERR_ALIGN;
+  hq::Params p = {};
+  p.nb = static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 16);
+  p.n_tiles = (p.nb + hq::kTileBlocks - 1) / hq::kTileBlocks;
+  p.dq_q = q;
+  p.dq_s = scales;
+  p.dq_sglobal = s_global;
+  p.dq_out = out;
+  const int g = unrotate ? group : 0;
+  switch (g) {
+    case 0: return launch(hq::k_dequant_nvfp4<0>, p, stream);
+    case 16: return launch(hq::k_dequant_nvfp4<16>, p, stream);
+    default: return launch(hq::k_dequant_nvfp4<256>, p, stream);
+  }
+}
+
+const char* hq_status_string(hq_status status) {
+  switch (status) {
+    case HQ_OK: return "HQ_OK";
+    case HQ_ERR_NULL: return "HQ_ERR_NULL: a required pointer is NULL";
+    case HQ_ERR_SHAPE: return "HQ_ERR_SHAPE: bad M, K or ldx";
+    case HQ_ERR_ALIGN: return "HQ_ERR_ALIGN: pointer or row stride misaligned";
+    case HQ_ERR_DTYPE: return "HQ_ERR_DTYPE: unknown element type";
+    case HQ_ERR_GROUP: return "HQ_ERR_GROUP: rotation group must be 0, 16 or 256";
+    case HQ_ERR_CUDA: return "HQ_ERR_CUDA: CUDA runtime error";
+  }
+  return "unknown hq_status";
+}
+
+int hq_last_cuda_error(void) { return g_last_cuda_error; }
+
+int hq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+/*
+ * hq.h -- C ABI of libhq: fused Hadamard rotation + NVFP4 quantization on GB300 (sm_103a).
+ *
+ * What is computed ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §1 "The format,
+ * precisely" and §2 "The kernel"; storage layout from "NVFP4 Quantization" (Atlas docs),
+ * "The numeric format"):
+ *
+ *   x       : M x K activations, row-major, row stride ldx elements (ldx >= K).
+ *   rotation: every run of G consecutive elements of a row is multiplied by the
+ *             Sylvester-Hadamard matrix H_G scaled by 1/sqrt(G):  y = x . H_G / sqrt(G).
+ *             G = 16, G = 256 (= H16 (x) H16, scaled by 1/16), or G = 0 (rotation off: y = x).
+ *             Computed as a fixed-order fp32 butterfly: stages h = 1, 2, 4, ..., G/2, each
+ *             (a, b) -> (a + b, a - b), then one multiply by 1/sqrt(G).
+ *   amax    : max |y| over the whole tensor (exact).
+ *   s_global: amax / (448 * 6) in one fp32 division; 1.0 if that quotient is 0.
+ *   blocks  : every 16 consecutive elements of a row of y form one NVFP4 block.
+ *   s_block : E4M3 (float8 e4m3fn) value nearest to (block_amax / 6) / s_global, ties to even,
+ *             saturating at 448.  Stored as its 8-bit pattern.
+ *   codes   : s_f = s_block * s_global; if s_f == 0 every code of the block is 0, otherwise
+ *             code = E2M1 value nearest to y / s_f (IEEE fp32 division), grid
+ *             {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code, saturating at 6; bit 3 copies
+ *             the sign bit of the quotient (so -0.0 encodes as 0x8).
+ *   packing : q[r][j] = code[r][2j] | (code[r][2j+1] << 4)   (even element in the low nibble).
+ *
+ * Layouts (all row-major, contiguous, owned by the caller):
+ *   q       : uint8 [M, K/2]
+ *   scales  : uint8 [M, K/16]  (E4M3 bit patterns)
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller.  The library allocates no memory,
+ *     creates no stream and never synchronises the host; all work is enqueued on `stream`
+ *     (a cudaStream_t / CUstream of the current device; NULL = the legacy default stream).
+ *   - Argument errors are detected on the host before anything is enqueued and are returned
+ *     synchronously; nothing is launched in that case.
+ *   - A failed launch returns HQ_ERR_CUDA; hq_last_cuda_error() then gives the cudaError_t.
+ *   - An empty tensor (M == 0 or K == 0, with valid sizes) is a no-op that returns HQ_OK; its
+ *     data pointers may be NULL.  hq_rot_amax still writes 0 to `amax`, which must be valid.
+ *   - Non-finite input is outside the contract.  hq_rot_amax reports it: a NaN anywhere gives
+ *     a NaN amax and an infinity gives +inf, which the caller can read back.  Codes and scales
+ *     for such tensors are unspecified.  Nothing traps or waits on the device.
+ *   - Sizes are 64-bit element counts.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HQ_OK = 0,
+  HQ_ERR_NULL = 1,  /* a required pointer is NULL */
+  HQ_ERR_SHAPE = 2, /* M < 0, K < 0, ldx < K, or K not a multiple of max(16, G) */
+  HQ_ERR_ALIGN = 3, /* a pointer or the row stride breaks the alignment rules below */
+  HQ_ERR_DTYPE = 4, /* unknown element type */
+  HQ_ERR_GROUP = 5, /* rotation group not in {0, 16, 256} */
+  HQ_ERR_CUDA = 6   /* the CUDA runtime refused a launch or an enqueue */
+} hq_status;
+
+typedef enum {
+  HQ_F32 = 0, /* IEEE binary32 */
+  HQ_BF16 = 1 /* bfloat16; widened to fp32 exactly */
+} hq_dtype;
+
+/* A cudaStream_t (CUstream) passed as a plain pointer. */
+typedef void* hq_stream;
+
+/*
+ * hq_rot_amax -- pass 1: rotate and reduce the global amax.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2, "The global scale is the one
+ *    thing not fused": the amax of the whole rotated tensor is needed before any block scale.)
+ *
+ *   x      : [M, K] of `dtype`, row stride ldx elements.  16-byte aligned; ldx * sizeof(dtype)
+ *            a multiple of 16 bytes.
+ *   group  : 0, 16 or 256.  K must be a multiple of max(16, group).
+ *   amax   : 1 float, overwritten with max |y| (this call zeroes it first, on `stream`).
+ *            4-byte aligned.
+ *   y      : optional fp32 [M, K] (row stride K), 16-byte aligned, receives the rotated tensor;
+ *            NULL to skip (the normal case: the rotation is never stored).
+ */
+hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                      int group, float* amax, float* y, hq_stream stream);
+
+/*
+ * hq_rotate_quant_nvfp4 -- pass 2: one read of x, one write of the codes and block scales.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §1 table and §2 kernel: rotate,
+ *    block amax, E4M3 scale, E2M1 codes, two codes per byte.)
+ *
+ *   x, dtype, M, K, ldx, group : as for hq_rot_amax.
+ *   amax     : 1 float on the device, the global amax of the rotated tensor (normally written by
+ *              hq_rot_amax on the same stream; any non-negative finite value is accepted, e.g.
+ *              an amax kept from an earlier step).
+ *   q        : uint8 [M, K/2], 16-byte aligned.
+ *   scales   : uint8 [M, K/16], 4-byte aligned.
+ *   s_global : optional 1 float, receives s_global (the per-tensor fp32 scale); NULL to skip.
+ */
+hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                int64_t ldx, int group, const float* amax, uint8_t* q,
+                                uint8_t* scales, float* s_global, hq_stream stream);
+
+/*
+ * hq_dequant_nvfp4 -- round trip for checks (not part of the quantization hot path).
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2 dequantize:
+ *    value = (+-grid[code & 7]) * (s_block * s_global), then the rotation applied again when the
+ *    data was rotated; H_G / sqrt(G) is symmetric and orthonormal, so it is its own inverse.)
+ *
+ *   q, scales : as written by hq_rotate_quant_nvfp4 (q 8-byte aligned).
+ *   s_global  : 1 float on the device.
+ *   group     : 0, 16 or 256; the rotation to undo when `unrotate` is non-zero (then 16 or 256,
+ *               and K a multiple of it); otherwise only checked.
+ *   out       : fp32 [M, K] (row stride K), 16-byte aligned.
+ *   The two products are rounded in that order (s_f first), then the butterfly as above.
+ */
+hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float* s_global,
+                           int64_t M, int64_t K, int group, int unrotate, float* out,
+                           hq_stream stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* hq_status_string(hq_status status);
+
+/* The cudaError_t behind the last HQ_ERR_CUDA returned on the calling host thread (0 if none). */
+int hq_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int hq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HQ_H_ */

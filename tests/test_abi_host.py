@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports every
+function include/hq.h declares, and rejects bad arguments synchronously, before any CUDA call.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hq.h")
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hadamard_rotation_gb300 import build
+    import hadamard_rotation_gb300 as hq
+
+    build.build()
+    return hq.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("hq_rot_amax", "hq_rotate_quant_nvfp4", "hq_dequant_nvfp4"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "hq.h"\nint main(void){ return (int)HQ_OK + (int)HQ_BF16; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c",
+                    str(src), "-o", str(tmp_path / "use.o")], check=True)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.hq_version() >= 100
+    for code in range(7):
+        assert lib.hq_status_string(code).decode().startswith("HQ_")
+    assert b"unknown" in lib.hq_status_string(99)
+    assert lib.hq_last_cuda_error() == 0
+
+
+P = ctypes.c_void_p
+
+
+def rq(lib, x=FAKE, dt=1, M=4, K=32, ldx=32, G=16, amax=FAKE, q=FAKE, s=FAKE, sg=None):
+    return lib.hq_rotate_quant_nvfp4(P(x) if x else None, dt, M, K, ldx, G, P(amax) if amax else None,
+                                     P(q) if q else None, P(s) if s else None,
+                                     P(sg) if sg else None, None)
+
+
+def ra(lib, x=FAKE, dt=1, M=4, K=32, ldx=32, G=16, amax=FAKE, y=None):
+    return lib.hq_rot_amax(P(x) if x else None, dt, M, K, ldx, G, P(amax) if amax else None,
+                           P(y) if y else None, None)
+
+
+def dq(lib, q=FAKE, s=FAKE, sg=FAKE, M=4, K=32, G=16, un=1, out=FAKE):
+    return lib.hq_dequant_nvfp4(P(q) if q else None, P(s) if s else None, P(sg) if sg else None,
+                                M, K, G, un, P(out) if out else None, None)
+
+
+def test_null_pointers(lib):
+    assert rq(lib, x=0) == 1 and rq(lib, amax=0) == 1 and rq(lib, q=0) == 1 and rq(lib, s=0) == 1
+    assert ra(lib, x=0) == 1 and ra(lib, amax=0) == 1
+    assert dq(lib, q=0) == 1 and dq(lib, s=0) == 1 and dq(lib, sg=0) == 1 and dq(lib, out=0) == 1
+
+
+def test_bad_shapes(lib):
+    assert rq(lib, K=24, ldx=24) == 2            # K not a multiple of 16
+    assert rq(lib, K=272, ldx=272, G=256) == 2   # K not a multiple of 256
+    assert rq(lib, M=-1) == 2
+    assert rq(lib, K=-16) == 2
+    assert rq(lib, ldx=16) == 2                  # ldx < K
+    assert rq(lib, M=2 ** 62, K=64, ldx=64) == 2  # M*K overflows
+    assert ra(lib, K=48, ldx=48, G=256) == 2
+    assert dq(lib, K=24) == 2
+    assert dq(lib, K=272, G=256) == 2
+    assert dq(lib, M=-3) == 2
+
+
+def test_bad_group_and_dtype(lib):
+    for G in (1, 8, 32, 64, 128, 512, -16):
+        assert rq(lib, G=G) == 5 and ra(lib, G=G) == 5
+    assert dq(lib, G=0, un=1) == 5
+    assert dq(lib, G=32, un=0) == 5
+    assert rq(lib, dt=2) == 4 and ra(lib, dt=-1) == 4
+
+
+def test_alignment(lib):
+    assert rq(lib, x=FAKE + 2) == 3
+    assert rq(lib, dt=1, ldx=36) == 3            # 72 B row stride: not a multiple of 16
+    assert rq(lib, dt=0, ldx=34) == 3            # 136 B row stride
+    assert rq(lib, q=FAKE + 8) == 3
+    assert rq(lib, s=FAKE + 2) == 3
+    assert rq(lib, amax=FAKE + 2) == 3
+    assert rq(lib, sg=FAKE + 1) == 3
+    assert ra(lib, y=FAKE + 4) == 3
+    assert dq(lib, out=FAKE + 8) == 3
+    assert dq(lib, q=FAKE + 4) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a CUDA device")
+def test_valid_arguments_without_a_device_report_cuda_error(lib):
+    # Arguments pass validation, so the call reaches the CUDA runtime, which has no device.
+    assert ra(lib) == 6
+    assert lib.hq_last_cuda_error() != 0
+
+
+def test_empty_quantize_is_a_noop(lib):
+    # M == 0: valid, nothing to enqueue (no CUDA call is made for pass 2 or dequant).
+    assert rq(lib, M=0) == 0
+    assert dq(lib, M=0) == 0
+
+
+def test_binding_rejects_host_tensors():
+    import hadamard_rotation_gb300 as hq
+
+    x = torch.zeros(4, 32, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        hq.hq_rot_amax(x, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        hq.hq_rotate_quant_nvfp4(x, 16, torch.zeros(1))

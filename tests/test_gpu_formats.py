@@ -1,0 +1,120 @@
+"""The GPU's two roundings, driven through the public quantizer (rotation off, so y = x):
+
+* E2M1: every fp32 quotient in [1/8, 6.375], both signs (~94 million values), plus signed
+  zeros and subnormals.  Each block is [6.375, t1 .. t15] and one row holds 2688, so
+  s_global = 2688 / 2688 = 1 and the block scale is E4M3(6.375 / 6 = 1.0625) = 1.0 (a tie,
+  to the even mantissa), which makes every quotient equal to t exactly.
+* E4M3: blocks [6 v, 0 ...] for every E4M3 value v, every midpoint between neighbours and
+  the fp32 values next to each midpoint, plus random v; with s_global = 1 the block scale is
+  E4M3(v).
+
+Expected bytes come from the CPU oracle, whose roundings are pinned exhaustively by the
+"not gpu" tests.  Sources: "A Fused Hadamard + NVFP4 Quantization Kernel in Triton" §1
+(format table), §2 (_e2m1_code ties to the even code, E4M3 clamp 448), §3 (RNE float8 cast).
+"""
+import numpy as np
+import pytest
+import torch
+
+import hadamard_rotation_gb300 as hq
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+K = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from hadamard_rotation_gb300 import build
+
+    build.build()
+    oracle.build()
+    hq.load()
+
+
+def f32_bits(v: float) -> int:
+    return int(np.array([v], np.float32).view(np.uint32)[0])
+
+
+def blocks_tensor(first_elems: np.ndarray, rest: np.ndarray, per_block: int) -> np.ndarray:
+    """Row 0 = [2688, 0, ...]; then blocks [first_elems[b], rest[b*per_block : ...], 0 ...]."""
+    nblk = first_elems.size
+    blk = np.zeros((nblk, 16), np.float32)
+    blk[:, 0] = first_elems
+    if per_block:
+        pad = np.zeros(nblk * per_block, np.float32)
+        pad[: rest.size] = rest
+        blk[:, 1:1 + per_block] = pad.reshape(nblk, per_block)
+    per_row = K // 16
+    rows = (nblk + per_row - 1) // per_row
+    body = np.zeros((rows * per_row, 16), np.float32)
+    body[:nblk] = blk
+    x = np.zeros((rows + 1, K), np.float32)
+    x[0, 0] = 2688.0
+    x[1:] = body.reshape(rows, K)
+    return x
+
+
+def run_both(x: np.ndarray):
+    xt = torch.from_numpy(x).cuda()
+    amax = hq.hq_rot_amax(xt, 0)
+    q, s, sg = hq.hq_rotate_quant_nvfp4(xt, 0, amax)
+    torch.cuda.synchronize()
+    oq, os_, oamax, osg = oracle.quantize(x, 0)
+    assert amax.item() == oamax == 2688.0 and sg.item() == osg == 1.0
+    return q.cpu().numpy(), s.cpu().numpy(), oq, os_
+
+
+def compare(name, g, o):
+    if not np.array_equal(g, o):
+        bad = np.argwhere(g != o)[:5]
+        raise AssertionError(f"{name}: {int((g != o).sum())} differ, first {bad.tolist()}")
+
+
+def test_e2m1_every_quotient_in_range():
+    lo, hi = f32_bits(0.125), f32_bits(6.375)
+    t = np.arange(lo, hi + 1, dtype=np.uint32).view(np.float32)
+    t = np.concatenate([t, -t])
+    n = (t.size + 14) // 15
+    x = blocks_tensor(np.full(n, 6.375, np.float32), t, 15)
+    gq, gs, oq, os_ = run_both(x)
+    assert (os_[1:].reshape(-1)[:n] == 0x38).all()      # every block scale is exactly 1.0
+    compare("scales", gs, os_)
+    compare("codes", gq, oq)
+
+
+def test_e2m1_signed_zeros_and_subnormal_quotients():
+    t = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-40, -1e-40, 1.1754942e-38, -1.1754942e-38,
+                  1e-10, -1e-10, 0.1, -0.1, 0.25, -0.25, 0.2500001, -0.2500001], np.float32)
+    x = blocks_tensor(np.full(2, 6.375, np.float32), np.concatenate([t[:15], t[15:]]), 15)
+    gq, gs, oq, os_ = run_both(x)
+    compare("scales", gs, os_)
+    compare("codes", gq, oq)
+    codes = np.stack([oq[1] & 0xF, oq[1] >> 4], -1).reshape(-1)[:32]
+    # block 0: [anchor 6.375 -> 7, +0 -> 0, -0 -> 8, 1e-45 -> 0, -1e-45 -> 8, ...]
+    assert codes[:5].tolist() == [7, 0, 8, 0, 8]
+
+
+def e4m3_table():
+    c = np.arange(127)
+    ef, m = c >> 3, c & 7
+    return np.where(ef == 0, m * 2.0 ** -9, (1 + m / 8.0) * 2.0 ** (ef - 7))
+
+
+def test_e4m3_every_value_and_midpoint():
+    table = e4m3_table()
+    mids = ((table[:-1] + table[1:]) / 2).astype(np.float32)
+    v = np.concatenate([
+        table.astype(np.float32), mids,
+        np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+        np.array([2.0 ** -11, 2.0 ** -10, 3 * 2.0 ** -10, 446, 447.99, 448], np.float32),
+        (np.random.default_rng(1).random(100_000) * 448).astype(np.float32),
+        np.exp2(np.random.default_rng(2).uniform(-16, 8.8, 100_000)).astype(np.float32),
+    ])
+    v = v[v * 6 <= 2688]
+    first = (v.astype(np.float64) * 6).astype(np.float32)
+    x = blocks_tensor(first, np.zeros(0, np.float32), 0)
+    gq, gs, oq, os_ = run_both(x)
+    compare("scales", gs, os_)
+    compare("codes", gq, oq)

@@ -1,0 +1,232 @@
+"""GPU vs CPU oracle, through the C ABI.  Codes, scales, amax, s_global and dequantized
+values must be bit-exact; the exposed rotated tensor y must be too (the contract allows 1e-6
+relative; the butterfly order is the same, so it is exact).
+
+Workloads are the five named activation tensors (synth.WORKLOADS) at full size, run with the
+same entry points and launch configuration as bench.py, plus edge cases: a single block, ragged
+tiles, strided rows, all-zero and underflowing tensors, extreme magnitudes (the kernel's exact
+slow path), non-finite input, another stream, and tiling invariance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hadamard_rotation_gb300 as hq
+import oracle
+from hadamard_rotation_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from hadamard_rotation_gb300 import build
+
+    build.build()
+    oracle.build()
+    hq.load()
+
+
+def f32_bits(a) -> np.ndarray:
+    return np.asarray(a, np.float32).view(np.uint32)
+
+
+def first_diffs(a: np.ndarray, b: np.ndarray, n=5):
+    idx = np.argwhere(a != b)[:n]
+    return [(tuple(i), int(a[tuple(i)]), int(b[tuple(i)])) for i in idx]
+
+
+def assert_bytes_equal(name, gpu: np.ndarray, ref: np.ndarray):
+    assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
+    if not np.array_equal(gpu, ref):
+        bad = int(np.count_nonzero(gpu != ref))
+        raise AssertionError(f"{name}: {bad} of {gpu.size} differ; first: {first_diffs(gpu, ref)}")
+
+
+def gpu_quantize(x_host: torch.Tensor, group: int, want_y=False, stream=None, x_dev=None):
+    x = x_dev if x_dev is not None else x_host.cuda()
+    y = torch.empty(x.shape, dtype=torch.float32, device=x.device) if want_y else None
+    amax = hq.hq_rot_amax(x, group, y=y, stream=stream)
+    q, s, sg = hq.hq_rotate_quant_nvfp4(x, group, amax, stream=stream)
+    torch.cuda.synchronize()
+    out = dict(q=q.cpu().numpy(), s=s.cpu().numpy(), amax=amax.cpu().numpy(), sg=sg.cpu().numpy())
+    if want_y:
+        out["y"] = y.cpu().numpy()
+    out["_dev"] = (q, s, sg)
+    return out
+
+
+def check_against_oracle(x_host: torch.Tensor, group: int, want_y=False, x_dev=None, label=""):
+    g = gpu_quantize(x_host, group, want_y=want_y, x_dev=x_dev)
+    xo = synth.as_oracle_array(x_host)
+    oq, os_, oamax, osg = oracle.quantize(xo, group)
+    tag = f"{label} group={group}"
+    assert f32_bits(g["amax"])[0] == f32_bits([oamax])[0], (tag, g["amax"], oamax)
+    assert f32_bits(g["sg"])[0] == f32_bits([osg])[0], (tag, g["sg"], osg)
+    assert_bytes_equal(f"{tag} scales", g["s"], os_)
+    assert_bytes_equal(f"{tag} codes", g["q"], oq)
+    if want_y:
+        _, oy = oracle.rot_amax(xo, group, want_y=True)
+        assert_bytes_equal(f"{tag} y", f32_bits(g["y"]), f32_bits(oy))
+    return g, (oq, os_, oamax, osg)
+
+
+# ---------------------------------------------------------------- the named workloads ------
+
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_workload_parity(name):
+    w = synth.WORKLOADS[name]
+    x_host = synth.generate(w)
+    x_dev = x_host.cuda()
+    for group in w.groups:
+        g, (oq, os_, oamax, osg) = check_against_oracle(x_host, group, x_dev=x_dev, label=name)
+        if w.roundtrip:
+            q, s, sg = g["_dev"]
+            back = hq.hq_dequant_nvfp4(q, s, sg, group, unrotate=True)
+            torch.cuda.synchronize()
+            ref = oracle.dequant(oq, os_, osg, group, True)
+            assert_bytes_equal(f"{name} dequant", f32_bits(back.cpu().numpy()), f32_bits(ref))
+        del g
+    if w.zero_rows:
+        g = gpu_quantize(x_host, w.groups[0], x_dev=x_dev)
+        assert not g["s"][: w.zero_rows].any() and not g["q"][: w.zero_rows].any()
+
+
+# ---------------------------------------------------------------- shapes and edge cases ----
+
+def rand_input(M, K, dtype, seed, outliers=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    if outliers and K >= 16:
+        cols = rng.choice(K, max(1, K // 64), replace=False)
+        x[:, cols] *= 30.0
+    if M > 3:
+        x[2] = 0.0
+    t = torch.from_numpy(x)
+    return t if dtype == torch.float32 else t.to(dtype)
+
+
+SHAPES = [
+    (1, 16, 0), (1, 16, 16), (2, 256, 256), (17, 48, 16), (3, 272, 16), (129, 256, 256),
+    (5, 768, 256), (1000, 272, 0), (257, 1024, 16), (31, 4096, 256), (4099, 96, 16),
+]
+
+
+@pytest.mark.parametrize("M,K,group", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_shapes_and_ragged_tails(M, K, group, dtype):
+    x = rand_input(M, K, dtype, seed=M * 7 + K + group)
+    check_against_oracle(x, group, want_y=True, label=f"{M}x{K}")
+
+
+@pytest.mark.parametrize("group", [0, 16, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_strided_rows(group, dtype):
+    big = rand_input(300, 1024 + 256, dtype, seed=11)
+    x_dev = big.cuda()[:, :1024]
+    assert x_dev.stride(0) == 1280
+    view_host = big[:, :1024].contiguous()
+    check_against_oracle(view_host, group, x_dev=x_dev, label="strided")
+    # strided device input, strided host input to the oracle: both agree with contiguous
+    g1 = gpu_quantize(view_host, group)
+    g2 = gpu_quantize(view_host, group, x_dev=x_dev)
+    assert_bytes_equal("strided vs contiguous codes", g2["q"], g1["q"])
+
+
+@pytest.mark.parametrize("group", [0, 16, 256])
+def test_dequant_parity(group):
+    x = rand_input(64, 512, torch.float32, seed=5)
+    for unrotate in ([False, True] if group else [False]):
+        g, (oq, os_, oamax, osg) = check_against_oracle(x, group)
+        q, s, sg = g["_dev"]
+        back = hq.hq_dequant_nvfp4(q, s, sg, group if group else 16, unrotate=unrotate)
+        torch.cuda.synchronize()
+        ref = oracle.dequant(oq, os_, osg, group, unrotate)
+        assert_bytes_equal(f"dequant g={group} un={unrotate}", f32_bits(back.cpu().numpy()), f32_bits(ref))
+
+
+@pytest.mark.parametrize("scale_exp", [-140, -125, -100, -60, 60, 100, 110])
+@pytest.mark.parametrize("group", [0, 16, 256])
+def test_extreme_magnitudes_use_exact_path(scale_exp, group):
+    """Tensors scaled far from 1: s_f leaves the fast division domain (or y becomes subnormal),
+    so the kernel takes its literal-division path; results must still equal the oracle."""
+    x = rand_input(40, 512, torch.float32, seed=abs(scale_exp) + group)
+    x = (x.double() * 2.0 ** scale_exp).float()
+    x[7, :16] = torch.tensor(np.float32(2.0 ** scale_exp) * np.arange(16, dtype=np.float32) * 1e-3)
+    check_against_oracle(x, group, want_y=True, label=f"2^{scale_exp}")
+
+
+def test_mixed_magnitudes_in_one_tensor():
+    """Blocks of very different size in one tensor: tiny blocks get zero or subnormal scales."""
+    x = rand_input(64, 1024, torch.float32, seed=3)
+    x[10:20] *= 1e-30
+    x[20:30] *= 1e-38
+    x[30, 5] = 3.0e38
+    for group in (0, 16, 256):
+        check_against_oracle(x, group, label="mixed")
+
+
+def test_zero_and_underflowing_tensors():
+    for x in (torch.zeros(8, 64), torch.full((8, 64), 1e-44), -torch.zeros(8, 64)):
+        for group in (0, 16):
+            g, _ = check_against_oracle(x, group, label="zero")
+            assert g["sg"][0] == 1.0
+            assert not g["q"].any() and not g["s"].any()
+
+
+def test_nonfinite_input_surfaces_in_amax():
+    x = torch.ones(64, 256, device="cuda")
+    x[33, 7] = float("inf")
+    for group in (0, 16, 256):
+        assert torch.isinf(hq.hq_rot_amax(x, group)).item()
+    x[12, 200] = float("nan")
+    for group in (0, 16, 256):
+        assert torch.isnan(hq.hq_rot_amax(x, group)).item()
+
+
+def test_empty_tensor():
+    x = torch.empty(0, 64, device="cuda", dtype=torch.bfloat16)
+    amax = hq.hq_rot_amax(x, 16)
+    q, s, sg = hq.hq_rotate_quant_nvfp4(x, 16, amax)
+    torch.cuda.synchronize()
+    assert amax.item() == 0.0 and q.numel() == 0 and s.numel() == 0
+
+
+def test_other_stream_and_repeat_calls():
+    x_host = rand_input(512, 2048, torch.bfloat16, seed=9)
+    ref = gpu_quantize(x_host, 16)
+    s = torch.cuda.Stream()
+    x = x_host.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            amax = hq.hq_rot_amax(x, 16, stream=s)
+            q, sc, sg = hq.hq_rotate_quant_nvfp4(x, 16, amax, stream=s)
+    s.synchronize()
+    assert_bytes_equal("stream codes", q.cpu().numpy(), ref["q"])
+    assert_bytes_equal("stream scales", sc.cpu().numpy(), ref["s"])
+
+
+def test_tiling_invariance():
+    """A row's codes do not depend on which tile, warp or CTA handled it: quantizing a slice of
+    rows with the full tensor's amax reproduces those rows of the full result."""
+    x_host = rand_input(3000, 768, torch.bfloat16, seed=21)
+    x = x_host.cuda()
+    for group in (0, 16, 256):
+        amax = hq.hq_rot_amax(x, group)
+        q, s, _ = hq.hq_rotate_quant_nvfp4(x, group, amax)
+        for r0, r1 in ((0, 1), (5, 6), (123, 1187), (2999, 3000)):
+            qs, ss, _ = hq.hq_rotate_quant_nvfp4(x[r0:r1], group, amax)
+            torch.cuda.synchronize()
+            assert torch.equal(qs, q[r0:r1]) and torch.equal(ss, s[r0:r1])
+
+
+def test_host_quantizer_matches_device_path():
+    w = synth.WORKLOADS["bf16_4096x4096"]
+    x_host = synth.generate(w).pin_memory()
+    hqz = hq.HostQuantizer(w.M, w.K, torch.bfloat16, 16)
+    qh, sh, sg = hqz(x_host)
+    oq, os_, oamax, osg = oracle.quantize(synth.as_oracle_array(x_host), 16)
+    assert_bytes_equal("host codes", qh.numpy(), oq)
+    assert_bytes_equal("host scales", sh.numpy(), os_)
+    assert np.float32(sg) == osg
