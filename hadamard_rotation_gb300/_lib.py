@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.hq_status_string.restype = ctypes.c_char_p
         lib.hq_last_cuda_error.argtypes = []
         lib.hq_last_cuda_error.restype = i32
+        lib.hq_read_fault.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+        lib.hq_read_fault.restype = i32
         lib.hq_version.argtypes = []
         lib.hq_version.restype = i32
         _lib = lib

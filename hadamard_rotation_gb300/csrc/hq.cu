@@ -51,7 +51,7 @@ struct GridCache {
 };
 GridCache g_grid;
 
-cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, unsigned* grid) {
+cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, size_t smem, unsigned* grid) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -69,7 +69,12 @@ cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, unsigned* grid) {
     if (dev >= 0 && dev < 64) g_grid.sms[dev] = sms;
   }
   if (per_sm == 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, hq::kThreads, 0);
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, hq::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     std::lock_guard<std::mutex> lock(g_grid.mu);
@@ -87,12 +92,14 @@ cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, unsigned* grid) {
   return cudaSuccess;
 }
 
+// Launch with `smem` bytes of dynamic shared memory (the TMA ring of the
+// contiguous-row kernels; 0 for the others).
 template <typename Kernel>
-hq_status launch(Kernel kernel, const hq::Params& p, hq_stream stream) {
+hq_status launch(Kernel kernel, const hq::Params& p, hq_stream stream, size_t smem = 0) {
   unsigned grid = 0;
-  cudaError_t e = persistent_grid(reinterpret_cast<const void*>(kernel), p.n_tiles, &grid);
+  cudaError_t e = persistent_grid(reinterpret_cast<const void*>(kernel), p.n_tiles, smem, &grid);
   if (e != cudaSuccess) return cuda_fail(e);
-  kernel<<<grid, hq::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  kernel<<<grid, hq::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return HQ_OK;
@@ -130,32 +137,50 @@ hq::Params base_params(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t
 // Rows are read as a flat array when they are back to back.
 bool is_strided(int64_t M, int64_t K, int64_t ldx) { return M > 1 && ldx != K; }
 
+// How contiguous rows are read (hq::LoadMode): through the per-warp TMA ring
+// (default) or with direct vector loads.
+#ifndef HQ_PASS1_MODE
+#define HQ_PASS1_MODE hq::kLoadTma
+#endif
+#ifndef HQ_PASS2_MODE
+#define HQ_PASS2_MODE hq::kLoadTma
+#endif
+
+template <int STAGES>
+size_t ring_bytes(int mode, bool bf16) {
+  if (mode != hq::kLoadTma) return 0;
+  return bf16 ? hq::Ring<true, STAGES>::kSmemBytes : hq::Ring<false, STAGES>::kSmemBytes;
+}
+
+template <int G, bool BF16, int MODE>
+hq_status launch_rot_amax(const hq::Params& p, bool write_y, hq_stream s) {
+  const size_t smem = ring_bytes<HQ_PASS1_STAGES>(MODE, BF16);
+  return write_y ? launch(hq::k_rot_amax<G, BF16, MODE, true>, p, s, smem)
+                 : launch(hq::k_rot_amax<G, BF16, MODE, false>, p, s, smem);
+}
+
 template <int G>
 hq_status dispatch_rot_amax(const hq::Params& p, bool bf16, bool strided, bool write_y,
                             hq_stream s) {
-  using namespace hq;
-  if (bf16) {
-    if (strided)
-      return write_y ? launch(k_rot_amax<G, true, true, true>, p, s)
-                     : launch(k_rot_amax<G, true, true, false>, p, s);
-    return write_y ? launch(k_rot_amax<G, true, false, true>, p, s)
-                   : launch(k_rot_amax<G, true, false, false>, p, s);
-  }
-  if (strided)
-    return write_y ? launch(k_rot_amax<G, false, true, true>, p, s)
-                   : launch(k_rot_amax<G, false, true, false>, p, s);
-  return write_y ? launch(k_rot_amax<G, false, false, true>, p, s)
-                 : launch(k_rot_amax<G, false, false, false>, p, s);
+  constexpr int kMode = HQ_PASS1_MODE;
+  if (bf16)
+    return strided ? launch_rot_amax<G, true, hq::kLoadStrided>(p, write_y, s)
+                   : launch_rot_amax<G, true, kMode>(p, write_y, s);
+  return strided ? launch_rot_amax<G, false, hq::kLoadStrided>(p, write_y, s)
+                 : launch_rot_amax<G, false, kMode>(p, write_y, s);
 }
 
 template <int G>
 hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream s) {
-  using namespace hq;
+  using hq::k_rotate_quant_nvfp4;
+  constexpr int kMode = HQ_PASS2_MODE;
   if (bf16)
-    return strided ? launch(k_rotate_quant_nvfp4<G, true, true>, p, s)
-                   : launch(k_rotate_quant_nvfp4<G, true, false>, p, s);
-  return strided ? launch(k_rotate_quant_nvfp4<G, false, true>, p, s)
-                 : launch(k_rotate_quant_nvfp4<G, false, false>, p, s);
+    return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided>, p, s)
+                   : launch(k_rotate_quant_nvfp4<G, true, kMode>, p, s,
+                            ring_bytes<HQ_PASS2_STAGES>(kMode, true));
+  return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided>, p, s)
+                 : launch(k_rotate_quant_nvfp4<G, false, kMode>, p, s,
+                          ring_bytes<HQ_PASS2_STAGES>(kMode, false));
 }
 
 }  // namespace
@@ -248,6 +273,20 @@ const char* hq_status_string(hq_status status) {
 }
 
 int hq_last_cuda_error(void) { return g_last_cuda_error; }
+
+hq_status hq_read_fault(unsigned int* fault, int clear) {
+  if (!fault) return HQ_ERR_NULL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpyFromSymbol(fault, g_hq_fault, sizeof(unsigned int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clear && *fault) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_hq_fault, &zero, sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return HQ_OK;
+}
 
 int hq_version(void) { return 100; }
 

@@ -9,17 +9,27 @@
 //                         E4M3 block scale, E2M1 codes, write codes + scales once.
 //   k_dequant_nvfp4       round trip: codes * scales, optional inverse rotation.
 //
-// Work decomposition (all three kernels): a warp owns a "tile" of 128 NVFP4
-// blocks (2048 elements); each lane holds 4 whole blocks (64 values) in
-// registers.  Which 4 blocks a lane holds depends on the rotation group:
-//   G <= 16 : block 32*j + lane of the tile (j = 0..3) -- each warp-wide memory
-//             instruction covers 32 consecutive blocks;
+// Work decomposition.  A warp owns a "tile" of 128 NVFP4 blocks (2048 elements,
+// 4 KB of bf16); each lane holds 4 whole blocks (64 values) in registers.  Which
+// 4 blocks a lane holds depends on the rotation group:
+//   G <= 16 : block 32*j + lane of the tile (j = 0..3);
 //   G == 256: block 16*(lane/4) + (lane%4) + 4*j -- the 4 lanes of a quad hold
 //             the 16 blocks of one 256-group; index bits 4,5 of the group are the
 //             lane bits, bits 6,7 select the register block j.
 // The 64 values sit in float2 pairs (block 0 with block 1, block 2 with block 3)
 // so the butterfly and the division run on the packed fp32x2 pipe of sm_100-
 // family parts (FADD2/FFMA2/FMUL2): one instruction per two values.
+//
+// Data movement.  When the rows of x are back to back (the normal case) every
+// warp runs its own TMA pipeline: a ring of kStages tile slots in shared memory,
+// each filled by one cp.async.bulk global->shared copy that completes on the
+// slot's mbarrier.  A warp keeps kStages tiles in flight while it computes
+// (pass 1: 8 warps x 4 x 4 KB = 128 KB per SM, pass 2: 16 warps x 2 x 4 KB) without
+// spending registers on them.  Strided rows (ldx != K) load directly into registers
+// (LoadMode below).
+// Every mbarrier wait is bounded (about one second of %globaltimer); a wait that
+// runs out records kFaultWaitTimeout in g_hq_fault, waits (bounded) for the
+// warp's copies still in flight and leaves the loop, so nothing can hang.
 //
 // Bit-exactness.  The butterfly performs the stages h = 1, 2, 4, 8 (inside a
 // block), then for G = 256 h = 16, 32 (across the quad's lanes), 64, 128
@@ -39,6 +49,17 @@ constexpr int kThreads = 256;            // 8 warps per CTA
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kBlocksPerLane = 4;
 constexpr int kTileBlocks = 32 * kBlocksPerLane;  // 128 NVFP4 blocks per warp tile
+
+// Fault bits recorded by the kernels (read back with hq_read_fault()).
+constexpr unsigned kFaultWaitTimeout = 1u;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
+
+}  // namespace hq
+
+// Device-side fault word of the library (one per device that loads it).
+__device__ unsigned int g_hq_fault;
+
+namespace hq {
 
 // ---------------------------------------------------------------------------
 // Unsigned 32-bit division by an invariant divisor with one multiply-high:
@@ -83,16 +104,9 @@ struct Params {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
+// a - b with one rounding: b * (-1) is exact, so fma(b, -1, a) = RN(a - b).
 __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 %%hq_a, %%hq_b, %%hq_d;\n\t"
-      "mov.b64 %%hq_a, {%2, %3};\n\t"
-      "mov.b64 %%hq_b, {%4, %5};\n\t"
-      "sub.rn.f32x2 %%hq_d, %%hq_a, %%hq_b;\n\t"
-      "mov.b64 {%0, %1}, %%hq_d;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
+  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
 }
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
@@ -103,6 +117,33 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   float d;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
   return d;
+}
+
+// Three-input max (sm_100 family).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// max |v[i]| over 16 values (the .x or .y lane of each pair), exact.
+template <bool Y>
+__device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
+  auto g = [&](int i) { return fabsf(Y ? v[i].y : v[i].x); };
+  float m = max3(g(0), g(1), g(2));
+#pragma unroll
+  for (int i = 3; i < 15; i += 2) m = max3(m, g(i), g(i + 1));
+  return fmaxf(m, g(15));
+}
+
+// a / b rounded to nearest even from r = RN(1/b), by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(a r), e = a - q0 b (exact),
+// q = RN(q0 + e r).  Valid while a, b, r, q0 and e stay normal.
+__device__ __forceinline__ float div_markstein(float a, float b, float r) {
+  const float q0 = __fmul_rn(a, r);
+  const float e = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(e, r, q0);
 }
 
 // ---------------------------------------------------------------------------
@@ -155,6 +196,77 @@ __device__ __forceinline__ float2 e2m1x2_to_f32(uint32_t byte) {
 }
 
 // ---------------------------------------------------------------------------
+// TMA bulk copies and mbarriers (inline PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared accesses (and those it has
+// synchronised with) before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// x is streamed once: its lines are the first to leave L2.
+__device__ __forceinline__ uint64_t l2_stream_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory, completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void tma_load(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Gives up after
+// about kWaitLimitNs and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 15u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (i == 0)
+        t0 = now;
+      else if (now - t0 > kWaitLimitNs)
+        return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Tile geometry.
 // ---------------------------------------------------------------------------
 template <int G>
@@ -182,14 +294,11 @@ __device__ __forceinline__ const uint8_t* block_ptr(const Params& p, uint64_t b,
   }
 }
 
-// Load one 16-element block and widen to fp32 (bf16 -> fp32 is exact).
-// Element i of block `jb` goes to the .x (jb even) or .y (jb odd) lane of v[i].
+// Widen 16 elements (bf16 -> fp32 is exact: the bf16 bits are the top half).
 template <bool BF16>
-__device__ __forceinline__ void load_block(const uint8_t* ptr, float (&f)[16]) {
+__device__ __forceinline__ void widen(const uint4* w4, float (&f)[16]) {
   if constexpr (BF16) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(ptr));
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(ptr) + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t w[8] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       f[2 * k] = __uint_as_float(w[k] << 16);
@@ -198,11 +307,10 @@ __device__ __forceinline__ void load_block(const uint8_t* ptr, float (&f)[16]) {
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(ptr) + k);
-      f[4 * k + 0] = __uint_as_float(a.x);
-      f[4 * k + 1] = __uint_as_float(a.y);
-      f[4 * k + 2] = __uint_as_float(a.z);
-      f[4 * k + 3] = __uint_as_float(a.w);
+      f[4 * k + 0] = __uint_as_float(w4[k].x);
+      f[4 * k + 1] = __uint_as_float(w4[k].y);
+      f[4 * k + 2] = __uint_as_float(w4[k].z);
+      f[4 * k + 3] = __uint_as_float(w4[k].w);
     }
   }
 }
@@ -213,27 +321,163 @@ struct Lane4 {
   float2 P[2][16];
 };
 
+__device__ __forceinline__ void put_block(Lane4& t, int j, const float (&f)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (j & 1)
+      t.P[j >> 1][i].y = f[i];
+    else
+      t.P[j >> 1][i].x = f[i];
+  }
+}
+
+// Direct global loads (strided rows).
 template <int G, bool BF16, bool STRIDED>
-__device__ __forceinline__ void load_tile(const Params& p, uint64_t tile_base, int lane,
-                                          bool (&valid)[4], Lane4& t) {
+__device__ __forceinline__ void load_tile_global(const Params& p, uint64_t tile_base, int lane,
+                                                 bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
+  constexpr int n16 = BF16 ? 2 : 4;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint64_t b = tile_base + lane_block<G>(lane, j);
     valid[j] = b < p.nb;
-    float f[16];
+    uint4 w4[n16];
     if (valid[j]) {
-      load_block<BF16>(block_ptr<STRIDED>(p, b, es), f);
+      const uint4* src = reinterpret_cast<const uint4*>(block_ptr<STRIDED>(p, b, es));
+#pragma unroll
+      for (int k = 0; k < n16; ++k) w4[k] = __ldg(src + k);
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) f[i] = 0.0f;
+      for (int k = 0; k < n16; ++k) w4[k] = make_uint4(0u, 0u, 0u, 0u);
     }
+    float f[16];
+    widen<BF16>(w4, f);
+    put_block(t, j, f);
+  }
+}
+
+// Loads from a tile staged in shared memory (block b of the tile at b*16*es).
+template <int G, bool BF16>
+__device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t tile_base, uint64_t nb,
+                                               int lane, bool (&valid)[4], Lane4& t) {
+  constexpr int es = BF16 ? 2 : 4;
+  constexpr int n16 = BF16 ? 2 : 4;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (j & 1)
-        t.P[j >> 1][i].y = f[i];
-      else
-        t.P[j >> 1][i].x = f[i];
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t bl = lane_block<G>(lane, j);
+    valid[j] = tile_base + bl < nb;
+    uint4 w4[n16];
+    if (valid[j]) {
+      const uint4* src = reinterpret_cast<const uint4*>(slot + bl * 16u * es);
+#pragma unroll
+      for (int k = 0; k < n16; ++k) w4[k] = src[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < n16; ++k) w4[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    float f[16];
+    widen<BF16>(w4, f);
+    put_block(t, j, f);
+  }
+}
+
+// Ring depth (tiles in flight per warp).  Pass 1 does little arithmetic per
+// byte and runs best with a deep ring and one CTA per SM; pass 2 needs its
+// registers for arithmetic and runs best with two CTAs per SM and a 2-deep ring.
+#ifndef HQ_PASS1_STAGES
+#define HQ_PASS1_STAGES 4
+#endif
+#ifndef HQ_PASS2_STAGES
+#define HQ_PASS2_STAGES 2
+#endif
+// Shared-memory ring geometry of the TMA pipeline.
+template <bool BF16, int STAGES>
+struct Ring {
+  static constexpr int kElemBytes = BF16 ? 2 : 4;
+  static constexpr int kTileBytes = kTileBlocks * 16 * kElemBytes;  // 4 KB / 8 KB
+  // fp32 tiles are twice as large: at most 3 of them per warp (192 KB per CTA).
+  static constexpr int kStages = BF16 ? STAGES : (STAGES > 3 ? 3 : STAGES);
+  static constexpr int kDataBytes = kWarpsPerCta * kStages * kTileBytes;
+  static constexpr int kSmemBytes = kDataBytes + kWarpsPerCta * kStages * 8;
+};
+
+// How a kernel reads x.
+enum LoadMode : int {
+  kLoadTma = 0,      // contiguous rows, per-warp TMA ring in shared memory
+  kLoadDirect = 1,   // contiguous rows, vector loads straight into registers
+  kLoadStrided = 2,  // rows ldx apart, vector loads straight into registers
+};
+
+// Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
+// values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
+template <int G, bool BF16, int MODE, int STAGES, typename Body>
+__device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + wid;
+  const uint64_t nw = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  if constexpr (MODE != kLoadTma) {
+    for (uint64_t seq = gw; seq < p.n_tiles; seq += nw) {
+      const uint64_t base = seq * kTileBlocks;
+      bool valid[4];
+      Lane4 t;
+      load_tile_global<G, BF16, MODE == kLoadStrided>(p, base, lane, valid, t);
+      body(base, lane, valid, t);
+    }
+  } else {
+    using R = Ring<BF16, STAGES>;
+    extern __shared__ __align__(1024) uint8_t hq_smem[];
+    uint8_t* ring = hq_smem + wid * R::kStages * R::kTileBytes;
+    const uint32_t ring_s = smem_addr(ring);
+    const uint32_t bar0 = smem_addr(hq_smem + R::kDataBytes) + wid * R::kStages * 8;
+    const uint64_t policy = l2_stream_policy();
+
+    auto issue = [&](uint64_t seq, int slot) {
+      const uint64_t first = seq * kTileBlocks;
+      const uint64_t nblk = (p.nb - first < kTileBlocks) ? (p.nb - first) : kTileBlocks;
+      tma_load(ring_s + slot * R::kTileBytes, p.x + first * 16u * R::kElemBytes,
+               static_cast<uint32_t>(nblk * 16u * R::kElemBytes), bar0 + slot * 8, policy);
+    };
+
+    if (lane == 0) {
+      for (int s = 0; s < R::kStages; ++s) mbar_init(bar0 + s * 8, 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    uint64_t issued = 0;  // tiles of this warp handed to TMA so far
+    if (lane == 0) {
+      for (int s = 0; s < R::kStages; ++s)
+        if (gw + s * nw < p.n_tiles) issue(gw + s * nw, s);
+    }
+    for (int s = 0; s < R::kStages; ++s)
+      if (gw + s * nw < p.n_tiles) ++issued;
+
+    uint64_t k = 0;
+    for (uint64_t seq = gw; seq < p.n_tiles; seq += nw, ++k) {
+      const int slot = static_cast<int>(k % R::kStages);
+      const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
+      const bool ok = mbar_wait(bar0 + slot * 8, parity);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+        for (uint64_t m = k; m < issued; ++m)
+          mbar_wait(bar0 + static_cast<int>(m % R::kStages) * 8,
+                    static_cast<uint32_t>((m / R::kStages) & 1));
+        return;
+      }
+      const uint64_t base = seq * kTileBlocks;
+      bool valid[4];
+      Lane4 t;
+      load_tile_smem<G, BF16>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+      __syncwarp();  // every lane has read the slot
+      const uint64_t next = seq + R::kStages * nw;
+      if (next < p.n_tiles) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(next, slot);
+        }
+        ++issued;
+      }
+      body(base, lane, valid, t);
     }
   }
 }
@@ -320,17 +564,10 @@ __device__ __forceinline__ constexpr float sqrt_g() {
 // ---------------------------------------------------------------------------
 // Pass 1: rotate + amax.
 // ---------------------------------------------------------------------------
-template <int G, bool BF16, bool STRIDED, bool WRITE_Y>
-__global__ void __launch_bounds__(kThreads, 2) k_rot_amax(Params p) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta) + (threadIdx.x >> 5);
-  const uint64_t n_warps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+template <int G, bool BF16, int MODE, bool WRITE_Y>
+__global__ void __launch_bounds__(kThreads, 1) k_rot_amax(Params p) {
   float zmax = 0.0f;
-  for (uint64_t tile = warp; tile < p.n_tiles; tile += n_warps) {
-    const uint64_t base = tile * kTileBlocks;
-    bool valid[4];
-    Lane4 t;
-    load_tile<G, BF16, STRIDED>(p, base, lane, valid, t);
+  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES>(p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     rotate_tile<G>(t, lane);
 #pragma unroll
     for (int k = 0; k < 2; ++k)
@@ -356,9 +593,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_rot_amax(Params p) {
         }
       }
     }
-  }
+  });
   // max over the CTA, then one atomic per CTA.  |y| = RN(|z| / sqrt(G)) is
   // monotone in |z|, so max |y| = RN(max |z| / sqrt(G)) exactly.
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) zmax = max_nan(zmax, __shfl_xor_sync(0xFFFFFFFFu, zmax, m));
   __shared__ float red[kWarpsPerCta];
@@ -378,79 +616,73 @@ __global__ void __launch_bounds__(kThreads, 2) k_rot_amax(Params p) {
 // ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
-template <int G, bool BF16, bool STRIDED>
+template <int G, bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta) + (threadIdx.x >> 5);
-  const uint64_t n_warps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-
   // s_global = amax / (448 * 6), or 1 if that is 0.
   const float amax = *p.amax_in;
   float s_global = __fdiv_rn(amax, 2688.0f);
   if (s_global == 0.0f) s_global = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.sglobal_out) *p.sglobal_out = s_global;
+  // Reciprocals for the block-scale divisions (Markstein fast path).
+  const float r6 = __frcp_rn(6.0f);
+  const float rg = __frcp_rn(s_global);
+  const bool sg_ok = s_global >= 0x1p-60f && s_global <= 0x1p60f;
+  const bool q_fast = s_global >= 0x1p-87f && s_global <= 0x1p91f;
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
 
-  for (uint64_t tile = warp; tile < p.n_tiles; tile += n_warps) {
-    const uint64_t base = tile * kTileBlocks;
-    bool valid[4];
-    Lane4 t;
-    load_tile<G, BF16, STRIDED>(p, base, lane, valid, t);
+  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(
+      p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     rotate_tile<G>(t, lane);
 
     // Block amax of z, then of y = z / sqrt(G): RN(max|z| * c) = max RN(|z| * c).
-    float2 zm[2];
+    float am[4];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      float mx = 0.0f, my = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        mx = fmaxf(mx, fabsf(t.P[k][i].x));
-        my = fmaxf(my, fabsf(t.P[k][i].y));
-      }
-      zm[k] = make_float2(mx, my);
+      am[2 * k] = __fmul_rn(block_absmax<false>(t.P[k]), c);
+      am[2 * k + 1] = __fmul_rn(block_absmax<true>(t.P[k]), c);
     }
 
-    // Block scales: v = (amax_b / 6) / s_global -> E4M3 (RNE, satfinite).
+    // Block scales: v = (amax_b / 6) / s_global, two correctly rounded
+    // divisions, then E4M3 (RNE, satfinite).  The Markstein form is exact for
+    // amax_b in [2^-90, 2^90] and s_global in [2^-60, 2^60]; below 2^-90 it can be
+    // off by an ulp of a value under 2^-29, which rounds to the E4M3 zero either
+    // way, so only the upper bound needs a check.
+    bool v_fast = sg_ok;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v_fast &= am[j] <= 0x1p90f;
+    float v[4];
+    if (v_fast) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = div_markstein(div_markstein(am[j], 6.0f, r6), s_global, rg);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fdiv_rn(__fdiv_rn(am[j], 6.0f), s_global);
+    }
     uint32_t sb2[2];    // two E4M3 patterns per pair
     float2 sf[2];       // s_f = s_block * s_global
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const float ax = __fmul_rn(zm[k].x, c);
-      const float ay = __fmul_rn(zm[k].y, c);
-      const float vx = __fdiv_rn(__fdiv_rn(ax, 6.0f), s_global);
-      const float vy = __fdiv_rn(__fdiv_rn(ay, 6.0f), s_global);
-      sb2[k] = e4m3x2(vx, vy);
+      sb2[k] = e4m3x2(v[2 * k], v[2 * k + 1]);
       const float2 sbf = e4m3x2_to_f32(sb2[k]);
-      sf[k] = make_float2(__fmul_rn(sbf.x, s_global), __fmul_rn(sbf.y, s_global));
+      sf[k] = mul2(sbf, make_float2(s_global, s_global));
     }
 
     // Fast path: q = RN(y / s_f) = RN(z / D), D = s_f * sqrt(G), by Markstein's
-    // correction: r = RN(1/D), q0 = RN(z r), e = z - q0 D (exact), q = RN(q0 + e r)
-    // (P. Markstein, "Computation of elementary functions on the IBM RISC
-    // System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the theorem that q is
-    // the correctly rounded quotient when r is the correctly rounded reciprocal
-    // and nothing under/overflows).  The domain s_f in [2^-96, 2^100] keeps D,
-    // r, z and e normal wherever the rounding decides a code (|q| >= 1/8); a
-    // smaller quotient gives code 0 with the sign of z either way, and
-    // y = RN(z c) equals z c there except for values that only give such codes.
+    // correction with r = RN(1/D) (as div_markstein).  The domain s_f in
+    // [2^-96, 2^100] keeps D, r, z and e normal wherever the rounding decides a
+    // code (|q| >= 1/8); a smaller quotient gives code 0 with the sign of z either
+    // way, and y = RN(z c) equals z c there except for values that only give such
+    // codes.  A non-zero s_block lies in [2^-9, 448], so q_fast (s_global in
+    // [2^-87, 2^91]) puts every non-zero s_f of the tensor in that domain.
     //
     // The steps run on negated values, with nr = -r:  q0n = RN(z nr) = -q0,
     // e = RN(z + q0n D), qn = RN(q0n + e nr) = -q.  In this form qn is -q even for
     // z = +-0 (the direct form turns -0 into +0, since e = +0 and +0 + -0 = +0),
     // so code(q) = code(qn) with the sign bit flipped: one XOR per 8 codes.
-    bool fast = true;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float a = sf[k].x, b = sf[k].y;
-      fast &= (a == 0.0f) || (a >= 0x1p-96f && a <= 0x1p100f);
-      fast &= (b == 0.0f) || (b >= 0x1p-96f && b <= 0x1p100f);
-    }
-
     uint32_t w[4][2];  // packed codes per block: elements 0..7, 8..15
-    if (fast) {
+    if (q_fast) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const float dx = (sf[k].x == 0.0f) ? 1.0f : __fmul_rn(sf[k].x, sq);
@@ -499,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
       const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
       __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
     }
-  }
+  });
 }
 
 // ---------------------------------------------------------------------------

@@ -124,6 +124,15 @@ const char* hq_status_string(hq_status status);
 /* The cudaError_t behind the last HQ_ERR_CUDA returned on the calling host thread (0 if none). */
 int hq_last_cuda_error(void);
 
+/*
+ * hq_read_fault -- the library's device fault word on the current device (synchronous: waits
+ * for all work on the device first).  0 means no kernel recorded a fault.  Bit 0 (value 1):
+ * a kernel's wait for one of its own shared-memory tile copies exceeded about one second; that
+ * warp stopped early, so the outputs of the affected call are incomplete.  With `clear` non-zero
+ * the word is reset to 0 after reading.
+ */
+hq_status hq_read_fault(unsigned int* fault, int clear);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int hq_version(void);
 

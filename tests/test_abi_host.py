@@ -139,3 +139,7 @@ def test_binding_rejects_host_tensors():
         hq.hq_rot_amax(x, 16)
     with pytest.raises(ValueError, match="CUDA"):
         hq.hq_rotate_quant_nvfp4(x, 16, torch.zeros(1))
+
+
+def test_read_fault_rejects_null(lib):
+    assert lib.hq_read_fault(None, 0) == 1

@@ -118,3 +118,62 @@ def test_e4m3_every_value_and_midpoint():
     gq, gs, oq, os_ = run_both(x)
     compare("scales", gs, os_)
     compare("codes", gq, oq)
+
+
+def test_quotients_next_to_every_decision_point_under_many_scales():
+    """Division stress: for 160 global scales (random mantissas, plus extremes that leave the
+    kernel's fast-division domain) and every non-zero E4M3 block scale e, a block [anchor,
+    values] whose values lie within 3 ulps of t * s_f for every E2M1 midpoint and grid value t,
+    both signs.  The amax is passed to pass 2 directly, so s_global = amax / 2688 is arbitrary
+    and s_f = e * s_global has a full mantissa."""
+    rng = np.random.default_rng(7)
+    points = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    codes = np.arange(1, 127, dtype=np.uint8)
+    evals = e4m3_table()[1:]
+    amaxes = list(np.exp2(rng.uniform(-8, 12, 150)).astype(np.float32)) + \
+        [np.float32(v) for v in (1e-30, 3e-25, 1e-20, 7e15, 1e25, 2e30, 3e33, 1e-35, 5e-38, 1e37)]
+    for amax in amaxes:
+        sg = np.float32(amax) / np.float32(2688.0)
+        sg = np.float32(1.0) if sg == 0 else sg
+        rows = []
+        for e in evals:
+            D = np.float32(np.float32(e) * sg)
+            anchor = np.float32(6.0 * float(e) * float(sg))
+            base = (points * float(D)).astype(np.float32)
+            vals = np.concatenate([np.nextafter(base, np.float32(np.inf)), base,
+                                   np.nextafter(base, np.float32(0))])
+            for _ in range(2):
+                vals = np.concatenate([vals, np.nextafter(vals[-14:], np.float32(np.inf)),
+                                       np.nextafter(vals[:14], np.float32(0))])
+            vals = np.concatenate([vals, -vals]).astype(np.float32)
+            n = (vals.size + 14) // 15
+            blk = np.zeros((n, 16), np.float32)
+            blk[:, 0] = anchor
+            pad = np.zeros(n * 15, np.float32)
+            pad[: vals.size] = vals
+            blk[:, 1:] = pad.reshape(n, 15)
+            rows.append(blk.reshape(-1))
+        width = max(r.size for r in rows)
+        width = (width + 15) // 16 * 16
+        x = np.zeros((len(rows), width), np.float32)
+        for i, r in enumerate(rows):
+            x[i, : r.size] = r
+        xt = torch.from_numpy(x).cuda()
+        a_dev = torch.tensor([amax], dtype=torch.float32, device="cuda")
+        q, s, sgd = hq.hq_rotate_quant_nvfp4(xt, 0, a_dev)
+        torch.cuda.synchronize()
+        oq, os_, _, osg = oracle.quantize(x, 0, amax=float(amax))
+        assert sgd.item() == osg
+        compare(f"scales amax={amax}", s.cpu().numpy(), os_)
+        compare(f"codes amax={amax}", q.cpu().numpy(), oq)
+        if 1 <= amax <= 4096:
+            # the block scales came out as designed, so every t * s_f decision was exercised
+            assert (os_[:, 0] == codes).all()
+
+
+def test_no_device_fault_recorded():
+    import ctypes
+
+    v = ctypes.c_uint(12345)
+    assert hq.load().hq_read_fault(ctypes.byref(v), 1) == 0
+    assert v.value == 0
