@@ -42,11 +42,13 @@ DEFAULT_WORKLOAD = "bf16_32768x28672"
 METRIC = "rotate+NVFP4-quant GB/s (bytes in+out) and % of GB300 HBM peak"
 L2_BYTES = 126 * 1024 * 1024
 
-# Pass-2 DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the kernel source it was taken on.  Captured on the
-# bf16 [16384, 8192] G=16 tensor and scaled by element count to the bench workload; the
-# capture and its command are summarised under profiles/.
-NCU_TRAFFIC = {}
+# Pass-2 DRAM traffic per launch from a one-pass ncu capture of the bench workload
+# itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
+# it was taken on: a changed kernel reports null until it is captured again.
+NCU_TRAFFIC = {
+    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.880 GB read + 0.4975 GB written
+    ("6d9b0e521decb38a", "bf16_32768x28672", 16): 1.880e9 + 0.4975e9,
+}
 
 
 def kernel_source_hash() -> str:
