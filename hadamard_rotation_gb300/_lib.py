@@ -56,6 +56,17 @@ def load() -> ctypes.CDLL:
         lib.hq_status_string.restype = ctypes.c_char_p
         lib.hq_last_cuda_error.argtypes = []
         lib.hq_last_cuda_error.restype = i32
+        sz = ctypes.c_size_t
+        lib.hq_host_pipeline_workspace_bytes.argtypes = [i64, i64, i32]
+        lib.hq_host_pipeline_workspace_bytes.restype = sz
+        lib.hq_host_pipeline_create.argtypes = [i64, i64, i32, i32, p, sz, ctypes.POINTER(p)]
+        lib.hq_host_pipeline_create.restype = i32
+        lib.hq_host_pipeline_submit.argtypes = [p, p, p, p, p]
+        lib.hq_host_pipeline_submit.restype = i32
+        lib.hq_host_pipeline_wait.argtypes = [p]
+        lib.hq_host_pipeline_wait.restype = i32
+        lib.hq_host_pipeline_destroy.argtypes = [p]
+        lib.hq_host_pipeline_destroy.restype = i32
         lib.hq_read_fault.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.hq_read_fault.restype = i32
         lib.hq_version.argtypes = []

@@ -105,49 +105,77 @@ def quantize_nvfp4(x: torch.Tensor, group: int, stream: torch.cuda.Stream | None
 
 
 class HostQuantizer:
-    """Quantize host tensors: pinned host -> device, both passes, device -> pinned host.
+    """Quantize tensors that live in pinned host memory, through the library's host pipeline.
 
-    Device buffers and pinned outputs are allocated once here; each call then enqueues
-    one host-to-device copy of x, the two kernels and the device-to-host copies of the
-    codes, scales and s_global on ``stream``.
+    The pipeline (hq_host_pipeline_* in include/hq.h) copies x to the device, runs both passes
+    and copies the codes, scales and s_global back.  Consecutive submissions overlap: the input
+    copy of one runs while the previous one computes and copies its results back.  Its device
+    workspace (two buffer sets) is allocated here with torch; the library allocates none.
     """
 
     def __init__(self, M: int, K: int, dtype: torch.dtype, group: int,
-                 device: torch.device | str = "cuda", stream: torch.cuda.Stream | None = None):
-        self.M, self.K, self.group = M, K, group
+                 device: torch.device | str = "cuda"):
+        if dtype not in _DTYPES:
+            raise ValueError(f"dtype must be float32 or bfloat16, got {dtype}")
+        self.M, self.K, self.group, self.dtype = M, K, group, dtype
         self.device = torch.device(device)
-        self.stream = stream
-        self.x_dev = torch.empty((M, K), dtype=dtype, device=self.device)
-        self.amax = torch.empty(1, dtype=torch.float32, device=self.device)
-        self.q_dev = torch.empty((M, K // 2), dtype=torch.uint8, device=self.device)
-        self.s_dev = torch.empty((M, K // 16), dtype=torch.uint8, device=self.device)
-        self.sg_dev = torch.empty(1, dtype=torch.float32, device=self.device)
+        lib = _lib.load()
+        dt = _DTYPES[dtype]
+        nbytes = lib.hq_host_pipeline_workspace_bytes(M, K, dt)
+        if nbytes == 0:
+            raise ValueError(f"invalid sizes for the host pipeline: M={M}, K={K}")
+        self.work = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            check(lib.hq_host_pipeline_create(M, K, dt, group, _ptr(self.work), nbytes,
+                                              ctypes.byref(handle)), "hq_host_pipeline_create")
+        self._handle = handle
         self.q_host = torch.empty((M, K // 2), dtype=torch.uint8, pin_memory=True)
         self.s_host = torch.empty((M, K // 16), dtype=torch.uint8, pin_memory=True)
         self.sg_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
 
     @property
     def h2d_bytes(self) -> int:
-        return self.x_dev.numel() * self.x_dev.element_size()
+        return self.M * self.K * (2 if self.dtype == torch.bfloat16 else 4)
 
     @property
     def d2h_bytes(self) -> int:
-        return self.q_host.numel() + self.s_host.numel() + 4
+        return self.M * self.K // 2 + self.M * self.K // 16 + 4
 
-    def enqueue(self, x_host: torch.Tensor) -> None:
-        """Enqueue one quantization of the pinned host tensor ``x_host`` (no host sync)."""
-        s = self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
-        with torch.cuda.stream(s):
-            self.x_dev.copy_(x_host, non_blocking=True)
-            hq_rot_amax(self.x_dev, self.group, amax=self.amax, stream=s)
-            hq_rotate_quant_nvfp4(self.x_dev, self.group, self.amax, q=self.q_dev,
-                                  scales=self.s_dev, s_global=self.sg_dev, stream=s)
-            self.q_host.copy_(self.q_dev, non_blocking=True)
-            self.s_host.copy_(self.s_dev, non_blocking=True)
-            self.sg_host.copy_(self.sg_dev, non_blocking=True)
+    def submit(self, x_host: torch.Tensor, q_host: torch.Tensor | None = None,
+               s_host: torch.Tensor | None = None, sg_host: torch.Tensor | None = None) -> None:
+        """Enqueue one quantization of ``x_host``; outputs go to the given host tensors (default:
+        this object's pinned buffers).  Every buffer must stay untouched until wait()."""
+        if x_host.is_cuda or x_host.dtype != self.dtype or tuple(x_host.shape) != (self.M, self.K) \
+                or not x_host.is_contiguous():
+            raise ValueError(f"x_host must be a contiguous host {self.dtype} tensor [{self.M}, {self.K}]")
+        q_host = self.q_host if q_host is None else q_host
+        s_host = self.s_host if s_host is None else s_host
+        sg_host = self.sg_host if sg_host is None else sg_host
+        for t, shape, dt, name in ((q_host, (self.M, self.K // 2), torch.uint8, "q_host"),
+                                   (s_host, (self.M, self.K // 16), torch.uint8, "s_host"),
+                                   (sg_host, (1,), torch.float32, "sg_host")):
+            if t.is_cuda or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host {dt} tensor {shape}")
+        check(_lib.load().hq_host_pipeline_submit(self._handle, _ptr(x_host), _ptr(q_host),
+                                                  _ptr(s_host), _ptr(sg_host)),
+              "hq_host_pipeline_submit")
+
+    def wait(self) -> None:
+        check(_lib.load().hq_host_pipeline_wait(self._handle), "hq_host_pipeline_wait")
 
     def __call__(self, x_host: torch.Tensor):
-        self.enqueue(x_host)
-        s = self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
-        s.synchronize()
+        self.submit(x_host)
+        self.wait()
         return self.q_host, self.s_host, float(self.sg_host[0])
+
+    def close(self) -> None:
+        if getattr(self, "_handle", None):
+            check(_lib.load().hq_host_pipeline_destroy(self._handle), "hq_host_pipeline_destroy")
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

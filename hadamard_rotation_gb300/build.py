@@ -13,8 +13,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "hq.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "hq_kernels.cuh"), os.path.join(INCLUDE, "hq.h")]
+SOURCES = [os.path.join(CSRC, "hq.cu"), os.path.join(CSRC, "hq_host.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "hq_kernels.cuh"), os.path.join(CSRC, "hq_internal.h"),
+                  os.path.join(INCLUDE, "hq.h")]
 LIB = os.path.join(PKG, "libhq.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -27,8 +28,9 @@ def nvcc_path() -> str:
 
 
 def nvcc_command(out: str, extra: list[str] | None = None) -> list[str]:
-    return [nvcc_path(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-            "-I", INCLUDE, *(extra or []), "-o", out, *SOURCES]
+    return [nvcc_path(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
+            "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, *(extra or []), "-o", out,
+            *SOURCES]
 
 
 def up_to_date() -> bool:

@@ -12,16 +12,21 @@
 #include <mutex>
 
 #include "hq.h"
+#include "hq_internal.h"
 #include "hq_kernels.cuh"
 
 namespace {
-
 thread_local int g_last_cuda_error = 0;
+}  // namespace
 
-hq_status cuda_fail(cudaError_t e) {
+hq_status hq::cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return HQ_ERR_CUDA;
 }
+
+namespace {
+
+using hq::cuda_fail;
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -1,0 +1,218 @@
+// hq_host.cu -- host pipeline of libhq: quantize tensors that live in host memory.
+//
+// One submission = copy x host -> device, pass 1 (hq_rot_amax), pass 2
+// (hq_rotate_quant_nvfp4), copy codes, scales and s_global device -> host.
+// Consecutive submissions overlap: two buffer sets in the caller's device
+// workspace alternate, and the three phases run on three streams ordered by
+// events, so the input copy of submission n+1 runs while submission n computes
+// and while its outputs travel back (the two copy directions use separate copy
+// engines).
+//
+//   in stream      H2D(n) ........ H2D(n+1) ........ H2D(n+2)
+//   compute stream        pass1,2(n)         pass1,2(n+1)
+//   out stream                      D2H(n) ........  D2H(n+1)
+//
+// Slot reuse: submission n+2 overwrites the buffers of submission n, so its input
+// copy waits until pass 2 of n has finished reading x, and its kernels wait until
+// the output copy of n has finished reading the codes.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <new>
+
+#include "hq.h"
+#include "hq_internal.h"
+
+struct hq_host_pipeline {
+  int device = 0;
+  int64_t M = 0, K = 0;
+  hq_dtype dtype = HQ_BF16;
+  int group = 16;
+  size_t x_bytes = 0, q_bytes = 0, s_bytes = 0;
+  struct Slot {
+    uint8_t* x = nullptr;
+    uint8_t* q = nullptr;
+    uint8_t* s = nullptr;
+    float* amax = nullptr;
+    float* sglobal = nullptr;
+    cudaEvent_t in_done = nullptr;       // input copy finished
+    cudaEvent_t compute_done = nullptr;  // pass 2 finished
+    cudaEvent_t out_done = nullptr;      // output copies finished
+    bool used = false;
+  } slot[2];
+  cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
+  uint64_t submitted = 0;
+};
+
+namespace {
+
+hq_status fail(cudaError_t e) { return hq::cuda_fail(e); }
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool sizes(int64_t M, int64_t K, hq_dtype dt, size_t* xb, size_t* qb, size_t* sb) {
+  if (M <= 0 || K <= 0 || K % 16 != 0) return false;
+  if (M > INT64_MAX / K) return false;
+  const uint64_t n = static_cast<uint64_t>(M) * static_cast<uint64_t>(K);
+  *xb = n * (dt == HQ_BF16 ? 2u : 4u);
+  *qb = n / 2;
+  *sb = n / 16;
+  return true;
+}
+
+size_t slot_bytes(size_t xb, size_t qb, size_t sb) {
+  return round_up(xb) + round_up(qb) + round_up(sb) + 2 * kAlign;
+}
+
+void destroy_objects(hq_host_pipeline* p) {
+  for (auto& s : p->slot) {
+    if (s.in_done) cudaEventDestroy(s.in_done);
+    if (s.compute_done) cudaEventDestroy(s.compute_done);
+    if (s.out_done) cudaEventDestroy(s.out_done);
+  }
+  if (p->in) cudaStreamDestroy(p->in);
+  if (p->compute) cudaStreamDestroy(p->compute);
+  if (p->out) cudaStreamDestroy(p->out);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hq_host_pipeline_workspace_bytes(int64_t M, int64_t K, hq_dtype dtype) {
+  size_t xb, qb, sb;
+  if ((dtype != HQ_F32 && dtype != HQ_BF16) || !sizes(M, K, dtype, &xb, &qb, &sb)) return 0;
+  return 2 * slot_bytes(xb, qb, sb);
+}
+
+hq_status hq_host_pipeline_create(int64_t M, int64_t K, hq_dtype dtype, int group, void* d_work,
+                                  size_t work_bytes, hq_host_pipeline** out) {
+  if (!out || !d_work) return HQ_ERR_NULL;
+  *out = nullptr;
+  if (dtype != HQ_F32 && dtype != HQ_BF16) return HQ_ERR_DTYPE;
+  if (group != 0 && group != 16 && group != 256) return HQ_ERR_GROUP;
+  size_t xb, qb, sb;
+  if (!sizes(M, K, dtype, &xb, &qb, &sb) || K % (group > 16 ? group : 16) != 0)
+    return HQ_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(d_work) % kAlign != 0) return HQ_ERR_ALIGN;
+  const size_t per_slot = slot_bytes(xb, qb, sb);
+  if (work_bytes < 2 * per_slot) return HQ_ERR_SHAPE;
+
+  hq_host_pipeline* p = new (std::nothrow) hq_host_pipeline();
+  if (!p) return HQ_ERR_NULL;
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e != cudaSuccess) {
+    delete p;
+    return fail(e);
+  }
+  p->M = M;
+  p->K = K;
+  p->dtype = dtype;
+  p->group = group;
+  p->x_bytes = xb;
+  p->q_bytes = qb;
+  p->s_bytes = sb;
+  uint8_t* base = static_cast<uint8_t*>(d_work);
+  for (int i = 0; i < 2; ++i) {
+    auto& s = p->slot[i];
+    uint8_t* b = base + i * per_slot;
+    s.x = b;
+    b += round_up(xb);
+    s.q = b;
+    b += round_up(qb);
+    s.s = b;
+    b += round_up(sb);
+    s.amax = reinterpret_cast<float*>(b);
+    s.sglobal = reinterpret_cast<float*>(b + kAlign);
+  }
+  const unsigned ev_flags = cudaEventDisableTiming;
+  for (auto& s : p->slot) {
+    if ((e = cudaEventCreateWithFlags(&s.in_done, ev_flags)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&s.compute_done, ev_flags)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&s.out_done, ev_flags)) != cudaSuccess) {
+      destroy_objects(p);
+      delete p;
+      return fail(e);
+    }
+  }
+  if ((e = cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&p->compute, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking)) != cudaSuccess) {
+    destroy_objects(p);
+    delete p;
+    return fail(e);
+  }
+  *out = p;
+  return HQ_OK;
+}
+
+hq_status hq_host_pipeline_submit(hq_host_pipeline* p, const void* x_host, uint8_t* q_host,
+                                  uint8_t* scales_host, float* s_global_host) {
+  if (!p || !x_host || !q_host || !scales_host || !s_global_host) return HQ_ERR_NULL;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(e);
+  if (dev != p->device && (e = cudaSetDevice(p->device)) != cudaSuccess) return fail(e);
+  auto& s = p->slot[p->submitted & 1];
+  hq_status st = HQ_OK;
+  // input copy: the slot's x must no longer be read by an earlier pass 2
+  if (s.used && (e = cudaStreamWaitEvent(p->in, s.compute_done, 0)) != cudaSuccess) st = fail(e);
+  if (st == HQ_OK &&
+      (e = cudaMemcpyAsync(s.x, x_host, p->x_bytes, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK && (e = cudaEventRecord(s.in_done, p->in)) != cudaSuccess) st = fail(e);
+  // both passes: after the input arrived and after the slot's last outputs left
+  if (st == HQ_OK && (e = cudaStreamWaitEvent(p->compute, s.in_done, 0)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK && s.used && (e = cudaStreamWaitEvent(p->compute, s.out_done, 0)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK)
+    st = hq_rot_amax(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, nullptr, p->compute);
+  if (st == HQ_OK)
+    st = hq_rotate_quant_nvfp4(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, s.q, s.s,
+                               s.sglobal, p->compute);
+  if (st == HQ_OK && (e = cudaEventRecord(s.compute_done, p->compute)) != cudaSuccess)
+    st = fail(e);
+  // output copies
+  if (st == HQ_OK && (e = cudaStreamWaitEvent(p->out, s.compute_done, 0)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK &&
+      (e = cudaMemcpyAsync(q_host, s.q, p->q_bytes, cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK && (e = cudaMemcpyAsync(scales_host, s.s, p->s_bytes, cudaMemcpyDeviceToHost,
+                                          p->out)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK && (e = cudaMemcpyAsync(s_global_host, s.sglobal, sizeof(float),
+                                          cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+    st = fail(e);
+  if (st == HQ_OK && (e = cudaEventRecord(s.out_done, p->out)) != cudaSuccess) st = fail(e);
+  if (st == HQ_OK) {
+    s.used = true;
+    ++p->submitted;
+  }
+  if (dev != p->device) cudaSetDevice(dev);
+  return st;
+}
+
+hq_status hq_host_pipeline_wait(hq_host_pipeline* p) {
+  if (!p) return HQ_ERR_NULL;
+  cudaError_t e = cudaStreamSynchronize(p->out);
+  if (e != cudaSuccess) return fail(e);
+  e = cudaStreamSynchronize(p->compute);
+  if (e != cudaSuccess) return fail(e);
+  e = cudaStreamSynchronize(p->in);
+  if (e != cudaSuccess) return fail(e);
+  return HQ_OK;
+}
+
+hq_status hq_host_pipeline_destroy(hq_host_pipeline* p) {
+  if (!p) return HQ_OK;
+  hq_status st = hq_host_pipeline_wait(p);
+  destroy_objects(p);
+  delete p;
+  return st;
+}
+
+}  // extern "C"

@@ -46,6 +46,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define HQ_API __attribute__((visibility("default")))
+#else
+#define HQ_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -81,7 +87,7 @@ typedef void* hq_stream;
  *   y      : optional fp32 [M, K] (row stride K), 16-byte aligned, receives the rotated tensor;
  *            NULL to skip (the normal case: the rotation is never stored).
  */
-hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+HQ_API hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
                       int group, float* amax, float* y, hq_stream stream);
 
 /*
@@ -97,7 +103,7 @@ hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64
  *   scales   : uint8 [M, K/16], 4-byte aligned.
  *   s_global : optional 1 float, receives s_global (the per-tensor fp32 scale); NULL to skip.
  */
-hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
@@ -114,15 +120,15 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
  *   out       : fp32 [M, K] (row stride K), 16-byte aligned.
  *   The two products are rounded in that order (s_f first), then the butterfly as above.
  */
-hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float* s_global,
+HQ_API hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float* s_global,
                            int64_t M, int64_t K, int group, int unrotate, float* out,
                            hq_stream stream);
 
 /* Human-readable name of a status code (static storage). */
-const char* hq_status_string(hq_status status);
+HQ_API const char* hq_status_string(hq_status status);
 
 /* The cudaError_t behind the last HQ_ERR_CUDA returned on the calling host thread (0 if none). */
-int hq_last_cuda_error(void);
+HQ_API int hq_last_cuda_error(void);
 
 /*
  * hq_read_fault -- the library's device fault word on the current device (synchronous: waits
@@ -131,10 +137,48 @@ int hq_last_cuda_error(void);
  * warp stopped early, so the outputs of the affected call are incomplete.  With `clear` non-zero
  * the word is reset to 0 after reading.
  */
-hq_status hq_read_fault(unsigned int* fault, int clear);
+HQ_API hq_status hq_read_fault(unsigned int* fault, int clear);
+
+/*
+ * Host pipeline -- quantize tensors that live in (pinned) host memory.
+ *   Not a step of the method itself: the transport around it.  One submission copies x to the
+ *   device, runs hq_rot_amax and hq_rotate_quant_nvfp4 there, and copies the codes, the scales
+ *   and s_global back.  Consecutive submissions overlap: the pipeline alternates between two
+ *   buffer sets in the caller's device workspace and runs input copies, kernels and output
+ *   copies on three streams of its own, ordered by events, so the input copy of one submission
+ *   runs while the previous one computes and copies its results back.
+ *
+ *   The pipeline object is host memory owned by the library (freed by _destroy); it also owns
+ *   three CUDA streams and six events on the device that is current at _create.  It allocates
+ *   no device memory: `d_work` (at least hq_host_pipeline_workspace_bytes(M, K, dtype) bytes,
+ *   256-byte aligned, owned by the caller) holds both buffer sets.  Host buffers should be pinned
+ *   (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous; every host buffer of a
+ *   submission must stay valid and untouched until hq_host_pipeline_wait() returns.
+ */
+typedef struct hq_host_pipeline hq_host_pipeline;
+
+/* Device workspace bytes for M x K tensors of `dtype` (0 if the sizes are invalid). */
+HQ_API size_t hq_host_pipeline_workspace_bytes(int64_t M, int64_t K, hq_dtype dtype);
+
+/* Create a pipeline for M x K row-major tensors (contiguous rows) and rotation `group`. */
+HQ_API hq_status hq_host_pipeline_create(int64_t M, int64_t K, hq_dtype dtype, int group,
+                                         void* d_work, size_t work_bytes,
+                                         hq_host_pipeline** out);
+
+/* Enqueue one quantization and return at once.  x_host: [M, K] of dtype; q_host: [M, K/2] bytes;
+ * scales_host: [M, K/16] bytes; s_global_host: 1 float.  Results are complete after
+ * hq_host_pipeline_wait(). */
+HQ_API hq_status hq_host_pipeline_submit(hq_host_pipeline* p, const void* x_host, uint8_t* q_host,
+                                         uint8_t* scales_host, float* s_global_host);
+
+/* Block the calling thread until every submitted quantization has finished. */
+HQ_API hq_status hq_host_pipeline_wait(hq_host_pipeline* p);
+
+/* Wait for outstanding work, then release the streams, events and the object (NULL is a no-op). */
+HQ_API hq_status hq_host_pipeline_destroy(hq_host_pipeline* p);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
-int hq_version(void);
+HQ_API int hq_version(void);
 
 #ifdef __cplusplus
 }

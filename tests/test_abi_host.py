@@ -143,3 +143,25 @@ def test_binding_rejects_host_tensors():
 
 def test_read_fault_rejects_null(lib):
     assert lib.hq_read_fault(None, 0) == 1
+
+
+def test_host_pipeline_argument_checks(lib):
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    out = ctypes.c_void_p(1234)
+    ref = ctypes.byref(out)
+    assert lib.hq_host_pipeline_workspace_bytes(0, 32, 1) == 0
+    assert lib.hq_host_pipeline_workspace_bytes(4, 24, 1) == 0
+    assert lib.hq_host_pipeline_workspace_bytes(4, 32, 7) == 0
+    need = lib.hq_host_pipeline_workspace_bytes(4, 32, 1)
+    assert need > 2 * (4 * 32 * 2)
+    assert lib.hq_host_pipeline_create(4, 32, 1, 16, None, need, ref) == 1
+    assert out.value is None or out.value == 1234 or out.value == 0
+    assert lib.hq_host_pipeline_create(4, 32, 1, 16, P(FAKE), need, None) == 1
+    assert lib.hq_host_pipeline_create(4, 32, 5, 16, P(FAKE), need, ref) == 4
+    assert lib.hq_host_pipeline_create(4, 32, 1, 8, P(FAKE), need, ref) == 5
+    assert lib.hq_host_pipeline_create(4, 48, 1, 256, P(FAKE), need, ref) == 2
+    assert lib.hq_host_pipeline_create(4, 32, 1, 16, P(FAKE + 16), need, ref) == 3
+    assert lib.hq_host_pipeline_create(4, 32, 1, 16, P(FAKE), need - 1, ref) == 2
+    assert lib.hq_host_pipeline_submit(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE)) == 1
+    assert lib.hq_host_pipeline_wait(None) == 1
+    assert lib.hq_host_pipeline_destroy(None) == 0

@@ -221,7 +221,30 @@ def test_tiling_invariance():
             assert torch.equal(qs, q[r0:r1]) and torch.equal(ss, s[r0:r1])
 
 
-def test_host_quantizer_matches_device_path():
+def test_host_pipeline_matches_oracle_over_overlapping_submissions():
+    """Five submissions in flight through the two-slot host pipeline, each with its own input
+    and output buffers; every result must equal the oracle's for its own input."""
+    M, K = 1024, 2048
+    hqz = hq.HostQuantizer(M, K, torch.bfloat16, 16)
+    xs, outs = [], []
+    for i in range(5):
+        x = rand_input(M, K, torch.bfloat16, seed=100 + i).pin_memory()
+        q = torch.empty((M, K // 2), dtype=torch.uint8, pin_memory=True)
+        s = torch.empty((M, K // 16), dtype=torch.uint8, pin_memory=True)
+        sg = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        hqz.submit(x, q, s, sg)
+        xs.append(x)
+        outs.append((q, s, sg))
+    hqz.wait()
+    for x, (q, s, sg) in zip(xs, outs):
+        oq, os_, oamax, osg = oracle.quantize(synth.as_oracle_array(x), 16)
+        assert_bytes_equal("pipeline codes", q.numpy(), oq)
+        assert_bytes_equal("pipeline scales", s.numpy(), os_)
+        assert np.float32(sg.item()) == osg
+    hqz.close()
+
+
+def test_host_quantizer_matches_oracle_on_a_workload():
     w = synth.WORKLOADS["bf16_4096x4096"]
     x_host = synth.generate(w).pin_memory()
     hqz = hq.HostQuantizer(w.M, w.K, torch.bfloat16, 16)
@@ -230,3 +253,4 @@ def test_host_quantizer_matches_device_path():
     assert_bytes_equal("host codes", qh.numpy(), oq)
     assert_bytes_equal("host scales", sh.numpy(), os_)
     assert np.float32(sg) == osg
+    hqz.close()
