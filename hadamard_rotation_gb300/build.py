@@ -13,7 +13,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "hq.cu"), os.path.join(CSRC, "hq_host.cu")]
+SOURCES = [os.path.join(CSRC, "hq.cu"), os.path.join(CSRC, "hq_host.cu"),
+           os.path.join(CSRC, "hq_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "hq_kernels.cuh"), os.path.join(CSRC, "hq_internal.h"),
                   os.path.join(INCLUDE, "hq.h")]
 LIB = os.path.join(PKG, "libhq.so")

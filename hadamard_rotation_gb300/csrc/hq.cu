@@ -273,6 +273,8 @@ const char* hq_status_string(hq_status status) {
     case HQ_ERR_DTYPE: return "HQ_ERR_DTYPE: unknown element type";
     case HQ_ERR_GROUP: return "HQ_ERR_GROUP: rotation group must be 0, 16 or 256";
     case HQ_ERR_CUDA: return "HQ_ERR_CUDA: CUDA runtime error";
+    case HQ_ERR_TOO_LARGE:
+      return "HQ_ERR_TOO_LARGE: tensor exceeds the fixed scratch of the allocation-free entry point";
   }
   return "unknown hq_status";
 }

@@ -63,7 +63,9 @@ typedef enum {
   HQ_ERR_ALIGN = 3, /* a pointer or the row stride breaks the alignment rules below */
   HQ_ERR_DTYPE = 4, /* unknown element type */
   HQ_ERR_GROUP = 5, /* rotation group not in {0, 16, 256} */
-  HQ_ERR_CUDA = 6   /* the CUDA runtime refused a launch or an enqueue */
+  HQ_ERR_CUDA = 6,  /* the CUDA runtime refused a launch or an enqueue */
+  HQ_ERR_TOO_LARGE = 7 /* the tensor does not fit the fixed scratch of
+                          hq_quantize_nvfp4_host_noalloc */
 } hq_status;
 
 typedef enum {
@@ -176,6 +178,39 @@ HQ_API hq_status hq_host_pipeline_wait(hq_host_pipeline* p);
 
 /* Wait for outstanding work, then release the streams, events and the object (NULL is a no-op). */
 HQ_API hq_status hq_host_pipeline_destroy(hq_host_pipeline* p);
+
+/*
+ * hq_quantize_nvfp4_host_noalloc -- the quantization of one host tensor with no device
+ * allocation at all.  The pages have no counterpart: this entry point is for callers that cannot
+ * obtain device memory themselves.  Examples: a plug-in loaded into a host program that owns the
+ * whole device memory pool and hands its extensions no allocator; a serving loop that fixed its
+ * memory footprint at start-up and must not allocate on the request path (an allocation there
+ * can fail, or stall on the allocator).  Those callers can neither provide the workspace of the
+ * host pipeline nor let the library allocate one.
+ *
+ * It does what one submission of the host pipeline does, in order on `stream`: copy x_host to the
+ * device, hq_rot_amax, hq_rotate_quant_nvfp4, copy the codes, scales and s_global back.  Results
+ * are complete when `stream` reaches that point (synchronize it, or record an event).  Its
+ * device staging is one fixed array of HQ_NOALLOC_SCRATCH_BYTES inside the library, reserved on
+ * every device where the library is loaded and held until the process exits.
+ *
+ *   Limit: the tensor must fit that array: with n = M*K and e = 2 (bf16) or 4 (fp32) bytes,
+ *   r(b) = b rounded up to a multiple of 256, it needs r(n e) + r(n/2) + r(n/16) + 512 bytes
+ *   (about 13.1 million bf16 or 7.35 million fp32 elements).  Larger tensors return
+ *   HQ_ERR_TOO_LARGE before anything is enqueued.
+ *   Set-up: the first call on a device looks up the array's device address (once per device,
+ *   with that device current), so make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its contents there; calls
+ *   whose work overlaps on the GPU (other streams, other host threads) race on it, so order
+ *   them (one stream, or events).  The call clears what must start at zero (the amax).
+ *   Host buffers should be pinned for the copies to be asynchronous.  x_host: [M, K] of dtype,
+ *   contiguous rows; q_host: [M, K/2]; scales_host: [M, K/16]; s_global_host: 1 float.
+ */
+#define HQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+HQ_API hq_status hq_quantize_nvfp4_host_noalloc(const void* x_host, hq_dtype dtype, int64_t M,
+                                                int64_t K, int group, uint8_t* q_host,
+                                                uint8_t* scales_host, float* s_global_host,
+                                                hq_stream stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 HQ_API int hq_version(void);
