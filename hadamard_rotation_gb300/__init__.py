@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     hq_dequant_nvfp4,
     hq_rot_amax,
     hq_rotate_quant_nvfp4,
+    hq_rotate_quant_nvfp4_delayed,
     quantize_nvfp4,
 )
 
@@ -18,6 +19,7 @@ __all__ = [
     "hq_dequant_nvfp4",
     "hq_rot_amax",
     "hq_rotate_quant_nvfp4",
+    "hq_rotate_quant_nvfp4_delayed",
     "lib_path",
     "load",
     "quantize_nvfp4",

@@ -79,6 +79,26 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     return q, scales, s_global
 
 
+def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.Tensor,
+                                  amax_next: torch.Tensor | None = None,
+                                  q: torch.Tensor | None = None,
+                                  scales: torch.Tensor | None = None,
+                                  s_global: torch.Tensor | None = None,
+                                  stream: torch.cuda.Stream | None = None):
+    """Single pass with a delayed amax: quantize with ``amax_prev`` and reduce this tensor's
+    amax into ``amax_next``.  Returns (q, scales, s_global, amax_next)."""
+    dt, M, K, ldx = _x_args(x)
+    amax_prev = _need(amax_prev, (1,), torch.float32, x.device, "amax_prev")
+    amax_next = _need(amax_next, (1,), torch.float32, x.device, "amax_next")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    check(_lib.load().hq_rotate_quant_nvfp4_delayed(
+        _ptr(x), dt, M, K, ldx, group, _ptr(amax_prev), _ptr(amax_next), _ptr(q), _ptr(scales),
+        _ptr(s_global), _stream_handle(stream)), "hq_rotate_quant_nvfp4_delayed")
+    return q, scales, s_global, amax_next
+
+
 def hq_dequant_nvfp4(q: torch.Tensor, scales: torch.Tensor, s_global: torch.Tensor, group: int,
                      unrotate: bool, out: torch.Tensor | None = None,
                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:

@@ -175,16 +175,16 @@ hq_status dispatch_rot_amax(const hq::Params& p, bool bf16, bool strided, bool w
                  : launch_rot_amax<G, false, kMode>(p, write_y, s);
 }
 
-template <int G>
+template <int G, bool NEXT>
 hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream s) {
   using hq::k_rotate_quant_nvfp4;
   constexpr int kMode = HQ_PASS2_MODE;
   if (bf16)
-    return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided>, p, s)
-                   : launch(k_rotate_quant_nvfp4<G, true, kMode>, p, s,
+    return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided, NEXT>, p, s)
+                   : launch(k_rotate_quant_nvfp4<G, true, kMode, NEXT>, p, s,
                             ring_bytes<HQ_PASS2_STAGES>(kMode, true));
-  return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided>, p, s)
-                 : launch(k_rotate_quant_nvfp4<G, false, kMode>, p, s,
+  return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided, NEXT>, p, s)
+                 : launch(k_rotate_quant_nvfp4<G, false, kMode, NEXT>, p, s,
                           ring_bytes<HQ_PASS2_STAGES>(kMode, false));
 }
 
@@ -231,9 +231,41 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
   const bool bf16 = dtype == HQ_BF16;
   const bool strided = is_strided(M, K, ldx);
   switch (group) {
-    case 0: return dispatch_quant<0>(p, bf16, strided, stream);
-    case 16: return dispatch_quant<16>(p, bf16, strided, stream);
-    default: return dispatch_quant<256>(p, bf16, strided, stream);
+    case 0: return dispatch_quant<0, false>(p, bf16, strided, stream);
+    case 16: return dispatch_quant<16, false>(p, bf16, strided, stream);
+    default: return dispatch_quant<256, false>(p, bf16, strided, stream);
+  }
+}
+
+hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                        int64_t ldx, int group, const float* amax_prev,
+                                        float* amax_next, uint8_t* q, uint8_t* scales,
+                                        float* s_global, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (!amax_next) return HQ_ERR_NULL;
+  if (!aligned(amax_next, 4)) return HQ_ERR_ALIGN;
+  if (M > 0 && K > 0) {
+    if (!amax_prev || !q || !scales || amax_prev == amax_next) return HQ_ERR_NULL;
+    if (!aligned(amax_prev, 4) || !aligned(q, 16) || !aligned(scales, 4) ||
+        (s_global && !aligned(s_global, 4)))
+      return HQ_ERR_ALIGN;
+  }
+  cudaError_t e = cudaMemsetAsync(amax_next, 0, sizeof(float), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (M == 0 || K == 0) return HQ_OK;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.amax_in = amax_prev;
+  p.amax_out = amax_next;
+  p.q = q;
+  p.s = scales;
+  p.sglobal_out = s_global;
+  const bool bf16 = dtype == HQ_BF16;
+  const bool strided = is_strided(M, K, ldx);
+  switch (group) {
+    case 0: return dispatch_quant<0, true>(p, bf16, strided, stream);
+    case 16: return dispatch_quant<16, true>(p, bf16, strided, stream);
+    default: return dispatch_quant<256, true>(p, bf16, strided, stream);
   }
 }
 

@@ -119,21 +119,38 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return d;
 }
 
-// Three-input max (sm_100 family).
-__device__ __forceinline__ float max3(float a, float b, float c) {
+// Three-input max that keeps a NaN (sm_100 family).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
   float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-// max |v[i]| over 16 values (the .x or .y lane of each pair), exact.
+// max |v[i]| over 16 values (the .x or .y lane of each pair), exact; NaN if any is NaN.
 template <bool Y>
 __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
   auto g = [&](int i) { return fabsf(Y ? v[i].y : v[i].x); };
-  float m = max3(g(0), g(1), g(2));
+  float m = max3_nan(g(0), g(1), g(2));
 #pragma unroll
-  for (int i = 3; i < 15; i += 2) m = max3(m, g(i), g(i + 1));
-  return fmaxf(m, g(15));
+  for (int i = 3; i < 15; i += 2) m = max3_nan(m, g(i), g(i + 1));
+  return max_nan(m, g(15));
+}
+
+// max over the CTA of each thread's `v`, then one atomicMax into *out.  Non-negative
+// floats (and NaN, with the sign bit clear) order like their bit patterns as unsigned
+// integers.  Every thread of the CTA must call this.
+__device__ __forceinline__ void cta_amax_to_global(float v, float* out) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = max_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  __shared__ float red[kWarpsPerCta];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarpsPerCta; ++w) m = max_nan(m, red[w]);
+    atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(m));
+  }
 }
 
 // a / b rounded to nearest even from r = RN(1/b), by Markstein's correction
@@ -594,29 +611,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_rot_amax(Params p) {
       }
     }
   });
-  // max over the CTA, then one atomic per CTA.  |y| = RN(|z| / sqrt(G)) is
-  // monotone in |z|, so max |y| = RN(max |z| / sqrt(G)) exactly.
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) zmax = max_nan(zmax, __shfl_xor_sync(0xFFFFFFFFu, zmax, m));
-  __shared__ float red[kWarpsPerCta];
-  if (lane == 0) red[threadIdx.x >> 5] = zmax;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarpsPerCta; ++w) m = max_nan(m, red[w]);
-    const float a = __fmul_rn(m, inv_sqrt_g<G>());
-    // non-negative floats (and NaN, with the sign cleared by fabs) order like
-    // their bit patterns as unsigned integers.
-    atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(a));
-  }
+  // |y| = RN(|z| / sqrt(G)) is monotone in |z|, so max |y| = RN(max |z| / sqrt(G))
+  // exactly; the scaling commutes with the max over the CTA.
+  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), p.amax_out);
 }
 
 // ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
-template <int G, bool BF16, int MODE>
+// REDUCE_NEXT: also reduce this tensor's amax into p.amax_out (zeroed by the host
+// call) while quantizing with the given one -- the single-pass, delayed-amax mode.
+template <int G, bool BF16, int MODE, bool REDUCE_NEXT>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   // s_global = amax / (448 * 6), or 1 if that is 0.
   const float amax = *p.amax_in;
@@ -631,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
+  float next_amax = 0.0f;  // max of the block amaxes this thread saw (REDUCE_NEXT)
 
   for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
@@ -643,6 +649,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
       am[2 * k] = __fmul_rn(block_absmax<false>(t.P[k]), c);
       am[2 * k + 1] = __fmul_rn(block_absmax<true>(t.P[k]), c);
     }
+    if constexpr (REDUCE_NEXT)
+      next_amax = max3_nan(next_amax, max_nan(am[0], am[1]), max_nan(am[2], am[3]));
 
     // Block scales: v = (amax_b / 6) / s_global, two correctly rounded
     // divisions, then E4M3 (RNE, satfinite).  The Markstein form is exact for
@@ -732,6 +740,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
       __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
     }
   });
+  if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
 }
 
 // ---------------------------------------------------------------------------

@@ -58,7 +58,7 @@ extern "C" {
 
 typedef enum {
   HQ_OK = 0,
-  HQ_ERR_NULL = 1,  /* a required pointer is NULL */
+  HQ_ERR_NULL = 1,  /* a required pointer is NULL (or two that must differ are the same) */
   HQ_ERR_SHAPE = 2, /* M < 0, K < 0, ldx < K, or K not a multiple of max(16, G) */
   HQ_ERR_ALIGN = 3, /* a pointer or the row stride breaks the alignment rules below */
   HQ_ERR_DTYPE = 4, /* unknown element type */
@@ -108,6 +108,29 @@ HQ_API hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K
 HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
+
+/*
+ * hq_rotate_quant_nvfp4_delayed -- single-pass mode: quantize with an amax kept from an earlier
+ *   step while reducing this tensor's amax for the next one.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2, on the global scale:
+ *    production stacks run a small amax reduction ahead of the kernel *or reuse an amax from a
+ *    previous step*, so that the per-block work stays a single pass.)
+ *
+ *   Reads x once.  Codes, scales and s_global are exactly those of hq_rotate_quant_nvfp4 with
+ *   amax = *amax_prev; *amax_next receives max |y| of this tensor, exactly as hq_rot_amax would
+ *   (this call zeroes it first, on `stream`).  When *amax_prev is smaller than this tensor's
+ *   amax, blocks whose scale would exceed 448 saturate (scale 448, codes clipped at 6): the
+ *   price of a stale global scale.
+ *
+ *   x, dtype, M, K, ldx, group, q, scales, s_global : as for hq_rotate_quant_nvfp4.
+ *   amax_prev : 1 float on the device (read).      amax_next : 1 float on the device (written).
+ *   The two must be different floats; passing the same pointer returns HQ_ERR_NULL.
+ */
+HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M,
+                                               int64_t K, int64_t ldx, int group,
+                                               const float* amax_prev, float* amax_next,
+                                               uint8_t* q, uint8_t* scales, float* s_global,
+                                               hq_stream stream);
 
 /*
  * hq_dequant_nvfp4 -- round trip for checks (not part of the quantization hot path).

@@ -165,3 +165,16 @@ def test_host_pipeline_argument_checks(lib):
     assert lib.hq_host_pipeline_submit(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE)) == 1
     assert lib.hq_host_pipeline_wait(None) == 1
     assert lib.hq_host_pipeline_destroy(None) == 0
+
+
+def test_delayed_argument_checks(lib):
+    def dl(x=FAKE, dt=1, M=4, K=32, ldx=32, G=16, prev=FAKE, nxt=FAKE + 64, q=FAKE, s=FAKE, sg=None):
+        return lib.hq_rotate_quant_nvfp4_delayed(
+            P(x) if x else None, dt, M, K, ldx, G, P(prev) if prev else None,
+            P(nxt) if nxt else None, P(q) if q else None, P(s) if s else None,
+            P(sg) if sg else None, None)
+    assert dl(nxt=0) == 1
+    assert dl(prev=0) == 1 and dl(q=0) == 1 and dl(s=0) == 1
+    assert dl(prev=FAKE + 64) == 1        # the two amax pointers alias
+    assert dl(G=32) == 5 and dl(dt=3) == 4 and dl(K=24, ldx=24) == 2
+    assert dl(nxt=FAKE + 66) == 3 and dl(q=FAKE + 8) == 3
