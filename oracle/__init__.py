@@ -15,8 +15,10 @@ from .hq_oracle import (  # noqa: F401
     e4m3_codes_bits,
     e4m3_values,
     global_scale,
+    int8_rotate,
     lib_path,
     quantize,
     rot_amax,
     rotate,
+    rotate_quant_int8,
 )

@@ -360,3 +360,79 @@ void hqo_e4m3_values(const uint8_t* codes, int64_t n, float* out) {
 float hqo_global_scale(float amax) { return global_scale(amax); }
 
 }  // extern "C"
+
+// ===========================================================================
+// INT8 per-token rotate-quant ("hyperflow_h3_flash_int8.py", HyperFlow: module
+// docstring, regular_hadamard, rotate_quant_kernel).
+//
+//   R_G      = kron(H4/2, ..., H4/2) (G a power of 4), with
+//              H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]]: orthonormal,
+//              symmetric, rows summing to one.
+//   y        = x . R_G on every run of G consecutive channels of a row.
+//   scale    = max(amax_row |y|, 1e-12) / 127 (one per row, fp32)
+//   inv      = 1 / scale
+//   q        = clamp(rint(y * inv), -127, 127) as int8 (round half to even).
+//
+// Readings (the page's rotation is a tensor-core dot product of unspecified
+// order): the Kronecker factors are applied digit by digit, least significant
+// base-4 digit (contiguous channels) first, as the page's factored kernel does
+// (inner factor, then outer).  H4 = J - 2 P (J all ones, P the exchange matrix),
+// so one 4-point step of H4/2 on (v0, v1, v2, v3) is out_k = S/2 - v_(3-k) with
+// S = (v0 + v1) + (v2 + v3); out_k is rounded once (fmaf: S/2 is exact inside).
+// ===========================================================================
+namespace {
+
+void regular_hadamard_group(float* z, int G) {
+  for (int stride = 1; stride < G; stride *= 4) {
+    for (int base = 0; base < G; ++base) {
+      if ((base / stride) % 4 != 0) continue;  // base has digit 0 at this position
+      float v[4];
+      for (int k = 0; k < 4; ++k) v[k] = z[base + k * stride];
+      const float S = (v[0] + v[1]) + (v[2] + v[3]);
+      for (int k = 0; k < 4; ++k) z[base + k * stride] = std::fmaf(0.5f, S, -v[3 - k]);
+    }
+  }
+}
+
+bool int8_group_ok(int G) { return G == 4 || G == 16 || G == 64 || G == 256 || G == 1024; }
+
+}  // namespace
+
+extern "C" {
+
+// y = x . R_G on a flat array of n values (n % G == 0).
+int hqo_int8_rotate(const float* in, int64_t n, int group, float* out) {
+  if (!in || !out || n < 0 || !int8_group_ok(group) || n % group != 0) return HQO_ERR_ARG;
+  std::memcpy(out, in, sizeof(float) * n);
+  for (int64_t g0 = 0; g0 < n; g0 += group) regular_hadamard_group(out + g0, group);
+  return HQO_OK;
+}
+
+// q: int8 [M, K] (row stride K); scales: fp32 [M].
+int hqo_rotate_quant_int8(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, int group,
+                          int8_t* q, float* scales, int nthreads) {
+  if (!x || !q || !scales || M < 0 || K < 0 || ldx < K) return HQO_ERR_ARG;
+  if (!int8_group_ok(group) || K % group != 0) return HQO_ERR_ARG;
+  if (dtype != DT_F32 && dtype != DT_BF16) return HQO_ERR_ARG;
+  parallel_rows(M, nthreads, [&](int64_t r0, int64_t r1, int) {
+    std::vector<float> y(static_cast<size_t>(K));
+    for (int64_t r = r0; r < r1; ++r) {
+      for (int64_t k = 0; k < K; ++k) y[k] = load_elem(x, dtype, r * ldx + k);
+      for (int64_t g0 = 0; g0 < K; g0 += group) regular_hadamard_group(y.data() + g0, group);
+      float amax = 0.0f;
+      for (int64_t k = 0; k < K; ++k) amax = amax_update(amax, std::fabs(y[k]));
+      const float scale = ((amax > 1e-12f) ? amax : 1e-12f) / 127.0f;
+      const float inv = 1.0f / scale;
+      scales[r] = scale;
+      for (int64_t k = 0; k < K; ++k) {
+        float v = std::rint(y[k] * inv);
+        if (v > 127.0f) v = 127.0f;
+        if (v < -127.0f) v = -127.0f;
+        q[r * K + k] = static_cast<int8_t>(v);
+      }
+    }
+  });
+  return HQO_OK;
+}
+
+}  // extern "C"

@@ -64,6 +64,10 @@ def _load():
             lib.hqo_e4m3_codes_bits.restype = None
             lib.hqo_e4m3_values.argtypes = [p, i64, p]
             lib.hqo_e4m3_values.restype = None
+            lib.hqo_int8_rotate.argtypes = [p, i64, i32, p]
+            lib.hqo_int8_rotate.restype = i32
+            lib.hqo_rotate_quant_int8.argtypes = [p, i32, i64, i64, i64, i32, p, p, i32]
+            lib.hqo_rotate_quant_int8.restype = i32
             lib.hqo_global_scale.argtypes = [ctypes.c_float]
             lib.hqo_global_scale.restype = ctypes.c_float
             _lib = lib
@@ -190,3 +194,26 @@ def e4m3_values(codes: np.ndarray) -> np.ndarray:
 
 def global_scale(amax: float) -> float:
     return float(_load().hqo_global_scale(ctypes.c_float(amax)))
+
+
+def int8_rotate(x: np.ndarray, group: int) -> np.ndarray:
+    """y = x . R_G (regular Hadamard) on every run of `group` values."""
+    lib = _load()
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty_like(x)
+    if lib.hqo_int8_rotate(_ptr(x), x.size, group, _ptr(out)):
+        raise ValueError("hqo_int8_rotate: bad arguments")
+    return out
+
+
+def rotate_quant_int8(x: np.ndarray, group: int, nthreads: int | None = None):
+    """Return (q int8 [M, K], scales float32 [M])."""
+    lib = _load()
+    M, K, ldx = _check2d(x)
+    q = np.empty((M, K), np.int8)
+    sc = np.empty(M, np.float32)
+    rc = lib.hqo_rotate_quant_int8(_ptr(x), _x_dtype(x), M, K, ldx, group, _ptr(q), _ptr(sc),
+                                   _threads(nthreads))
+    if rc:
+        raise ValueError("hqo_rotate_quant_int8: bad arguments")
+    return q, sc
