@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     HostQuantizer,
     hq_dequant_nvfp4,
     hq_rot_amax,
+    hq_rotate_quant_int8,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
     quantize_nvfp4,
@@ -18,6 +19,7 @@ __all__ = [
     "HostQuantizer",
     "hq_dequant_nvfp4",
     "hq_rot_amax",
+    "hq_rotate_quant_int8",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
     "lib_path",

@@ -99,6 +99,18 @@ def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.
     return q, scales, s_global, amax_next
 
 
+def hq_rotate_quant_int8(x: torch.Tensor, group: int, q: torch.Tensor | None = None,
+                         scales: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None):
+    """INT8 per-token rotate-quant: (q int8 [M, K], scales float32 [M])."""
+    dt, M, K, ldx = _x_args(x)
+    q = _need(q, (M, K), torch.int8, x.device, "q")
+    scales = _need(scales, (M,), torch.float32, x.device, "scales")
+    check(_lib.load().hq_rotate_quant_int8(_ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
+                                           _stream_handle(stream)), "hq_rotate_quant_int8")
+    return q, scales
+
+
 def hq_dequant_nvfp4(q: torch.Tensor, scales: torch.Tensor, s_global: torch.Tensor, group: int,
                      unrotate: bool, out: torch.Tensor | None = None,
                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:

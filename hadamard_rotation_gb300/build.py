@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "hq.cu"), os.path.join(CSRC, "hq_host.cu"),
            os.path.join(CSRC, "hq_noalloc.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "hq_kernels.cuh"), os.path.join(CSRC, "hq_internal.h"),
+DEPS = SOURCES + [os.path.join(CSRC, "hq_kernels.cuh"), os.path.join(CSRC, "hq_int8.cuh"),
+                  os.path.join(CSRC, "hq_internal.h"),
                   os.path.join(INCLUDE, "hq.h")]
 LIB = os.path.join(PKG, "libhq.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

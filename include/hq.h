@@ -133,6 +133,28 @@ HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, in
                                                hq_stream stream);
 
 /*
+ * hq_rotate_quant_int8 -- INT8 per-token rotate-quant with the regular Hadamard.
+ *   ("hyperflow_h3_flash_int8.py", HyperFlow: regular_hadamard, rotate_quant_kernel; the
+ *    activation side of a W8A8 linear whose weight was rotated offline.)
+ *
+ *   y      = x . R_G on every run of G consecutive channels of a row, R_G = kron(H4/2, ...),
+ *            H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]] (orthonormal, symmetric, rows
+ *            summing to one).  Fixed fp32 order: the base-4 digits of the channel index from the
+ *            least significant, each 4-point step out_k = RN(S/2 - v_(3-k)),
+ *            S = (v0 + v1) + (v2 + v3).
+ *   scales : fp32 [M], scale = max(amax_row |y|, 1e-12) / 127.
+ *   q      : int8 [M, K] row-major, q = clamp(rint(y * (1/scale)), -127, 127) (half to even).
+ *   x is read once; the rotated row stays on chip.
+ *
+ *   group  : 16, 64 or 256; K a multiple of group and at most 32768.
+ *   x      : [M, K] of dtype, row stride ldx (16-byte aligned; ldx * sizeof(dtype) % 16 == 0).
+ *   q      : 16-byte aligned.   scales : 4-byte aligned.
+ */
+HQ_API hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                      int64_t ldx, int group, int8_t* q, float* scales,
+                                      hq_stream stream);
+
+/*
  * hq_dequant_nvfp4 -- round trip for checks (not part of the quantization hot path).
  *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2 dequantize:
  *    value = (+-grid[code & 7]) * (s_block * s_global), then the rotation applied again when the

@@ -178,3 +178,17 @@ def test_delayed_argument_checks(lib):
     assert dl(prev=FAKE + 64) == 1        # the two amax pointers alias
     assert dl(G=32) == 5 and dl(dt=3) == 4 and dl(K=24, ldx=24) == 2
     assert dl(nxt=FAKE + 66) == 3 and dl(q=FAKE + 8) == 3
+
+
+def test_int8_argument_checks(lib):
+    def i8(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, q=FAKE, s=FAKE):
+        return lib.hq_rotate_quant_int8(P(x) if x else None, dt, M, K, ldx, G, P(q) if q else None,
+                                        P(s) if s else None, None)
+    assert i8(x=0) == 1 and i8(q=0) == 1 and i8(s=0) == 1
+    assert i8(G=32) == 5 and i8(G=0) == 5 and i8(G=4) == 5
+    assert i8(dt=2) == 4
+    assert i8(K=48, ldx=48, G=64) == 2 and i8(K=32768 + 256, ldx=32768 + 256, G=256) == 2
+    assert i8(ldx=32) == 2 and i8(M=-1) == 2
+    assert i8(x=FAKE + 8) == 3 and i8(q=FAKE + 4) == 3 and i8(s=FAKE + 2) == 3
+    assert i8(ldx=68) == 3                     # 136-byte bf16 row stride
+    assert i8(M=0) == 0

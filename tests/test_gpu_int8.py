@@ -1,0 +1,87 @@
+"""INT8 per-token rotate-quant (hq_rotate_quant_int8) against the oracle, bit-exact.
+
+"hyperflow_h3_flash_int8.py" (HyperFlow): regular_hadamard, rotate_quant_kernel.  Shapes cover
+one and several warp tiles per row (2048 channels each), ragged last tiles, 1 to 16 rows per CTA
+step, both input types, strided rows, zero rows (the 1e-12 floor) and extreme magnitudes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hadamard_rotation_gb300 as hq
+import oracle
+from hadamard_rotation_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from hadamard_rotation_gb300 import build
+
+    build.build()
+    oracle.build()
+    hq.load()
+
+
+def rand_input(M, K, dtype, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32) * np.float32(scale)
+    if K >= 64:
+        x[:, rng.choice(K, max(1, K // 100), replace=False)] *= 40.0
+    if M > 2:
+        x[1] = 0.0
+    t = torch.from_numpy(x)
+    return t if dtype == torch.float32 else t.to(dtype)
+
+
+def check(x_host, group, x_dev=None):
+    x = x_dev if x_dev is not None else x_host.cuda()
+    q, s = hq.hq_rotate_quant_int8(x, group)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.rotate_quant_int8(synth.as_oracle_array(x_host), group)
+    gs = s.cpu().numpy()
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32)), "scales differ"
+    gq = q.cpu().numpy()
+    if not np.array_equal(gq, oq):
+        bad = np.argwhere(gq != oq)
+        raise AssertionError(f"{len(bad)} codes differ, first {bad[:5].tolist()}")
+
+
+SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16), (9, 2304, 256),
+          (100, 4096, 64), (7, 32768, 256), (1000, 1024, 16), (301, 3072, 64), (64, 6144, 256),
+          (40, 30720, 16)]
+
+
+@pytest.mark.parametrize("M,K,group", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_int8_parity(M, K, group, dtype):
+    check(rand_input(M, K, dtype, seed=M + K + group), group)
+
+
+@pytest.mark.parametrize("group", [16, 64, 256])
+def test_int8_strided_rows(group):
+    big = rand_input(300, 4096 + 512, torch.bfloat16, seed=4)
+    check(big[:, :4096].contiguous(), group, x_dev=big.cuda()[:, :4096])
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-14, 1e30])
+def test_int8_extreme_magnitudes(scale):
+    for group in (16, 64, 256):
+        check(rand_input(50, 1024, torch.float32, seed=9, scale=scale), group)
+
+
+def test_int8_llm_sized_workload():
+    w = synth.Workload("int8_bf16_8192x8192", 8192, 8192, "bf16", 5, "normal", (256,),
+                       outlier_frac=0.01, outlier_factor=50.0)
+    x = synth.generate(w)
+    for group in (64, 256):
+        check(x, group)
+
+
+def test_int8_empty_and_limits():
+    x = torch.empty(0, 256, device="cuda", dtype=torch.bfloat16)
+    q, s = hq.hq_rotate_quant_int8(x, 256)
+    assert q.numel() == 0
+    with pytest.raises(hq.HQError):
+        hq.hq_rotate_quant_int8(torch.zeros(2, 32768 + 256, device="cuda", dtype=torch.bfloat16), 256)
