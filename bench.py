@@ -315,6 +315,30 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     single_ms = d0.elapsed_time(d1) / K
 
+    # ---- INT8 per-token rotate-quant (regular Hadamard, G = 256) on the same tensor ----
+    int8 = None
+    if w.K <= 32768 and w.K % 256 == 0:
+        q8 = torch.empty((w.M, w.K), dtype=torch.int8, device=dev)
+        s8 = torch.empty(w.M, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            hq.hq_rotate_quant_int8(x, 256, q=q8, scales=s8, stream=stream)
+        torch.cuda.synchronize(dev)
+        i0 = torch.cuda.Event(enable_timing=True)
+        i1 = torch.cuda.Event(enable_timing=True)
+        i0.record(stream)
+        for _ in range(K):
+            hq.hq_rotate_quant_int8(x, 256, q=q8, scales=s8, stream=stream)
+            if flush is not None:
+                flush.fill_(1.0)
+        i1.record(stream)
+        torch.cuda.synchronize(dev)
+        i8_ms = i0.elapsed_time(i1) / K
+        i8_bytes = bytes_in + w.numel + 4 * w.M
+        int8 = {"group": 256, "ms_per_launch": i8_ms, "bytes_per_launch": i8_bytes,
+                "gbs": i8_bytes / (i8_ms / 1e3) / 1e9,
+                "note": "hq_rotate_quant_int8 (x read once, int8 codes + fp32 per-row scales)"}
+        del q8, s8
+
     # ---- end to end through the public API, host buffers ----
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
     del q, s  # the host pipeline holds its own device buffers
@@ -341,6 +365,8 @@ def run_ours(args, w):
 
     # ---- roofline of the dominant kernel (pass 2) ----
     peak, peak_kind = load_peaks()
+    if int8 is not None:
+        int8["frac_of_peak"] = int8["gbs"] / peak
     p2 = sum(pass2) / K
     p1 = sum(pass1) / K
     achieved = step_bytes / (p2 / 1e3) / 1e9
@@ -370,6 +396,7 @@ def run_ours(args, w):
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
             "note": "hq_rotate_quant_nvfp4_delayed: quantize with the previous step's amax while "
                     "reducing this one (one read of x); not the metric's two-pass step"},
+        "int8_per_token": int8,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": hqz.h2d_bytes,
                 "d2h_bytes_per_step": hqz.d2h_bytes, "steps": e2e_steps,
                 "ms_per_step": e2e_ms / e2e_steps, "api": "HostQuantizer (hq_host_pipeline_*)",

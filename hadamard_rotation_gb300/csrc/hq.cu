@@ -165,9 +165,20 @@ hq_status launch_rot_amax(const hq::Params& p, bool write_y, hq_stream s) {
                  : launch(hq::k_rot_amax<G, BF16, MODE, false>, p, s, smem);
 }
 
+// Pass 1 for G <= 16 on contiguous, 32-byte aligned rows uses the streaming kernel
+// (1 = on).
+#ifndef HQ_PASS1_STREAM
+#define HQ_PASS1_STREAM 1
+#endif
+
 template <int G>
 hq_status dispatch_rot_amax(const hq::Params& p, bool bf16, bool strided, bool write_y,
                             hq_stream s) {
+  if constexpr (G <= 16) {
+    if (HQ_PASS1_STREAM && !strided && !write_y && aligned(p.x, 32))
+      return bf16 ? launch(hq::k_rot_amax_stream<G, true>, p, s)
+                  : launch(hq::k_rot_amax_stream<G, false>, p, s);
+  }
   constexpr int kMode = HQ_PASS1_MODE;
   if (bf16)
     return strided ? launch_rot_amax<G, true, hq::kLoadStrided>(p, write_y, s)

@@ -617,6 +617,92 @@ __global__ void __launch_bounds__(kThreads, 1) k_rot_amax(Params p) {
 }
 
 // ---------------------------------------------------------------------------
+// Pass 1, streaming form for G <= 16 on contiguous rows: every thread takes two
+// whole blocks per step (block b and b + S, S = threads in the grid), each with
+// one 256-bit load per 32 bytes, and keeps the next two in flight while it
+// rotates the current pair.  It needs no shared memory and about 60 registers,
+// so 32 warps per SM keep 64 KB of loads outstanding; x must be 32-byte aligned.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ld_v8_stream(const uint8_t* src, uint32_t* w) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+        "=r"(w[7])
+      : "l"(src));
+}
+
+#ifndef HQ_STREAM_DEPTH
+#define HQ_STREAM_DEPTH 1
+#endif
+
+template <int G, bool BF16>
+__global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_amax_stream(Params p) {
+  constexpr int kWords = BF16 ? 8 : 16;  // 32-bit words per 16-element block
+  const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;
+  uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  auto load = [&](uint64_t blk, uint32_t (&w)[kWords]) {
+    if (blk < p.nb) {
+      const uint8_t* src = p.x + blk * (16u * (BF16 ? 2u : 4u));
+#pragma unroll
+      for (int k = 0; k < kWords; k += 8) ld_v8_stream(src + 4 * k, w + k);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kWords; ++k) w[k] = 0u;
+    }
+  };
+  auto value = [&](const uint32_t (&w)[kWords], int i) {
+    if constexpr (BF16)
+      return __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+    else
+      return __uint_as_float(w[i]);
+  };
+  float zmax = 0.0f;
+  auto consume = [&](const uint32_t (&a)[kWords], const uint32_t (&c)[kWords]) {
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = make_float2(value(a, i), value(c, i));
+    if constexpr (G == 16) butterfly16(v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) zmax = max3_nan(zmax, fabsf(v[i].x), fabsf(v[i].y));
+  };
+#if HQ_STREAM_DEPTH == 1
+  uint32_t wa[kWords], wb[kWords];
+  load(b, wa);
+  load(b + S, wb);
+  for (; b < p.nb; b += 2 * S) {
+    uint32_t ca[kWords], cb[kWords];
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) { ca[k] = wa[k]; cb[k] = wb[k]; }
+    load(b + 2 * S, wa);
+    load(b + 3 * S, wb);
+    consume(ca, cb);
+  }
+#else
+  // two pairs in flight: (wa, wb) for step b, (wc, wd) for step b + 2S
+  uint32_t wa[kWords], wb[kWords], wc[kWords], wd[kWords];
+  load(b, wa);
+  load(b + S, wb);
+  load(b + 2 * S, wc);
+  load(b + 3 * S, wd);
+  for (; b < p.nb; b += 4 * S) {
+    uint32_t ca[kWords], cb[kWords];
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) { ca[k] = wa[k]; cb[k] = wb[k]; }
+    load(b + 4 * S, wa);
+    load(b + 5 * S, wb);
+    consume(ca, cb);
+    if (b + 2 * S >= p.nb) break;
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) { ca[k] = wc[k]; cb[k] = wd[k]; }
+    load(b + 6 * S, wc);
+    load(b + 7 * S, wd);
+    consume(ca, cb);
+  }
+#endif
+  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), p.amax_out);
+}
+
+// ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
 // REDUCE_NEXT: also reduce this tensor's amax into p.amax_out (zeroed by the host

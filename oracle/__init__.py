@@ -9,6 +9,7 @@ from .hq_oracle import (  # noqa: F401
     DT_F32,
     build,
     dequant,
+    dequant_mxfp4,
     e2m1_codes,
     e2m1_codes_bits,
     e4m3_codes,
@@ -18,6 +19,7 @@ from .hq_oracle import (  # noqa: F401
     int8_rotate,
     lib_path,
     quantize,
+    quantize_mxfp4,
     rot_amax,
     rotate,
     rotate_quant_int8,

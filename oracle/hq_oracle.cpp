@@ -362,6 +362,89 @@ float hqo_global_scale(float amax) { return global_scale(amax); }
 }  // extern "C"
 
 // ===========================================================================
+// MXFP4: E2M1 codes with one power-of-two (E8M0) scale per 32 consecutive
+// elements of a row, no per-tensor scale ("A Fused Hadamard + NVFP4
+// Quantization Kernel in Triton", §1: "MXFP4 (32-element blocks, power-of-two
+// E8M0 scales)"; "Try this": the same error study with MXFP4 semantics, the
+// rotation applied as before).  The pages give no rule for the scale; the
+// reading adopted is the usual MX rule: X = 2^(floor(log2 amax_b) - 2), 2 being
+// the exponent of E2M1's largest value 6, so amax_b / X lies in [4, 8); the E8M0
+// byte is that exponent + 127, clamped to [0, 254] (0 for an all-zero block);
+// codes are E2M1 (ties to even, saturating at 6) of y / X.
+// ===========================================================================
+namespace {
+
+int e8m0_code(float amax_b) {
+  if (!(amax_b > 0.0f)) return 0;
+  int e2;
+  std::frexp(amax_b, &e2);           // amax_b = m 2^e2, m in [0.5, 1): floor(log2) = e2 - 1
+  int code = (e2 - 1) - 2 + 127;
+  if (code < 0) code = 0;
+  if (code > 254) code = 254;
+  return code;
+}
+
+float e8m0_value(int code) { return std::ldexp(1.0f, code - 127); }
+
+}  // namespace
+
+extern "C" {
+
+// q: [M, K/2] packed codes (even element low), s: [M, K/32] E8M0 bytes.
+int hqo_quantize_mxfp4(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, int group,
+                       uint8_t* q, uint8_t* s, int nthreads) {
+  if (!x || !q || !s || M < 0 || K < 0 || ldx < K) return HQO_ERR_ARG;
+  if (!(group == 0 || group == 16 || group == 256)) return HQO_ERR_ARG;
+  if (K % 32 != 0 || (group > 0 && K % group != 0)) return HQO_ERR_ARG;
+  if (dtype != DT_F32 && dtype != DT_BF16) return HQO_ERR_ARG;
+  parallel_rows(M, nthreads, [&](int64_t r0, int64_t r1, int) {
+    std::vector<float> y(static_cast<size_t>(K));
+    for (int64_t r = r0; r < r1; ++r) {
+      rotate_row(x, dtype, r, K, ldx, group, y.data());
+      for (int64_t b = 0; b < K / 32; ++b) {
+        const float* yb = y.data() + 32 * b;
+        float amax_b = 0.0f;
+        for (int i = 0; i < 32; ++i) amax_b = amax_update(amax_b, std::fabs(yb[i]));
+        const int code = e8m0_code(amax_b);
+        s[r * (K / 32) + b] = static_cast<uint8_t>(code);
+        const float X = e8m0_value(code);
+        uint8_t codes[32];
+        for (int i = 0; i < 32; ++i) codes[i] = e2m1_code(yb[i] / X);
+        for (int j = 0; j < 16; ++j)
+          q[r * (K / 2) + 16 * b + j] =
+              static_cast<uint8_t>(codes[2 * j] | (codes[2 * j + 1] << 4));
+      }
+    }
+  });
+  return HQO_OK;
+}
+
+// value = (+-grid[c & 7]) * X, then the rotation again when `unrotate`.
+int hqo_dequant_mxfp4(const uint8_t* q, const uint8_t* s, int64_t M, int64_t K, int group,
+                      int unrotate, float* out, int nthreads) {
+  if (!q || !s || !out || M < 0 || K < 0 || K % 32 != 0) return HQO_ERR_ARG;
+  if (unrotate && !(group == 16 || group == 256)) return HQO_ERR_ARG;
+  if (unrotate && K % group != 0) return HQO_ERR_ARG;
+  parallel_rows(M, nthreads, [&](int64_t r0, int64_t r1, int) {
+    for (int64_t r = r0; r < r1; ++r) {
+      float* o = out + r * K;
+      for (int64_t k = 0; k < K; ++k) {
+        const uint8_t byte = q[r * (K / 2) + k / 2];
+        const uint8_t c = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+        const float mag = kE2M1Grid[c & 7];
+        const float val = (c & 8) ? -mag : mag;
+        o[k] = val * e8m0_value(s[r * (K / 32) + k / 32]);
+      }
+      if (unrotate)
+        for (int64_t g0 = 0; g0 < K; g0 += group) rotate_group(o + g0, group);
+    }
+  });
+  return HQO_OK;
+}
+
+}  // extern "C"
+
+// ===========================================================================
 // INT8 per-token rotate-quant ("hyperflow_h3_flash_int8.py", HyperFlow: module
 // docstring, regular_hadamard, rotate_quant_kernel).
 //

@@ -68,6 +68,10 @@ def _load():
             lib.hqo_int8_rotate.restype = i32
             lib.hqo_rotate_quant_int8.argtypes = [p, i32, i64, i64, i64, i32, p, p, i32]
             lib.hqo_rotate_quant_int8.restype = i32
+            lib.hqo_quantize_mxfp4.argtypes = [p, i32, i64, i64, i64, i32, p, p, i32]
+            lib.hqo_quantize_mxfp4.restype = i32
+            lib.hqo_dequant_mxfp4.argtypes = [p, p, i64, i64, i32, i32, p, i32]
+            lib.hqo_dequant_mxfp4.restype = i32
             lib.hqo_global_scale.argtypes = [ctypes.c_float]
             lib.hqo_global_scale.restype = ctypes.c_float
             _lib = lib
@@ -217,3 +221,29 @@ def rotate_quant_int8(x: np.ndarray, group: int, nthreads: int | None = None):
     if rc:
         raise ValueError("hqo_rotate_quant_int8: bad arguments")
     return q, sc
+
+
+def quantize_mxfp4(x: np.ndarray, group: int, nthreads: int | None = None):
+    """Return (q [M, K/2] u8, scales [M, K/32] E8M0 u8)."""
+    lib = _load()
+    M, K, ldx = _check2d(x)
+    q = np.empty((M, K // 2), np.uint8)
+    s = np.empty((M, K // 32), np.uint8)
+    rc = lib.hqo_quantize_mxfp4(_ptr(x), _x_dtype(x), M, K, ldx, group, _ptr(q), _ptr(s),
+                                _threads(nthreads))
+    if rc:
+        raise ValueError("hqo_quantize_mxfp4: bad arguments")
+    return q, s
+
+
+def dequant_mxfp4(q: np.ndarray, s: np.ndarray, group: int, unrotate: bool,
+                  nthreads: int | None = None) -> np.ndarray:
+    lib = _load()
+    M, K = q.shape[0], q.shape[1] * 2
+    q = np.ascontiguousarray(q, np.uint8)
+    s = np.ascontiguousarray(s, np.uint8)
+    out = np.empty((M, K), np.float32)
+    if lib.hqo_dequant_mxfp4(_ptr(q), _ptr(s), M, K, group, 1 if unrotate else 0, _ptr(out),
+                             _threads(nthreads)):
+        raise ValueError("hqo_dequant_mxfp4: bad arguments")
+    return out

@@ -254,3 +254,16 @@ def test_host_quantizer_matches_oracle_on_a_workload():
     assert_bytes_equal("host scales", sh.numpy(), os_)
     assert np.float32(sg) == osg
     hqz.close()
+
+
+@pytest.mark.parametrize("group", [0, 16])
+def test_pass1_on_16_byte_aligned_input(group):
+    """x whose base is 16- but not 32-byte aligned takes pass 1's TMA path instead of the
+    streaming one; both must give the oracle's amax."""
+    M, K = 257, 1024
+    x_host = rand_input(M, K, torch.bfloat16, seed=77)
+    flat = torch.empty(M * K + 8, dtype=torch.bfloat16, device="cuda")
+    x_dev = flat[8:].view(M, K)
+    x_dev.copy_(x_host)
+    assert x_dev.data_ptr() % 32 == 16
+    check_against_oracle(x_host, group, x_dev=x_dev, label="16B-aligned")
