@@ -6,9 +6,11 @@ is its Python binding.  ``synth`` draws the seeded synthetic activations.
 from ._lib import HQError, lib_path, load  # noqa: F401
 from .api import (  # noqa: F401
     HostQuantizer,
+    hq_dequant_mxfp4,
     hq_dequant_nvfp4,
     hq_rot_amax,
     hq_rotate_quant_int8,
+    hq_rotate_quant_mxfp4,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
     quantize_nvfp4,
@@ -17,9 +19,11 @@ from .api import (  # noqa: F401
 __all__ = [
     "HQError",
     "HostQuantizer",
+    "hq_dequant_mxfp4",
     "hq_dequant_nvfp4",
     "hq_rot_amax",
     "hq_rotate_quant_int8",
+    "hq_rotate_quant_mxfp4",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
     "lib_path",

@@ -99,6 +99,34 @@ def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.
     return q, scales, s_global, amax_next
 
 
+def hq_rotate_quant_mxfp4(x: torch.Tensor, group: int, q: torch.Tensor | None = None,
+                          scales: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None):
+    """MXFP4: (q uint8 [M, K/2], scales uint8 [M, K/32] E8M0 bytes); one pass over x."""
+    dt, M, K, ldx = _x_args(x)
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 32), torch.uint8, x.device, "scales")
+    check(_lib.load().hq_rotate_quant_mxfp4(_ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
+                                            _stream_handle(stream)), "hq_rotate_quant_mxfp4")
+    return q, scales
+
+
+def hq_dequant_mxfp4(q: torch.Tensor, scales: torch.Tensor, group: int, unrotate: bool,
+                     out: torch.Tensor | None = None,
+                     stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """MXFP4 round trip: float32 [M, K] = codes * 2^(byte - 127), optionally un-rotated."""
+    if not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor (libhq has no CPU path)")
+    M, K2 = q.shape
+    K = 2 * K2
+    q = _need(q, (M, K2), torch.uint8, q.device, "q")
+    scales = _need(scales, (M, K // 32), torch.uint8, q.device, "scales")
+    out = _need(out, (M, K), torch.float32, q.device, "out")
+    check(_lib.load().hq_dequant_mxfp4(_ptr(q), _ptr(scales), M, K, group, 1 if unrotate else 0,
+                                       _ptr(out), _stream_handle(stream)), "hq_dequant_mxfp4")
+    return out
+
+
 def hq_rotate_quant_int8(x: torch.Tensor, group: int, q: torch.Tensor | None = None,
                          scales: torch.Tensor | None = None,
                          stream: torch.cuda.Stream | None = None):

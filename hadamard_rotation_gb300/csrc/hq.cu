@@ -357,9 +357,69 @@ hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float*
   p.dq_out = out;
   const int g = unrotate ? group : 0;
   switch (g) {
-    case 0: return launch(hq::k_dequant_nvfp4<0>, p, stream);
-    case 16: return launch(hq::k_dequant_nvfp4<16>, p, stream);
-    default: return launch(hq::k_dequant_nvfp4<256>, p, stream);
+    case 0: return launch(hq::k_dequant_nvfp4<0, false>, p, stream);
+    case 16: return launch(hq::k_dequant_nvfp4<16, false>, p, stream);
+    default: return launch(hq::k_dequant_nvfp4<256, false>, p, stream);
+  }
+}
+
+hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                                int group, uint8_t* q, uint8_t* scales, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (K % 32 != 0) return HQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!q || !scales) return HQ_ERR_NULL;
+  if (!aligned(q, 16)) return HQ_ERR_ALIGN;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.q = q;
+  p.s = scales;
+  const bool bf16 = dtype == HQ_BF16;
+  const bool strided = is_strided(M, K, ldx);
+  using hq::k_rotate_quant_mxfp4;
+  constexpr int kMode = HQ_PASS2_MODE;
+  auto go = [&](auto k_strided, auto k_flat, size_t smem) {
+    return strided ? launch(k_strided, p, stream) : launch(k_flat, p, stream, smem);
+  };
+  switch (group) {
+    case 0:
+      return bf16 ? go(k_rotate_quant_mxfp4<0, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<0, true, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                  : go(k_rotate_quant_mxfp4<0, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<0, false, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+    case 16:
+      return bf16 ? go(k_rotate_quant_mxfp4<16, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<16, true, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                  : go(k_rotate_quant_mxfp4<16, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<16, false, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+    default:
+      return bf16 ? go(k_rotate_quant_mxfp4<256, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<256, true, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                  : go(k_rotate_quant_mxfp4<256, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<256, false, kMode>,
+                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+  }
+}
+
+hq_status hq_dequant_mxfp4(const uint8_t* q, const uint8_t* scales, int64_t M, int64_t K,
+                           int group, int unrotate, float* out, hq_stream stream) {
+  if (unrotate && group != 16 && group != 256) return HQ_ERR_GROUP;
+  if (!unrotate && group != 0 && group != 16 && group != 256) return HQ_ERR_GROUP;
+  if (M < 0 || K < 0 || K % 32 != 0) return HQ_ERR_SHAPE;
+  if (unrotate && K % group != 0) return HQ_ERR_SHAPE;
+  if (K > 0 && M > INT64_MAX / K) return HQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!q || !scales || !out) return HQ_ERR_NULL;
+  if (!aligned(q, 8) || !aligned(out, 16)) return HQ_ERR_ALIGN;
+  hq::Params p = {};
+  p.nb = static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 16);
+  p.n_tiles = (p.nb + hq::kTileBlocks - 1) / hq::kTileBlocks;
+  p.dq_q = q;
+  p.dq_s = scales;
+  p.dq_out = out;
+  switch (unrotate ? group : 0) {
+    case 0: return launch(hq::k_dequant_nvfp4<0, true>, p, stream);
+    case 16: return launch(hq::k_dequant_nvfp4<16, true>, p, stream);
+    default: return launch(hq::k_dequant_nvfp4<256, true>, p, stream);
   }
 }
 

@@ -830,15 +830,82 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// Dequant: value = (+-grid[c]) * (s_block * s_global), then optionally the
-// rotation again (y = RN(z / sqrt(G)) after the same butterfly).
+// MXFP4: one E8M0 scale per 32 consecutive elements, no per-tensor scale.
+//   X = 2^(floor(log2 amax_32) - 2) (amax_32 / X in [4, 8)); E8M0 byte = that
+//   exponent + 127, clamped at 0; codes = E2M1(y / X).  For a finite amax the
+//   byte is max(biased fp32 exponent of amax - 2, 0), two integer operations.
+// A 32-block is two consecutive 16-blocks, held by lanes l and l ^ 1 in both
+// lane mappings; its amax is one xor-shuffle away.  Division by X is an exact
+// multiply by 2^(127 - byte), with 1/sqrt(G) folded in; a lane holding a block
+// whose byte is below 8 (amax below 2^-117, where folding could round subnormal
+// values differently) applies the two steps literally.
 // ---------------------------------------------------------------------------
-template <int G>
+template <int G, bool BF16, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
+  constexpr float c = inv_sqrt_g<G>();
+  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(
+      p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
+    rotate_tile<G>(t, lane);
+    uint32_t code[4];
+    float inv[4];
+    bool literal = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = 2 * k + h;
+        const float am = __fmul_rn(h ? block_absmax<true>(t.P[k]) : block_absmax<false>(t.P[k]), c);
+        const float a32 = max_nan(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        const int eb = static_cast<int>(__float_as_uint(a32) >> 23);
+        code[j] = static_cast<uint32_t>(eb > 2 ? eb - 2 : 0);
+        inv[j] = __uint_as_float((254u - code[j]) << 23);  // 2^(127 - code), normal for code <= 253
+        // a subnormal y (|y| < 2^-126) reaches a quotient of 2^(3 - biased exponent):
+        // it can only decide a code in blocks whose byte is below 3; 8 leaves a margin
+        literal |= code[j] < 8;
+      }
+    }
+    uint32_t w[4][2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float2 f;
+      if (!literal) f = make_float2(__fmul_rn(inv[2 * k], c), __fmul_rn(inv[2 * k + 1], c));
+      float2 qv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (!literal) {
+          qv[i] = mul2(t.P[k][i], f);
+        } else {
+          const float2 y = mul2(t.P[k][i], make_float2(c, c));
+          qv[i] = mul2(y, make_float2(inv[2 * k], inv[2 * k + 1]));
+        }
+      }
+      w[2 * k][0] = e2m1x8(qv[0].x, qv[1].x, qv[2].x, qv[3].x, qv[4].x, qv[5].x, qv[6].x, qv[7].x);
+      w[2 * k][1] = e2m1x8(qv[8].x, qv[9].x, qv[10].x, qv[11].x, qv[12].x, qv[13].x, qv[14].x, qv[15].x);
+      w[2 * k + 1][0] = e2m1x8(qv[0].y, qv[1].y, qv[2].y, qv[3].y, qv[4].y, qv[5].y, qv[6].y, qv[7].y);
+      w[2 * k + 1][1] = e2m1x8(qv[8].y, qv[9].y, qv[10].y, qv[11].y, qv[12].y, qv[13].y, qv[14].y, qv[15].y);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (!valid[j]) continue;
+      const uint64_t b = base + lane_block<G>(lane, j);
+      __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0], w[j][1]));
+      if ((lane & 1) == 0)  // the even half writes the 32-block's scale byte
+        __stcs(reinterpret_cast<unsigned char*>(p.s + (b >> 1)), static_cast<unsigned char>(code[j]));
+    }
+  });
+}
+
+// ---------------------------------------------------------------------------
+// Dequant: value = (+-grid[c]) * (s_block * s_global), then optionally the
+// rotation again (y = RN(z / sqrt(G)) after the same butterfly).  MX: value =
+// (+-grid[c]) * 2^(byte - 127) for the 32-block's E8M0 byte.
+// ---------------------------------------------------------------------------
+template <int G, bool MX>
 __global__ void __launch_bounds__(kThreads, 2) k_dequant_nvfp4(Params p) {
   const int lane = threadIdx.x & 31;
   const uint64_t warp = (static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta) + (threadIdx.x >> 5);
   const uint64_t n_warps = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
-  const float s_global = *p.dq_sglobal;
+  const float s_global = MX ? 1.0f : *p.dq_sglobal;
   for (uint64_t tile = warp; tile < p.n_tiles; tile += n_warps) {
     const uint64_t base = tile * kTileBlocks;
     bool valid[4];
@@ -851,8 +918,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_dequant_nvfp4(Params p) {
       float s_f = 0.0f;
       if (valid[j]) {
         qw = __ldg(reinterpret_cast<const uint2*>(p.dq_q + b * 8u));
-        const float sb = e4m3x2_to_f32(__ldg(p.dq_s + b)).x;
-        s_f = __fmul_rn(sb, s_global);
+        if constexpr (MX) {
+          const uint32_t e = __ldg(p.dq_s + (b >> 1));
+          s_f = e >= 1u ? __uint_as_float(e << 23) : 0x1p-127f;  // 2^(e - 127)
+        } else {
+          const float sb = e4m3x2_to_f32(__ldg(p.dq_s + b)).x;
+          s_f = __fmul_rn(sb, s_global);
+        }
       }
       const float2 s2 = make_float2(s_f, s_f);
 #pragma unroll

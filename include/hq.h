@@ -133,6 +133,30 @@ HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, in
                                                hq_stream stream);
 
 /*
+ * hq_rotate_quant_mxfp4 -- MXFP4 variant: E2M1 codes with one power-of-two (E8M0) scale per 32
+ *   consecutive elements of a row and no per-tensor scale, so a single pass over x.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §1: MXFP4 has 32-element blocks and
+ *    power-of-two E8M0 scales; "Try this": the error study with MXFP4 semantics.)
+ *   The pages give no rule for the scale; this library uses the usual MX rule:
+ *   X = 2^(floor(log2 amax_32) - 2), so amax_32 / X lies in [4, 8) (2 is the exponent of E2M1's
+ *   largest value, 6); the stored byte is the exponent + 127, clamped to [0, 254] (0 for an
+ *   all-zero block); codes = E2M1(y / X) as for NVFP4 (ties to even, saturating at 6, sign bit
+ *   copied).  The rotation is as for NVFP4 (group 0, 16 or 256).
+ *
+ *   x, dtype, M, K, ldx, group : as for hq_rotate_quant_nvfp4, with K a multiple of 32 as well.
+ *   q      : uint8 [M, K/2], 16-byte aligned (same packing as NVFP4).
+ *   scales : uint8 [M, K/32] E8M0 bytes.
+ */
+HQ_API hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                       int64_t ldx, int group, uint8_t* q, uint8_t* scales,
+                                       hq_stream stream);
+
+/* hq_dequant_mxfp4 -- value = (+-grid[code & 7]) * 2^(byte - 127), then the rotation again when
+ * `unrotate` (group 16 or 256).  out: fp32 [M, K], 16-byte aligned; q 8-byte aligned. */
+HQ_API hq_status hq_dequant_mxfp4(const uint8_t* q, const uint8_t* scales, int64_t M, int64_t K,
+                                  int group, int unrotate, float* out, hq_stream stream);
+
+/*
  * hq_rotate_quant_int8 -- INT8 per-token rotate-quant with the regular Hadamard.
  *   ("hyperflow_h3_flash_int8.py", HyperFlow: regular_hadamard, rotate_quant_kernel; the
  *    activation side of a W8A8 linear whose weight was rotated offline.)

@@ -192,3 +192,16 @@ def test_int8_argument_checks(lib):
     assert i8(x=FAKE + 8) == 3 and i8(q=FAKE + 4) == 3 and i8(s=FAKE + 2) == 3
     assert i8(ldx=68) == 3                     # 136-byte bf16 row stride
     assert i8(M=0) == 0
+
+
+def test_mxfp4_argument_checks(lib):
+    def mx(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, q=FAKE, s=FAKE):
+        return lib.hq_rotate_quant_mxfp4(P(x) if x else None, dt, M, K, ldx, G, P(q) if q else None,
+                                         P(s) if s else None, None)
+    assert mx(x=0) == 1 and mx(q=0) == 1 and mx(s=0) == 1
+    assert mx(K=48, ldx=48) == 2             # not a multiple of 32
+    assert mx(G=64) == 5 and mx(dt=5) == 4
+    assert mx(q=FAKE + 8) == 3 and mx(x=FAKE + 4) == 3
+    assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 48, 0, 0, P(FAKE), None) == 2
+    assert lib.hq_dequant_mxfp4(None, P(FAKE), 4, 64, 0, 0, P(FAKE), None) == 1
+    assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 64, 0, 1, P(FAKE), None) == 5
