@@ -77,6 +77,24 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(value_ms: float) -> float:
+    """The largest of every rank's value (a host-side gloo all-reduce); the value itself when
+    no process group is initialised."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value_ms)
+    t = torch.tensor([float(value_ms)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_gbs(bytes_per_step_per_rank: int, steps: int, world: int, region_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed divided by the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * world / (region_ms / 1e3) / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -289,12 +307,9 @@ def run_ours(args, w):
     if flush is not None:
         # steps are timed launch to launch; the L2 flush between them is not part of a step
         region_ms = sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(K))
+    region_ms = max_over_ranks(region_ms)
     step_ms = region_ms / K
-    if pg:
-        t = torch.tensor([region_ms], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        region_ms = float(t.item())
-    value = step_bytes * K * world / (region_ms / 1e3) / 1e9
+    value = throughput_gbs(step_bytes, K, world, region_ms)
 
     # ---- single-pass mode (delayed amax): one kernel per step, reported beside the step ----
     amax_b = torch.empty(1, dtype=torch.float32, device=dev)
@@ -314,6 +329,29 @@ def run_ours(args, w):
     d1.record(stream)
     torch.cuda.synchronize(dev)
     single_ms = d0.elapsed_time(d1) / K
+
+    # ---- MXFP4 (E8M0 per 32, single pass) on the same tensor and group ----
+    mx = None
+    if w.K % 32 == 0:
+        s_mx = torch.empty((w.M, w.K // 32), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream)
+        torch.cuda.synchronize(dev)
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(K):
+            hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream)
+            if flush is not None:
+                flush.fill_(1.0)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        mx_ms = m0.elapsed_time(m1) / K
+        mx_bytes = bytes_in + w.numel // 2 + w.numel // 32
+        mx = {"group": group, "ms_per_launch": mx_ms, "bytes_per_launch": mx_bytes,
+              "gbs": mx_bytes / (mx_ms / 1e3) / 1e9,
+              "note": "hq_rotate_quant_mxfp4 (one pass: no global scale)"}
+        del s_mx
 
     # ---- INT8 per-token rotate-quant (regular Hadamard, G = 256) on the same tensor ----
     int8 = None
@@ -355,18 +393,16 @@ def run_ours(args, w):
     for _ in range(e2e_steps):
         hqz.submit(x_host)
     hqz.wait()
-    e2e_ms = (time.perf_counter() - t0) * 1e3
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3)
     hqz.close()
-    if pg:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_bytes * e2e_steps * world / (e2e_ms / 1e3) / 1e9
+    e2e_value = throughput_gbs(step_bytes, e2e_steps, world, e2e_ms)
 
     # ---- roofline of the dominant kernel (pass 2) ----
     peak, peak_kind = load_peaks()
     if int8 is not None:
         int8["frac_of_peak"] = int8["gbs"] / peak
+    if mx is not None:
+        mx["frac_of_peak"] = mx["gbs"] / peak
     p2 = sum(pass2) / K
     p1 = sum(pass1) / K
     achieved = step_bytes / (p2 / 1e3) / 1e9
@@ -396,6 +432,7 @@ def run_ours(args, w):
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
             "note": "hq_rotate_quant_nvfp4_delayed: quantize with the previous step's amax while "
                     "reducing this one (one read of x); not the metric's two-pass step"},
+        "mxfp4": mx,
         "int8_per_token": int8,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": hqz.h2d_bytes,
                 "d2h_bytes_per_step": hqz.d2h_bytes, "steps": e2e_steps,
