@@ -12,7 +12,6 @@
 #include <mutex>
 
 #include "hq.h"
-#include "hq_int8.cuh"
 #include "hq_internal.h"
 #include "hq_kernels.cuh"
 
@@ -200,64 +199,9 @@ hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream
                           ring_bytes<HQ_PASS2_STAGES>(kMode, false));
 }
 
-// INT8 per-token rotate-quant: one CTA of kI8Threads per SM, looping over row groups.
-template <int G, bool BF16, int MODE>
-hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
-  auto kernel = hq::k_rotate_quant_int8<G, BF16, MODE>;
-  const size_t smem = (MODE == hq::kLoadTma) ? static_cast<size_t>(hq::kI8RingBytes) : 0;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return cuda_fail(e);
-  if (smem > 48 * 1024 &&
-      (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem))) != cudaSuccess)
-    return cuda_fail(e);
-  const int64_t row_groups = (p.M + p.rows_per_iter - 1) / p.rows_per_iter;
-  const unsigned grid = static_cast<unsigned>(row_groups < sms ? row_groups : sms);
-  kernel<<<grid, hq::kI8Threads, smem, static_cast<cudaStream_t>(stream)>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
-  return HQ_OK;
-}
-
-template <int G>
-hq_status dispatch_int8(const hq::I8Params& p, bool bf16, hq_stream s) {
-  return bf16 ? launch_int8<G, true, hq::kLoadTma>(p, s)
-              : launch_int8<G, false, hq::kLoadDirect>(p, s);
-}
-
 }  // namespace
 
 extern "C" {
-
-hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
-                               int group, int8_t* q, float* scales, hq_stream stream) {
-  if (dtype != HQ_F32 && dtype != HQ_BF16) return HQ_ERR_DTYPE;
-  if (group != 16 && group != 64 && group != 256) return HQ_ERR_GROUP;
-  if (M < 0 || K < 0 || ldx < K || K % group != 0 || K > hq::kI8MaxK) return HQ_ERR_SHAPE;
-  if (M == 0 || K == 0) return HQ_OK;
-  if (!x || !q || !scales) return HQ_ERR_NULL;
-  const int64_t es = dtype == HQ_BF16 ? 2 : 4;
-  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scales, 4)) return HQ_ERR_ALIGN;
-  if (M > 1 && (ldx * es) % 16 != 0) return HQ_ERR_ALIGN;
-  hq::I8Params p = {};
-  p.x = static_cast<const uint8_t*>(x);
-  p.ldx_bytes = (M > 1 ? ldx : K) * es;
-  p.M = M;
-  p.K = K;
-  p.tiles_per_row = static_cast<int>((K + hq::kI8TileElems - 1) / hq::kI8TileElems);
-  p.rows_per_iter = hq::kI8Warps / p.tiles_per_row;
-  p.q = q;
-  p.scales = scales;
-  const bool bf16 = dtype == HQ_BF16;
-  switch (group) {
-    case 16: return dispatch_int8<16>(p, bf16, stream);
-    case 64: return dispatch_int8<64>(p, bf16, stream);
-    default: return dispatch_int8<256>(p, bf16, stream);
-  }
-}
 
 hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
                       int group, float* amax, float* y, hq_stream stream) {

@@ -14,19 +14,21 @@
 // Work decomposition.  A CTA of 16 warps handles whole rows: a row of K channels
 // is T = ceil(K / 2048) warp tiles (K <= 32768), the CTA takes R = 16 / T rows at
 // a time, and warp w handles tile (w mod T) of row (w / T).  Within a tile the
-// lane holds 4 blocks of 16 channels as in the NVFP4 kernels (G = 16: blocks
-// 32j + lane; G = 64, 256: blocks 16*(lane/4) + lane%4 + 4j, so the 4 lanes of a
-// quad hold 16 consecutive blocks).  Every value stays in registers from load to
-// store: the row's amax is reduced through shared memory between the two
-// halves, so x is read once.  bf16 rows stream through the per-warp TMA ring.
+// lane holds 4 blocks of 16 channels (G = 16: blocks 32j + lane; G = 64, 256: the
+// 4 lanes of a quad hold 16 consecutive blocks, lane % 4 being the block's digit
+// 2, in the lane-dependent slot order of i8_d3).  Every value stays in registers
+// from load to store: the row's amax is reduced through shared memory between
+// the two halves, so x is read once.  bf16 rows stream through the per-warp TMA
+// ring.
 //
 // The 4-point steps run on negated values: new_k = fma(S, -1/2, a_(3-k)) =
 // RN(a_(3-k) - S/2) = -out_k, one FFMA2 per two values and no negation; the sign
 // alternates from step to step (the sum S of negated inputs is exactly -S), so
 // after an odd number of steps (G = 64) the quantizer multiplies by -1/scale.
-// The step on digit 2 (G = 64, 256) runs across the quad: S comes from two
-// xor-shuffles, and each lane keeps its own input a_c and produces the output of
-// digit value 3 - c, which relabels the lane's block for the stores.
+// The step on digit 2 (G = 64, 256) runs across the quad as a reduce-scatter and
+// all-gather of S (1.5 shuffles per value); each lane keeps its own input a_c and
+// produces the output of digit value 3 - c, which relabels the lane's block for
+// the stores.  Digit 3 (G = 256) is in-lane, packed two positions per FADD2.
 #pragma once
 
 #include "hq_kernels.cuh"
@@ -65,10 +67,42 @@ __device__ __forceinline__ void h4_step(float2& a0, float2& a1, float2& a2, floa
   a3 = n3;
 }
 
+// Which digit-3 value (block index bits 2..3 within a 256-group, or which
+// 64-group of the quad for G = 64) register slot j of a lane holds, for G >= 64.
+// Slot j is P[j >> 1], component j & 1.  The map depends on the lane's position in
+// its quad so that the cross-lane step below runs the same instructions on all
+// four lanes: lane bit 0 swaps the two float2 arrays, lane bit 1 swaps .x and .y.
+// In every lane add2(P[0][i], P[1][i]) pairs digit-3 values {0, 1} and {2, 3}.
+__device__ __forceinline__ uint32_t i8_d3(int lane, int j) {
+  const int k = j >> 1, c = j & 1;
+  return static_cast<uint32_t>(((c ^ ((lane >> 1) & 1)) << 1) | (k ^ (lane & 1)));
+}
+
+// Block (of 16 channels, within the warp tile) that slot j of the lane loads.
+template <int G>
+__device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
+  if constexpr (G == 16)
+    return static_cast<uint32_t>(32 * j + lane);
+  else
+    return static_cast<uint32_t>((lane >> 2) * 16 + (lane & 3) + 4 * i8_d3(lane, j));
+}
+
+// Block that slot j holds after the rotation: each 4-point step leaves, in the
+// register that held input digit value d, the output of digit value 3 - d.
+template <int G>
+__device__ __forceinline__ uint32_t i8_out_block(int lane, int j) {
+  if constexpr (G == 16)
+    return static_cast<uint32_t>(32 * j + lane);
+  else if constexpr (G == 64)
+    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * i8_d3(lane, j));
+  else
+    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * (3 - i8_d3(lane, j)));
+}
+
 // The regular-Hadamard rotation of the lane's 4 blocks, digit by digit.
 // Returns +1 if the registers hold y, -1 if they hold -y.
 template <int G>
-__device__ __forceinline__ float rotate_regular(Lane4& t, int lane) {
+__device__ __forceinline__ float rotate_regular(Lane4& t) {
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     // digit 0: channels 4b .. 4b+3 of a block
@@ -81,65 +115,56 @@ __device__ __forceinline__ float rotate_regular(Lane4& t, int lane) {
   if constexpr (G == 16) {
     return 1.0f;
   } else {
-    // digit 2: the 4 blocks of the quad (lane % 4 is the digit), values now
-    // carry their true sign again (two negated steps).
+    // digit 2: the four lanes of a quad hold its four values (lane % 4).  The sum
+    // S = (v0 + v1) + (v2 + v3) of every position is reduced and scattered in two
+    // exchanges (lanes 0,1 form v0 + v1 and lanes 2,3 form v2 + v3 on half of the
+    // positions each, then every lane adds the other pair's sum on a quarter), and
+    // gathered back in two more.  Each lane then keeps its own input v_c and
+    // produces the negated output of digit value 3 - c.
     const float2 nh = make_float2(-0.5f, -0.5f);
+    float s[16];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int i = 0; i < 16; ++i) {
+      float2 r;
+      r.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 1);
+      r.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 1);
+      const float2 u = add2(t.P[0][i], r);  // the pair sum on this lane's P[0] positions
+      s[i] = __fadd_rn(u.x, __shfl_xor_sync(0xFFFFFFFFu, u.y, 2));
+    }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 a = t.P[k][i];
-        float2 p;
-        p.x = __shfl_xor_sync(0xFFFFFFFFu, a.x, 1);
-        p.y = __shfl_xor_sync(0xFFFFFFFFu, a.y, 1);
-        const float2 u = add2(a, p);  // v0 + v1 on lanes 0,1; v2 + v3 on lanes 2,3
-        float2 w;
-        w.x = __shfl_xor_sync(0xFFFFFFFFu, u.x, 2);
-        w.y = __shfl_xor_sync(0xFFFFFFFFu, u.y, 2);
-        const float2 s = add2(u, w);  // (v0 + v1) + (v2 + v3) on every lane
-        t.P[k][i] = fma2(s, nh, a);   // -out of digit value 3 - (lane % 4)
-      }
+    for (int i = 0; i < 16; ++i) {
+      const float2 s0 = make_float2(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 2));  // S on P[0]
+      float2 s1;                                                                   // S on P[1]
+      s1.x = __shfl_xor_sync(0xFFFFFFFFu, s0.x, 1);
+      s1.y = __shfl_xor_sync(0xFFFFFFFFu, s0.y, 1);
+      t.P[0][i] = fma2(s0, nh, t.P[0][i]);
+      t.P[1][i] = fma2(s1, nh, t.P[1][i]);
     }
     if constexpr (G == 64) {
       return -1.0f;
     } else {
-      // digit 3: the lane's register blocks j = 0..3 (P[0].x, P[0].y, P[1].x, P[1].y)
+      // digit 3: the lane's four slots; add2 pairs digit values {0,1} and {2,3}.
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float a0 = t.P[0][i].x, a1 = t.P[0][i].y, a2 = t.P[1][i].x, a3 = t.P[1][i].y;
-        const float s = __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
-        t.P[0][i].x = __fmaf_rn(s, -0.5f, a3);
-        t.P[0][i].y = __fmaf_rn(s, -0.5f, a2);
-        t.P[1][i].x = __fmaf_rn(s, -0.5f, a1);
-        t.P[1][i].y = __fmaf_rn(s, -0.5f, a0);
+        const float2 u = add2(t.P[0][i], t.P[1][i]);
+        const float sum = __fadd_rn(u.x, u.y);
+        const float2 s2 = make_float2(sum, sum);
+        t.P[0][i] = fma2(s2, nh, t.P[0][i]);
+        t.P[1][i] = fma2(s2, nh, t.P[1][i]);
       }
       return 1.0f;
     }
   }
 }
 
-// Block index (within the tile) that the lane's register block j holds after the
-// rotation (the digit-2 step relabels the quad's blocks c -> 3 - c).
-template <int G>
-__device__ __forceinline__ uint32_t i8_out_block(int lane, int j) {
-  if constexpr (G == 16)
-    return static_cast<uint32_t>(32 * j + lane);
-  else
-    return static_cast<uint32_t>((lane >> 2) * 16 + 4 * j + (3 - (lane & 3)));
+// Four packed int8 bytes (channel order) from the magic-add results of four channels.
+__device__ __forceinline__ uint32_t pack_i8x4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
-template <int G>
-__device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
-  return lane_block<G == 16 ? 16 : 256>(lane, j);
-}
-
-// Low byte of rint(v) for |v| < 2^22: adding 1.5 * 2^23 rounds to an integer
-// (half to even) and leaves it in the low mantissa bits, two's complement.
-__device__ __forceinline__ uint32_t int8_bits(float v) {
-  return __float_as_uint(__fadd_rn(v, 12582912.0f));
-}
-
-template <int G, bool BF16, int MODE>
+// FULL: every warp tile of a row is complete (K a multiple of the tile), so no
+// block needs a bounds check.
+template <int G, bool BF16, int MODE, bool FULL>
 __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p) {
   constexpr int es = BF16 ? 2 : 4;
   constexpr int kTileBytes = kI8TileElems * es;
@@ -151,9 +176,14 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   const int chunk = wid % T;
   const bool has_role = row_local < R;
   const int64_t chunk0 = static_cast<int64_t>(chunk) * kI8TileElems;
-  const int64_t nvalid = has_role ? (p.K - chunk0 < kI8TileElems ? p.K - chunk0 : kI8TileElems) : 0;
+  const int64_t nvalid =
+      FULL ? kI8TileElems : (has_role ? (p.K - chunk0 < kI8TileElems ? p.K - chunk0 : kI8TileElems) : 0);
+  auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < nvalid; };
 
-  __shared__ float tile_max[kI8Warps];
+  // Per-warp tile maxima, double buffered so that one barrier per iteration
+  // suffices: a warp can only overwrite a buffer after every warp has passed the
+  // barrier that follows its last read of it.
+  __shared__ float tile_max[2][kI8Warps];
   extern __shared__ __align__(1024) uint8_t hq_smem[];
   uint8_t* ring = hq_smem + wid * kI8Stages * kI8TileElems * 2;
   const uint32_t ring_s = smem_addr(ring);
@@ -189,9 +219,9 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   const int64_t first_rows = static_cast<int64_t>(blockIdx.x) * R;
   for (int64_t it = 0; first_rows + it * gridDim.x * R < p.M; ++it) {
     const int64_t r = row_of(it);
+    const int buf = static_cast<int>(it & 1);
     const bool active = mine(it);
     Lane4 t;
-    bool valid[4];
     float sign = 1.0f;
     float amax = 0.0f;
     if (active) {
@@ -209,9 +239,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t bl = i8_in_block<G>(lane, j);
-            valid[j] = static_cast<int64_t>(bl) * 16 < nvalid;
             uint4 w4[2];
-            if (valid[j]) {
+            if (block_ok(bl)) {
               const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kTileBytes + bl * 32u);
               w4[0] = src[0];
               w4[1] = src[1];
@@ -236,19 +265,19 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t bl = i8_in_block<G>(lane, j);
-          valid[j] = static_cast<int64_t>(bl) * 16 < nvalid;
+          const bool ok = block_ok(bl);
           uint4 w4[BF16 ? 2 : 4];
 #pragma unroll
           for (int k = 0; k < (BF16 ? 2 : 4); ++k)
-            w4[k] = valid[j] ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + k)
-                             : make_uint4(0u, 0u, 0u, 0u);
+            w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + k)
+                       : make_uint4(0u, 0u, 0u, 0u);
           float f[16];
           widen<BF16>(w4, f);
           put_block(t, j, f);
         }
       }
       if (!broken) {
-        sign = rotate_regular<G>(t, lane);
+        sign = rotate_regular<G>(t);
 #pragma unroll
         for (int k = 0; k < 2; ++k)
           amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
@@ -257,38 +286,48 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
     // amax of the row: warp max, then the row's T warps through shared memory.
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-    if (lane == 0) tile_max[wid] = amax;
+    if (lane == 0) tile_max[buf][wid] = amax;
     __syncthreads();
     if (active && !broken) {
-      float row_amax = tile_max[row_local * T];
-      for (int c = 1; c < T; ++c) row_amax = max_nan(row_amax, tile_max[row_local * T + c]);
+      // T <= 16: each half-warp reads the row's T tile maxima and reduces them.
+      const int c = lane & 15;
+      float row_amax = c < T ? tile_max[buf][row_local * T + c] : 0.0f;
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) row_amax = max_nan(row_amax, __shfl_xor_sync(0xFFFFFFFFu, row_amax, m));
       const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
       const float inv = __fdiv_rn(1.0f, scale) * sign;  // -inv when the registers hold -y
       if (chunk == 0 && lane == 0) p.scales[r] = scale;
       const float2 inv2 = make_float2(inv, inv);
+      // rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
+      // rounds (half to even) to an integer held, two's complement, in the low bits.
+      // The sum is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA
+      // 13.0, -O3) fuses a packed multiply whose only use is a packed add into one
+      // fused multiply-add even when both carry an explicit .rn, and rint of the
+      // unrounded product differs where RN(y * inv) is exactly k + 1/2.
+      const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+      const float2 one2 = make_float2(1.0f, 1.0f);
       int8_t* qrow = p.q + r * p.K + chunk0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t bo = i8_out_block<G>(lane, j);
-        if (static_cast<int64_t>(bo) * 16 >= nvalid) continue;
-        uint32_t w[4];
+      for (int k = 0; k < 2; ++k) {
+        uint32_t bx[16], by[16];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          uint32_t b[4];
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            const float2 pr = t.P[j >> 1][4 * k4 + u];
-            const float2 pr1 = t.P[j >> 1][4 * k4 + u + 1];
-            const float2 v = mul2(make_float2((j & 1) ? pr.y : pr.x, (j & 1) ? pr1.y : pr1.x), inv2);
-            b[u] = int8_bits(v.x);
-            b[u + 1] = int8_bits(v.y);
-          }
-          w[k4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+          bx[i] = __float_as_uint(v.x);
+          by[i] = __float_as_uint(v.y);
         }
-        __stcs(reinterpret_cast<uint4*>(qrow + bo * 16u), make_uint4(w[0], w[1], w[2], w[3]));
+        const uint32_t box = i8_out_block<G>(lane, 2 * k);
+        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
+        if (block_ok(box))
+          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
+                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
+                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
+        if (block_ok(boy))
+          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
+                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
+                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
       }
     }
-    __syncthreads();  // tile_max is reused by the next iteration
   }
 }
 

@@ -85,3 +85,38 @@ def test_int8_empty_and_limits():
     assert q.numel() == 0
     with pytest.raises(hq.HQError):
         hq.hq_rotate_quant_int8(torch.zeros(2, 32768 + 256, device="cuda", dtype=torch.bfloat16), 256)
+
+
+def _tie_row(group):
+    """One fp32 row of 2 * group channels whose rotated value y satisfies
+    RN(y * inv) = k + 1/2 exactly while the exact product y * inv is not k + 1/2:
+    rint of the rounded product (the definition) and of an unrounded one (a fused
+    multiply-add) differ.  A one-hot value v in a group rotates to +-v / sqrt(G) on
+    every channel, exactly, so group 0 fixes the row amax and group 1 carries y."""
+    r = np.float32(np.sqrt(group))
+    for amax in np.linspace(10.0, 60.0, 2001, dtype=np.float32):
+        scale = np.float32(amax / np.float32(127.0))
+        inv = np.float32(np.float32(1.0) / scale)
+        for k in range(20, 40):
+            y = np.float32((k + 0.5) / float(inv))
+            for _ in range(32):
+                y = np.nextafter(y, np.float32(-np.inf))
+            for _ in range(64):
+                prod = np.float32(y * inv)
+                exact = float(y) * float(inv)  # 24 x 24 bits: exact in float64
+                if float(prod) == k + 0.5 and np.rint(exact) != np.rint(prod):
+                    row = np.zeros(2 * group, np.float32)
+                    row[0] = amax * r
+                    row[group] = y * r
+                    assert row[0] / r == amax and row[group] / r == y
+                    return row
+                y = np.nextafter(y, np.float32(np.inf))
+    raise AssertionError("no tie case found")
+
+
+@pytest.mark.parametrize("group", [16, 64, 256])
+def test_int8_rint_of_rounded_product(group):
+    """q = rint(RN(y * (1/scale))): the product is rounded before rint."""
+    row = _tie_row(group)
+    x = torch.from_numpy(np.tile(row, (4, 1)))
+    check(x, group)
