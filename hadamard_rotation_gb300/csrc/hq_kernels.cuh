@@ -348,8 +348,16 @@ __device__ __forceinline__ void put_block(Lane4& t, int j, const float (&f)[16])
   }
 }
 
+// Register slot of the lane's block j (slot s is P[s >> 1], component s & 1).
+// ORDER 0: slot j.  ORDER 1: the two bits of j swapped, so that blocks j and
+// j ^ 1 sit in P[0] and P[1] (a packed pair) and blocks j and j ^ 2 in .x / .y.
+template <int ORDER>
+__device__ __forceinline__ constexpr int slot_of(int j) {
+  return ORDER == 0 ? j : (((j & 1) << 1) | (j >> 1));
+}
+
 // Direct global loads (strided rows).
-template <int G, bool BF16, bool STRIDED>
+template <int G, bool BF16, bool STRIDED, int ORDER = 0>
 __device__ __forceinline__ void load_tile_global(const Params& p, uint64_t tile_base, int lane,
                                                  bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
@@ -369,12 +377,12 @@ __device__ __forceinline__ void load_tile_global(const Params& p, uint64_t tile_
     }
     float f[16];
     widen<BF16>(w4, f);
-    put_block(t, j, f);
+    put_block(t, slot_of<ORDER>(j), f);
   }
 }
 
 // Loads from a tile staged in shared memory (block b of the tile at b*16*es).
-template <int G, bool BF16>
+template <int G, bool BF16, int ORDER = 0>
 __device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t tile_base, uint64_t nb,
                                                int lane, bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
@@ -394,15 +402,18 @@ __device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t til
     }
     float f[16];
     widen<BF16>(w4, f);
-    put_block(t, j, f);
+    put_block(t, slot_of<ORDER>(j), f);
   }
 }
 
-// Ring depth (tiles in flight per warp).  Pass 1 does little arithmetic per
-// byte and runs best with a deep ring and one CTA per SM; pass 2 needs its
-// registers for arithmetic and runs best with two CTAs per SM and a 2-deep ring.
+// Ring depth (tiles in flight per warp) and CTAs per SM.  Both passes run two
+// CTAs of 8 warps per SM (16 warps); pass 1 keeps 3 tiles per warp in flight,
+// pass 2, which needs more registers, 2.
 #ifndef HQ_PASS1_STAGES
-#define HQ_PASS1_STAGES 4
+#define HQ_PASS1_STAGES 3
+#endif
+#ifndef HQ_PASS1_MIN_CTAS
+#define HQ_PASS1_MIN_CTAS 2
 #endif
 #ifndef HQ_PASS2_STAGES
 #define HQ_PASS2_STAGES 2
@@ -427,7 +438,7 @@ enum LoadMode : int {
 
 // Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
 // values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
-template <int G, bool BF16, int MODE, int STAGES, typename Body>
+template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, typename Body>
 __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -438,7 +449,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
       const uint64_t base = seq * kTileBlocks;
       bool valid[4];
       Lane4 t;
-      load_tile_global<G, BF16, MODE == kLoadStrided>(p, base, lane, valid, t);
+      load_tile_global<G, BF16, MODE == kLoadStrided, ORDER>(p, base, lane, valid, t);
       body(base, lane, valid, t);
     }
   } else {
@@ -484,7 +495,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
       const uint64_t base = seq * kTileBlocks;
       bool valid[4];
       Lane4 t;
-      load_tile_smem<G, BF16>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+      load_tile_smem<G, BF16, ORDER>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
       __syncwarp();  // every lane has read the slot
       const uint64_t next = seq + R::kStages * nw;
       if (next < p.n_tiles) {
@@ -518,6 +529,28 @@ __device__ __forceinline__ void butterfly16(float2 (&v)[16]) {
   }
 }
 
+// H256 stages h = 16, 32: the partner block sits in lane ^ 1, lane ^ 2 of the
+// quad.  The lane holding the lower index computes a + b = own * 1 + partner,
+// the other a - b = own * (-1) + partner; both are one rounding (fma with an
+// exact product).  Every register slot is treated alike.
+__device__ __forceinline__ void cross_lane_stages(Lane4& t, int lane) {
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    const float sg = (lane & m) ? -1.0f : 1.0f;
+    const float2 s2 = make_float2(sg, sg);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float2 o;
+        o.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i].x, m);
+        o.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i].y, m);
+        t.P[k][i] = fma2(t.P[k][i], s2, o);
+      }
+    }
+  }
+}
+
 template <int G>
 __device__ __forceinline__ void rotate_tile(Lane4& t, int lane) {
   if constexpr (G == 0) {
@@ -526,25 +559,7 @@ __device__ __forceinline__ void rotate_tile(Lane4& t, int lane) {
     butterfly16(t.P[0]);
     butterfly16(t.P[1]);
     if constexpr (G == 256) {
-      // h = 16, 32: partner block sits in lane ^ 1, lane ^ 2 of the quad.  The
-      // lane holding the lower index computes a + b = own * 1 + partner, the
-      // other a - b = own * (-1) + partner; both are one rounding (fma with an
-      // exact product).
-#pragma unroll
-      for (int m = 1; m <= 2; m <<= 1) {
-        const float sg = (lane & m) ? -1.0f : 1.0f;
-        const float2 s2 = make_float2(sg, sg);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float2 o;
-            o.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i].x, m);
-            o.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i].y, m);
-            t.P[k][i] = fma2(t.P[k][i], s2, o);
-          }
-        }
-      }
+      cross_lane_stages(t, lane);
       // h = 64: register block j <-> j ^ 1, i.e. the two halves of each pair.
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -581,10 +596,47 @@ __device__ __forceinline__ constexpr float sqrt_g() {
 // ---------------------------------------------------------------------------
 // Pass 1: rotate + amax.
 // ---------------------------------------------------------------------------
+// max |z| over the lane's 4 blocks of a 256-group tile loaded in slot order 1,
+// without forming the outputs of the last stage.  Stages h = 1..32 as in
+// rotate_tile; h = 64 pairs blocks j, j ^ 1, here P[0] against P[1] (packed);
+// h = 128 pairs blocks j, j ^ 2, here the .x and .y halves, and only feeds the
+// max: for any a, b, max(|RN(a + b)|, |RN(a - b)|) = RN(|a| + |b|) (one of a + b,
+// a - b has magnitude |a| + |b|, the other at most that, and RN is monotone and
+// odd), which holds with a NaN too.  (An a, b = +-inf of opposite signs gives inf
+// where the stage gives a NaN, so non-finite input still surfaces.)
+__device__ __forceinline__ float absmax256_order1(Lane4& t, int lane) {
+  butterfly16(t.P[0]);
+  butterfly16(t.P[1]);
+  cross_lane_stages(t, lane);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 a = t.P[0][i];
+    const float2 b = t.P[1][i];
+    t.P[0][i] = add2(a, b);
+    t.P[1][i] = sub2(a, b);
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int i = 0; i < 16; i += 2)
+      m = max3_nan(m, __fadd_rn(fabsf(t.P[k][i].x), fabsf(t.P[k][i].y)),
+                   __fadd_rn(fabsf(t.P[k][i + 1].x), fabsf(t.P[k][i + 1].y)));
+  return m;
+}
+
 template <int G, bool BF16, int MODE, bool WRITE_Y>
-__global__ void __launch_bounds__(kThreads, 1) k_rot_amax(Params p) {
+__global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params p) {
+  // Without a rotated output, the 256-group takes slot order 1 and skips the
+  // last stage's outputs (absmax256_order1).
+  constexpr bool kAbsTrick = G == 256 && !WRITE_Y;
   float zmax = 0.0f;
-  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES>(p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
+  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0>(
+      p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
+    if constexpr (kAbsTrick) {
+      zmax = max_nan(zmax, absmax256_order1(t, lane));
+      return;
+    }
     rotate_tile<G>(t, lane);
 #pragma unroll
     for (int k = 0; k < 2; ++k)
