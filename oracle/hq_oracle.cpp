@@ -248,8 +248,8 @@ int hqo_rot_amax(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, in
 //   pass 1: amax of the rotated tensor (skipped when amax_in is given);
 //   pass 2: per 16-element block of a row, block amax, E4M3 block scale,
 //           E2M1 codes, two codes per byte with the even element in the low
-//           nibble ([P1] §2 "lo | (hi << 4)", [P4] "two E2M1 nibbles packed per
-//           byte").
+//           nibble (the packing step of [P1] §2, and the storage layout of [P4]
+//           "The numeric format").
 // q: [M, K/2] bytes, s: [M, K/16] E4M3 bytes, both row-major and contiguous.
 int hqo_quantize(const void* x, int dtype, int64_t M, int64_t K, int64_t ldx, int group,
                  const float* amax_in, uint8_t* q, uint8_t* s, float* amax_out,
@@ -364,9 +364,9 @@ float hqo_global_scale(float amax) { return global_scale(amax); }
 // ===========================================================================
 // MXFP4: E2M1 codes with one power-of-two (E8M0) scale per 32 consecutive
 // elements of a row, no per-tensor scale ("A Fused Hadamard + NVFP4
-// Quantization Kernel in Triton", §1: "MXFP4 (32-element blocks, power-of-two
-// E8M0 scales)"; "Try this": the same error study with MXFP4 semantics, the
-// rotation applied as before).  The pages give no rule for the scale; the
+// Quantization Kernel in Triton", §1, where the format table sets MXFP4 beside
+// NVFP4 with 32-element blocks and power-of-two E8M0 scales; "Try this", which
+// repeats the error study in MXFP4 with the rotation applied as before).  The pages give no rule for the scale; the
 // reading adopted is the usual MX rule: X = 2^(floor(log2 amax_b) - 2), 2 being
 // the exponent of E2M1's largest value 6, so amax_b / X lies in [4, 8); the E8M0
 // byte is that exponent + 127, clamped to [0, 254] (0 for an all-zero block);
