@@ -46,8 +46,8 @@ L2_BYTES = 126 * 1024 * 1024
 # itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.88 GB read + 0.49769 GB written
-    ("270dfcac3d68e5a5", "bf16_32768x28672", 16): 1.88e9 + 0.49769e9,
+    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.88 GB read + 0.49732 GB written
+    ("852840501048b42c", "bf16_32768x28672", 16): 1.88e9 + 0.49732e9,
 }
 
 
@@ -94,6 +94,26 @@ def max_over_ranks(value_ms: float) -> float:
 def throughput_gbs(bytes_per_step_per_rank: int, steps: int, world: int, region_ms: float) -> float:
     """Whole-job GB/s: the bytes every rank processed divided by the slowest rank's time."""
     return bytes_per_step_per_rank * steps * world / (region_ms / 1e3) / 1e9
+
+
+def time_launches(fn, K: int, stream, dev, flush) -> float:
+    """Average milliseconds of one call of fn over K back-to-back calls (CUDA events on the
+    launching stream, 3 untimed calls first; the L2 flush, when given, runs between calls)."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        fn()
+        if flush is not None:
+            flush.fill_(1.0)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / K
 
 
 def load_peaks():
@@ -331,23 +351,22 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     single_ms = d0.elapsed_time(d1) / K
 
+    # ---- pass 2 with the block scales in the swizzled GEMM layout, same tensor ----
+    s_sw = torch.empty(hq.hq_swizzled_scales_bytes(w.M, w.K), dtype=torch.uint8, device=dev)
+    sw_ms = time_launches(lambda: hq.hq_rotate_quant_nvfp4_swizzled(
+        x, group, amax, q=q, scales=s_sw, s_global=sg, stream=stream), K, stream, dev, flush)
+    swz = {"group": group, "ms_per_launch": sw_ms, "bytes_per_launch": step_bytes,
+           "gbs": step_bytes / (sw_ms / 1e3) / 1e9,
+           "note": "hq_rotate_quant_nvfp4_swizzled: pass 2 writing the scales in the 128x4-tile "
+                   "layout of block-scaled NVFP4 GEMMs"}
+    del s_sw
+
     # ---- MXFP4 (E8M0 per 32, single pass) on the same tensor and group ----
     mx = None
     if w.K % 32 == 0:
         s_mx = torch.empty((w.M, w.K // 32), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream)
-        torch.cuda.synchronize(dev)
-        m0 = torch.cuda.Event(enable_timing=True)
-        m1 = torch.cuda.Event(enable_timing=True)
-        m0.record(stream)
-        for _ in range(K):
-            hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream)
-            if flush is not None:
-                flush.fill_(1.0)
-        m1.record(stream)
-        torch.cuda.synchronize(dev)
-        mx_ms = m0.elapsed_time(m1) / K
+        mx_ms = time_launches(lambda: hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream),
+                              K, stream, dev, flush)
         mx_bytes = bytes_in + w.numel // 2 + w.numel // 32
         mx = {"group": group, "ms_per_launch": mx_ms, "bytes_per_launch": mx_bytes,
               "gbs": mx_bytes / (mx_ms / 1e3) / 1e9,
@@ -359,19 +378,8 @@ def run_ours(args, w):
     if w.K <= 32768 and w.K % 256 == 0:
         q8 = torch.empty((w.M, w.K), dtype=torch.int8, device=dev)
         s8 = torch.empty(w.M, dtype=torch.float32, device=dev)
-        for _ in range(3):
-            hq.hq_rotate_quant_int8(x, 256, q=q8, scales=s8, stream=stream)
-        torch.cuda.synchronize(dev)
-        i0 = torch.cuda.Event(enable_timing=True)
-        i1 = torch.cuda.Event(enable_timing=True)
-        i0.record(stream)
-        for _ in range(K):
-            hq.hq_rotate_quant_int8(x, 256, q=q8, scales=s8, stream=stream)
-            if flush is not None:
-                flush.fill_(1.0)
-        i1.record(stream)
-        torch.cuda.synchronize(dev)
-        i8_ms = i0.elapsed_time(i1) / K
+        i8_ms = time_launches(lambda: hq.hq_rotate_quant_int8(x, 256, q=q8, scales=s8, stream=stream),
+                              K, stream, dev, flush)
         i8_bytes = bytes_in + w.numel + 4 * w.M
         int8 = {"group": 256, "ms_per_launch": i8_ms, "bytes_per_launch": i8_bytes,
                 "gbs": i8_bytes / (i8_ms / 1e3) / 1e9,
@@ -404,6 +412,7 @@ def run_ours(args, w):
         int8["frac_of_peak"] = int8["gbs"] / peak
     if mx is not None:
         mx["frac_of_peak"] = mx["gbs"] / peak
+    swz["frac_of_peak"] = swz["gbs"] / peak
     p2 = sum(pass2) / K
     p1 = sum(pass1) / K
     achieved = step_bytes / (p2 / 1e3) / 1e9
@@ -433,6 +442,7 @@ def run_ours(args, w):
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
             "note": "hq_rotate_quant_nvfp4_delayed: quantize with the previous step's amax while "
                     "reducing this one (one read of x); not the metric's two-pass step"},
+        "swizzled_scales": swz,
         "mxfp4": mx,
         "int8_per_token": int8,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": hqz.h2d_bytes,

@@ -13,6 +13,8 @@ from .api import (  # noqa: F401
     hq_rotate_quant_mxfp4,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
+    hq_rotate_quant_nvfp4_swizzled,
+    hq_swizzled_scales_bytes,
     quantize_nvfp4,
 )
 
@@ -26,6 +28,8 @@ __all__ = [
     "hq_rotate_quant_mxfp4",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
+    "hq_rotate_quant_nvfp4_swizzled",
+    "hq_swizzled_scales_bytes",
     "lib_path",
     "load",
     "quantize_nvfp4",

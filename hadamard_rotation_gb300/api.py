@@ -79,6 +79,34 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     return q, scales, s_global
 
 
+def hq_swizzled_scales_bytes(M: int, K: int) -> int:
+    """Bytes of the swizzled scale buffer for an [M, K] tensor (128-row x 4-column tiles)."""
+    n = _lib.load().hq_swizzled_scales_bytes(M, K)
+    if n < 0:
+        raise ValueError("hq_swizzled_scales_bytes: M, K must be >= 0 and K a multiple of 16")
+    return n
+
+
+def hq_rotate_quant_nvfp4_swizzled(x: torch.Tensor, group: int, amax: torch.Tensor,
+                                   q: torch.Tensor | None = None,
+                                   scales: torch.Tensor | None = None,
+                                   s_global: torch.Tensor | None = None,
+                                   stream: torch.cuda.Stream | None = None):
+    """Pass 2 with the block scales in the swizzled tile layout of block-scaled NVFP4 GEMMs:
+    (q uint8 [M, K/2], scales uint8 [hq_swizzled_scales_bytes(M, K)], s_global float32 [1]).
+    Every byte of ``scales`` is written, padding entries as 0."""
+    dt, M, K, ldx = _x_args(x)
+    amax = _need(amax, (1,), torch.float32, x.device, "amax")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    n = hq_swizzled_scales_bytes(M, K)
+    scales = _need(scales, (n,), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    check(_lib.load().hq_rotate_quant_nvfp4_swizzled(
+        _ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q), _ptr(scales), _ptr(s_global),
+        _stream_handle(stream)), "hq_rotate_quant_nvfp4_swizzled")
+    return q, scales, s_global
+
+
 def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.Tensor,
                                   amax_next: torch.Tensor | None = None,
                                   q: torch.Tensor | None = None,

@@ -199,6 +199,18 @@ hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream
                           ring_bytes<HQ_PASS2_STAGES>(kMode, false));
 }
 
+// Pass 2 with swizzled scales: row-group tiles through the TMA ring, one bulk copy
+// per row, so contiguous and strided rows take the same kernel.
+template <int G>
+hq_status dispatch_quant_swizzled(const hq::Params& p, bool bf16, hq_stream s) {
+  using hq::k_rotate_quant_nvfp4;
+  if (bf16)
+    return launch(k_rotate_quant_nvfp4<G, true, hq::kLoadTma, false, true>, p, s,
+                  ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, true));
+  return launch(k_rotate_quant_nvfp4<G, false, hq::kLoadTma, false, true>, p, s,
+                ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, false));
+}
+
 }  // namespace
 
 extern "C" {
@@ -245,6 +257,46 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
     case 0: return dispatch_quant<0, false>(p, bf16, strided, stream);
     case 16: return dispatch_quant<16, false>(p, bf16, strided, stream);
     default: return dispatch_quant<256, false>(p, bf16, strided, stream);
+  }
+}
+
+int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0 || K % 16 != 0) return -1;
+  const int64_t rows = (M + 127) / 128 * 128;
+  const int64_t cols = (K / 16 + 3) / 4 * 4;
+  return rows * cols;
+}
+
+hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                         int64_t ldx, int group, const float* amax, uint8_t* q,
+                                         uint8_t* scales, float* s_global, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (M == 0 || K == 0) return HQ_OK;
+  if (!amax || !q || !scales) return HQ_ERR_NULL;
+  if (!aligned(amax, 4) || !aligned(q, 16) || !aligned(scales, 32) ||
+      (s_global && !aligned(s_global, 4)))
+    return HQ_ERR_ALIGN;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.amax_in = amax;
+  p.q = q;
+  p.s = scales;
+  p.sglobal_out = s_global;
+  // Row-group units: 16 per 128-row tile and column chunk of 128 blocks, 8 tiles each.
+  p.rows = static_cast<uint64_t>(M);
+  const uint64_t n_cc = (static_cast<uint64_t>(K / 16) + hq::kTileBlocks - 1) / hq::kTileBlocks;
+  const uint64_t n_units = static_cast<uint64_t>((M + 127) / 128) * 16u * n_cc;
+  if (n_units > 0x1FFFFFFFull) return HQ_ERR_SHAPE;
+  const uint64_t n_tiles = n_units * 8u;
+  p.n_cc = static_cast<uint32_t>(n_cc);
+  p.div_ncc = make_fast_div(p.n_cc);
+  p.n_tiles = n_tiles;
+  p.swz_col_tiles = static_cast<uint64_t>((K / 16 + 3) / 4);
+  const bool bf16 = dtype == HQ_BF16;
+  switch (group) {
+    case 0: return dispatch_quant_swizzled<0>(p, bf16, stream);
+    case 16: return dispatch_quant_swizzled<16>(p, bf16, stream);
+    default: return dispatch_quant_swizzled<256>(p, bf16, stream);
   }
 }
 

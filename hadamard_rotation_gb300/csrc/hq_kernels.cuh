@@ -90,8 +90,12 @@ struct Params {
   // pass 2
   const float* amax_in;
   uint8_t* q;              // [M, K/2]
-  uint8_t* s;              // [M, K/16]
+  uint8_t* s;              // [M, K/16], or the swizzled tile layout (swz_col_tiles > 0)
   float* sglobal_out;      // optional
+  uint64_t swz_col_tiles;  // swizzled scales: ceil(K/64) tiles of 4 scale columns per tile row
+  uint64_t rows;           // M (row-group tiles)
+  uint32_t n_cc;           // row-group tiles: column chunks of 16 blocks per row, ceil(K/256)
+  FastDiv div_ncc;         // divider for n_cc
   // dequant
   const uint8_t* dq_q;
   const uint8_t* dq_s;
@@ -251,6 +255,20 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const void* src, uint32_t
       "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 32 bytes to global memory in one 256-bit store (32-byte aligned address).
+__device__ __forceinline__ void st_v8(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                      uint32_t e, uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b),
+               "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
+// Arrive on `bar` announcing `bytes` of copies to come (0: a plain arrive).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -436,6 +454,24 @@ enum LoadMode : int {
   kLoadStrided = 2,  // rows ldx apart, vector loads straight into registers
 };
 
+// Row-group units (pass 2 with swizzled scales).  Unit u covers the columns
+// c0 = 128 cc .. c0 + 127 (blocks) of the 8 rows 128 rt + 2 k + {0, 1, 32, 33, 64,
+// 65, 96, 97}, k = 0..15: the rows whose scales of 4 consecutive columns make one
+// 32-byte piece of the swizzled layout.  Its 8 tiles rs = 0..7 (one row each, as
+// contiguous as a plain tile) go to one warp in order.
+// Units run over column chunks fastest, then k, then row tiles rt = 0 ..
+// ceil(M / 128) - 1; rows past M give empty tiles.
+struct RgTile {
+  uint64_t row;     // row of the tile (may be >= M)
+  uint64_t rt;      // row tile (128 rows)
+  uint32_t k;       // row pair within a 32-row band
+  uint64_t c0;      // first column (block) of the chunk
+  uint32_t ncols;   // blocks of the chunk inside the row: 1..128
+  int rs;           // tile within the unit
+  bool present;     // row < M
+};
+
+
 // Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
 // values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
 template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, typename Body>
@@ -506,6 +542,117 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
         ++issued;
       }
       body(base, lane, valid, t);
+    }
+  }
+}
+
+// Row-group units through the TMA ring: warp w of W takes the units w, w + W, ...,
+// each as its 8 tiles in order, and calls body(tile, lane, valid, t) with the
+// RgTile.  The unit positions (row group, column chunk) of the tile being read
+// and of the tile being fetched advance by W units with one carry, no division.
+template <int G, bool BF16, int STAGES, typename Body>
+__device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
+  using R = Ring<BF16, STAGES>;
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const uint32_t gw = blockIdx.x * kWarpsPerCta + wid;
+  const uint32_t nw = gridDim.x * kWarpsPerCta;
+  const uint32_t n_units = static_cast<uint32_t>(p.n_tiles >> 3);  // < 2^29
+  const uint32_t d_rg = fast_div(nw, p.div_ncc);
+  const uint32_t d_cc = nw - d_rg * p.n_cc;
+  struct Pos {
+    uint32_t u, rg, cc;  // unit, its row group (16 per row tile), its column chunk
+  };
+  auto start = [&]() {
+    Pos s;
+    s.u = gw;
+    s.rg = fast_div(gw, p.div_ncc);
+    s.cc = gw - s.rg * p.n_cc;
+    return s;
+  };
+  auto step = [&](Pos& s) {
+    s.u += nw;
+    s.rg += d_rg;
+    s.cc += d_cc;
+    if (s.cc >= p.n_cc) {
+      s.cc -= p.n_cc;
+      s.rg += 1;
+    }
+  };
+  auto tile_at = [&](const Pos& s, int rs) {
+    RgTile g;
+    g.rt = s.rg >> 4;
+    g.k = s.rg & 15u;
+    g.rs = rs;
+    g.row = g.rt * 128u + 2u * g.k + static_cast<uint32_t>(rs & 1) + 32u * static_cast<uint32_t>(rs >> 1);
+    g.c0 = static_cast<uint64_t>(s.cc) * kTileBlocks;
+    const uint64_t left = p.nbr - g.c0;
+    g.ncols = static_cast<uint32_t>(left < kTileBlocks ? left : kTileBlocks);
+    g.present = g.row < p.rows;
+    return g;
+  };
+
+  extern __shared__ __align__(1024) uint8_t hq_smem[];
+  uint8_t* ring = hq_smem + wid * R::kStages * R::kTileBytes;
+  const uint32_t ring_s = smem_addr(ring);
+  const uint32_t bar0 = smem_addr(hq_smem + R::kDataBytes) + wid * R::kStages * 8;
+  const uint64_t policy = l2_stream_policy();
+  auto issue = [&](const RgTile& g, int slot) {
+    if (g.present)
+      tma_load(ring_s + slot * R::kTileBytes, p.x + g.row * p.ldx_bytes + g.c0 * 16u * R::kElemBytes,
+               g.ncols * 16u * R::kElemBytes, bar0 + slot * 8, policy);
+    else
+      mbar_expect_tx(bar0 + slot * 8, 0);  // an empty tile: the phase completes at once
+  };
+
+  if (lane == 0) {
+    for (int s = 0; s < R::kStages; ++s) mbar_init(bar0 + s * 8, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  Pos ip = start();  // the next tile to fetch: unit ip, tile irs
+  int irs = 0;
+  uint64_t issued = 0;
+  for (int s = 0; s < R::kStages && ip.u < n_units; ++s) {
+    if (lane == 0) issue(tile_at(ip, irs), s);
+    ++issued;
+    if (++irs == 8) {
+      irs = 0;
+      step(ip);
+    }
+  }
+  Pos cp = start();  // the tile to read: unit cp, tile crs
+  int crs = 0;
+  for (uint64_t k = 0; cp.u < n_units; ++k) {
+    const int slot = static_cast<int>(k % R::kStages);
+    const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
+    const bool ok = mbar_wait(bar0 + slot * 8, parity);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+      if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+      for (uint64_t m = k; m < issued; ++m)
+        mbar_wait(bar0 + static_cast<int>(m % R::kStages) * 8, static_cast<uint32_t>((m / R::kStages) & 1));
+      return;
+    }
+    const RgTile g = tile_at(cp, crs);
+    bool valid[4];
+    Lane4 t;
+    load_tile_smem<G, BF16, 0>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
+    __syncwarp();  // every lane has read the slot
+    if (ip.u < n_units) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(tile_at(ip, irs), slot);
+      }
+      ++issued;
+      if (++irs == 8) {
+        irs = 0;
+        step(ip);
+      }
+    }
+    body(g, lane, valid, t);
+    if (++crs == 8) {
+      crs = 0;
+      step(cp);
     }
   }
 }
@@ -757,9 +904,13 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
 // ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
-// REDUCE_NEXT: also reduce this tensor's amax into p.amax_out (zeroed by the host
-// call) while quantizing with the given one -- the single-pass, delayed-amax mode.
-template <int G, bool BF16, int MODE, bool REDUCE_NEXT>
+// SWZ: write the scales in the swizzled tile layout of block-scaled NVFP4 GEMMs
+// (cuBLASLt's layout for 16-element block scales): the [M, K/16] scale matrix,
+// padded to whole tiles of 128 rows x 4 columns, each tile 512 contiguous bytes,
+// tiles row-major; inside a tile, row r and column c at (r % 32) * 16 + (r / 32) *
+// 4 + c.  The tiles of this mode are row groups (RgTile), so that every scale
+// store fills whole 32-byte pieces of that layout, padding included.
+template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   // s_global = amax / (448 * 6), or 1 if that is 0.
   const float amax = *p.amax_in;
@@ -775,9 +926,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
   float next_amax = 0.0f;  // max of the block amaxes this thread saw (REDUCE_NEXT)
+  uint32_t swz_acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // SWZ: scale words of the unit's rows
 
-  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(
-      p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
+  // tile: the tile's first block (flat tiles) or its RgTile (SWZ).
+  auto tile_body = [&](const auto& tile, int lane, bool (&valid)[4], Lane4& t) {
     rotate_tile<G>(t, lane);
 
     // Block amax of z, then of y = z / sqrt(G): RN(max|z| * c) = max RN(|z| * c).
@@ -866,18 +1018,69 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
       }
     }
 
-    // Stores: 8 code bytes and 1 scale byte per block, streaming (evict-first).
+    if constexpr (!SWZ) {
+      const uint64_t base = tile;
+      // Stores: 8 code bytes and 1 scale byte per block, streaming (evict-first).
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!valid[j]) continue;
-      const uint64_t b = base + lane_block<G>(lane, j);
-      const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
-      const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;  // s_f == 0: all codes 0
-      __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep, w[j][1] & keep));
-      const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
-      __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
+      for (int j = 0; j < 4; ++j) {
+        if (!valid[j]) continue;
+        const uint64_t b = base + lane_block<G>(lane, j);
+        const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
+        const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;  // s_f == 0: all codes 0
+        __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep, w[j][1] & keep));
+        const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
+        __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
+      }
+    } else {
+      // Row-group unit tile (base = tile index): one row segment, as a flat tile.
+      const RgTile& g = tile;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (!valid[j]) continue;
+        const uint64_t b = g.row * p.nbr + g.c0 + lane_block<G>(lane, j);
+        const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
+        const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;
+        __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep, w[j][1] & keep));
+      }
+      // Scales.  Row r, column c of the scale matrix sits at 512 * (row tile *
+      // swz_col_tiles + c / 4) + (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4, so the
+      // unit's 8 rows x 4 columns are the 32 bytes at 32 k of a column tile, row rs
+      // in word 4 (rs & 1) + (rs >> 1).  Lane L collects column group L (columns
+      // c0 + 4L .. + 3) of the unit's rows and writes its 32 bytes after the last
+      // tile.  Blocks outside the tensor carry scale 0, which the padding must hold.
+      // The 4 bytes of 4 consecutive columns (lanes 4m .. 4m+3) first go to lane 4m.
+      uint32_t word[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
+        const uint32_t w2 = sbyte | (__shfl_down_sync(0xFFFFFFFFu, sbyte, 1) << 8);
+        word[j] = w2 | (__shfl_down_sync(0xFFFFFFFFu, w2, 2) << 16);
+      }
+      // Column group L sits in lane 4 (L % 8), slot L / 8 (G <= 16: block 32 j + lane),
+      // or in lane 4 (L / 4), slot L % 4 (G = 256: block 16 (lane / 4) + lane % 4 + 4 j).
+      const int src = (G == 256) ? (lane & ~3) : 4 * (lane & 7);
+      const int want = (G == 256) ? (lane & 3) : (lane >> 3);
+      uint32_t mine = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t v = __shfl_sync(0xFFFFFFFFu, word[j], src);
+        if (j == want) mine = v;
+      }
+#pragma unroll
+      for (int i = 0; i < 7; ++i) swz_acc[i] = swz_acc[i + 1];
+      swz_acc[7] = mine;  // swz_acc[rs] holds row rs once rs = 7
+      if (g.rs == 7) {
+        const uint64_t ct = g.c0 / 4 + lane;
+        if (ct < p.swz_col_tiles)
+          st_v8(p.s + (g.rt * p.swz_col_tiles + ct) * 512u + 32u * g.k, swz_acc[0], swz_acc[2], swz_acc[4],
+                swz_acc[6], swz_acc[1], swz_acc[3], swz_acc[5], swz_acc[7]);
+      }
     }
-  });
+  };
+  if constexpr (SWZ)
+    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body);
+  else
+    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(p, tile_body);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
 }
 

@@ -110,6 +110,32 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
 /*
+ * hq_rotate_quant_nvfp4_swizzled -- pass 2 exactly as hq_rotate_quant_nvfp4, with the E4M3 block
+ * scales written straight into the tiled layout that block-scaled NVFP4 GEMMs read.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §6 "From interpreter to
+ *    hardware", Layout: cuBLASLt and CUTLASS take the block scales in a swizzled tiled layout,
+ *    and a production kernel writes it directly; the page does not spell the layout out.  The
+ *    layout here is cuBLASLt's for 16-element block scales; the GPU tests check it by feeding
+ *    the output to cuBLASLt's NVFP4 GEMM.)
+ *
+ *   scales : hq_swizzled_scales_bytes(M, K) bytes, 32-byte aligned.  The [M, K/16] scale
+ *            matrix is padded to R = round_up(M, 128) rows and C = round_up(K/16, 4) columns
+ *            and cut into tiles of 128 rows x 4 columns; tile (i, j) is the 512 bytes at
+ *            (i * C/4 + j) * 512, and inside it row r, column c (r < 128, c < 4) is the byte
+ *            (r % 32) * 16 + (r / 32) * 4 + c.  Every byte is written, padding entries as 0
+ *            (a GEMM reads them).
+ *   Everything else (x, amax, q, s_global, group, errors) as hq_rotate_quant_nvfp4.
+ */
+HQ_API hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t M,
+                                                int64_t K, int64_t ldx, int group,
+                                                const float* amax, uint8_t* q, uint8_t* scales,
+                                                float* s_global, hq_stream stream);
+
+/* Size in bytes of the swizzled scale buffer for an [M, K] tensor (-1 if M < 0, K < 0 or
+ * K % 16 != 0). */
+HQ_API int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K);
+
+/*
  * hq_rotate_quant_nvfp4_delayed -- single-pass mode: quantize with an amax kept from an earlier
  *   step while reducing this tensor's amax for the next one.
  *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2, on the global scale:

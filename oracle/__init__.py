@@ -23,4 +23,6 @@ from .hq_oracle import (  # noqa: F401
     rot_amax,
     rotate,
     rotate_quant_int8,
+    swizzle_scales,
+    unswizzle_scales,
 )

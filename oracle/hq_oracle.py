@@ -247,3 +247,39 @@ def dequant_mxfp4(q: np.ndarray, s: np.ndarray, group: int, unrotate: bool,
                              _threads(nthreads)):
         raise ValueError("hqo_dequant_mxfp4: bad arguments")
     return out
+
+
+def swizzle_scales(s: np.ndarray) -> np.ndarray:
+    """Row-major block scales [M, K/16] -> the swizzled tile layout of block-scaled NVFP4 GEMMs.
+
+    "A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §6 "From interpreter to hardware"
+    (Layout): GEMM consumers take the scales in a swizzled tiled layout, not spelled out on the
+    page.  Reading: cuBLASLt's layout for 16-element block scales.  The matrix is padded with
+    zeros to R = round_up(M, 128) rows and C = round_up(K/16, 4) columns and cut into tiles of
+    128 rows x 4 columns; tile (i, j) is the 512 bytes at (i * C/4 + j) * 512, and inside it row
+    r, column c is the byte (r % 32) * 16 + (r / 32) * 4 + c.  Pinned on the GPU by feeding the
+    library's output to cuBLASLt's NVFP4 GEMM (tests/test_gpu_swizzle.py).
+    """
+    s = np.ascontiguousarray(s, np.uint8)
+    M, C0 = s.shape
+    R = -(-M // 128) * 128
+    C = -(-C0 // 4) * 4
+    out = np.zeros(R * C, np.uint8)
+    for r in range(M):
+        i, rr = divmod(r, 128)
+        for c in range(C0):
+            j, cc = divmod(c, 4)
+            out[(i * (C // 4) + j) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + cc] = s[r, c]
+    return out
+
+
+def unswizzle_scales(buf: np.ndarray, M: int, C0: int) -> np.ndarray:
+    """Inverse of swizzle_scales: the [M, C0] row-major scales held in a swizzled buffer."""
+    C = -(-C0 // 4) * 4
+    out = np.empty((M, C0), np.uint8)
+    for r in range(M):
+        i, rr = divmod(r, 128)
+        for c in range(C0):
+            j, cc = divmod(c, 4)
+            out[r, c] = buf[(i * (C // 4) + j) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + cc]
+    return out

@@ -205,3 +205,23 @@ def test_mxfp4_argument_checks(lib):
     assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 48, 0, 0, P(FAKE), None) == 2
     assert lib.hq_dequant_mxfp4(None, P(FAKE), 4, 64, 0, 0, P(FAKE), None) == 1
     assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 64, 0, 1, P(FAKE), None) == 5
+
+
+def test_swizzled_argument_checks_and_size(lib):
+    def sw(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, a=FAKE, q=FAKE, s=FAKE, sg=None):
+        return lib.hq_rotate_quant_nvfp4_swizzled(
+            P(x) if x else None, dt, M, K, ldx, G, P(a) if a else None, P(q) if q else None,
+            P(s) if s else None, P(sg) if sg else None, None)
+    assert sw(a=0) == 1 and sw(q=0) == 1 and sw(s=0) == 1 and sw(x=0) == 1
+    assert sw(G=32) == 5 and sw(dt=2) == 4 and sw(K=24, ldx=24) == 2
+    assert sw(s=FAKE + 4) == 3 and sw(s=FAKE + 16) == 3   # the swizzled scales are 32-byte aligned
+    assert sw(q=FAKE + 8) == 3 and sw(x=FAKE + 8) == 3
+    assert sw(M=0) == 0
+    # tiles of 128 rows x 4 scale columns, padded
+    assert lib.hq_swizzled_scales_bytes(1, 16) == 128 * 4
+    assert lib.hq_swizzled_scales_bytes(128, 64) == 128 * 4
+    assert lib.hq_swizzled_scales_bytes(129, 64) == 256 * 4
+    assert lib.hq_swizzled_scales_bytes(200, 96) == 256 * 8
+    assert lib.hq_swizzled_scales_bytes(32768, 28672) == 32768 * 1792
+    assert lib.hq_swizzled_scales_bytes(0, 0) == 0
+    assert lib.hq_swizzled_scales_bytes(4, 24) == -1 and lib.hq_swizzled_scales_bytes(-1, 16) == -1
