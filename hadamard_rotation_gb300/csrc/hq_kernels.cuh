@@ -707,15 +707,14 @@ __device__ __forceinline__ void rotate_tile(Lane4& t, int lane) {
     butterfly16(t.P[1]);
     if constexpr (G == 256) {
       cross_lane_stages(t, lane);
-      // h = 64: register block j <-> j ^ 1, i.e. the two halves of each pair.
+      // h = 64: register block j <-> j ^ 1, i.e. the two halves of each pair:
+      // (a, b) -> (a + b, a - b) = fma((a, b), (1, -1), (b, a)), one rounding each.
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = t.P[k][i].x;
-          const float b = t.P[k][i].y;
-          t.P[k][i].x = __fadd_rn(a, b);
-          t.P[k][i].y = __fsub_rn(a, b);
+          const float2 v = t.P[k][i];
+          t.P[k][i] = fma2(v, make_float2(1.0f, -1.0f), make_float2(v.y, v.x));
         }
       }
       // h = 128: register block j <-> j ^ 2, i.e. pair 0 against pair 1.
