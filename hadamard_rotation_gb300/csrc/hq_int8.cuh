@@ -162,12 +162,111 @@ __device__ __forceinline__ uint32_t pack_i8x4(uint32_t b0, uint32_t b1, uint32_t
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
+// ---------------------------------------------------------------------------
+// Tensor memory (TMEM) for parking a rotated tile.  The CTA allocates all 512
+// columns once; warp w may touch TMEM lanes 32 (w % 4) .. + 31 only, and parks a
+// tile (64 fp32 values per lane) in 64 consecutive columns of its lanes.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kI8TmemCols = 512;
+
+__device__ __forceinline__ void tmem_alloc_all(uint32_t smem_dst) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_dst),
+               "r"(kI8TmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_all(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kI8TmemCols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 64 32-bit registers of each lane -> 64 consecutive TMEM columns of its lane.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]),
+        "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]), "r"(v[37]), "r"(v[38]), "r"(v[39]),
+        "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]), "r"(v[46]), "r"(v[47]),
+        "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]), "r"(v[55]),
+        "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+        "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
+        "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
+        "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+        "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void lane4_to_words(const Lane4& t, uint32_t (&v)[64]) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[32 * k + 2 * i] = __float_as_uint(t.P[k][i].x);
+      v[32 * k + 2 * i + 1] = __float_as_uint(t.P[k][i].y);
+    }
+}
+
+__device__ __forceinline__ void words_to_lane4(const uint32_t (&v)[64], Lane4& t) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      t.P[k][i] = make_float2(__uint_as_float(v[32 * k + 2 * i]), __uint_as_float(v[32 * k + 2 * i + 1]));
+}
+
+// One arrival on an mbarrier (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Max of a non-negative float (or NaN with the sign bit clear) over the warp:
+// such floats order like their bit patterns as unsigned integers.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(v)));
+}
+
 // FULL: every warp tile of a row is complete (K a multiple of the tile), so no
 // block needs a bounds check.
+//
+// Software pipeline.  Step it rotates this warp's tile of iteration it, publishes
+// its amax and parks the rotated values in TMEM (slot it % 2); then it waits for
+// the row of iteration it - 1 to be complete, takes that tile back from TMEM and
+// quantizes it.  A row's T warps meet on an mbarrier (T arrivals), not a CTA
+// barrier, so while one warp waits the others rotate.  Tile maxima and row
+// barriers rotate over 4 buffers: a warp reuses buffer b at iteration i + 4 only
+// after the row of iteration i + 2 is complete, that is after every warp of the row
+// has passed iteration i + 2 and so has read buffer b (it reads it at i + 1).
 template <int G, bool BF16, int MODE, bool FULL>
 __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p) {
   constexpr int es = BF16 ? 2 : 4;
   constexpr int kTileBytes = kI8TileElems * es;
+  constexpr int kBufs = 4;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
@@ -180,15 +279,28 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
       FULL ? kI8TileElems : (has_role ? (p.K - chunk0 < kI8TileElems ? p.K - chunk0 : kI8TileElems) : 0);
   auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < nvalid; };
 
-  // Per-warp tile maxima, double buffered so that one barrier per iteration
-  // suffices: a warp can only overwrite a buffer after every warp has passed the
-  // barrier that follows its last read of it.
-  __shared__ float tile_max[2][kI8Warps];
+  __shared__ float tile_max[kBufs][kI8Warps];
+  __shared__ __align__(8) uint64_t row_bar[kBufs][kI8Warps];  // [buffer][row_local], T arrivals
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ volatile int cta_broken;  // a wait ran out somewhere in the CTA: everyone stops
   extern __shared__ __align__(1024) uint8_t hq_smem[];
   uint8_t* ring = hq_smem + wid * kI8Stages * kI8TileElems * 2;
   const uint32_t ring_s = smem_addr(ring);
   const uint32_t bar0 = smem_addr(hq_smem + kI8Warps * kI8Stages * kI8TileElems * 2) + wid * kI8Stages * 8;
   const uint64_t policy = l2_stream_policy();
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kBufs; ++b)
+      for (int r = 0; r < R; ++r) mbar_init(smem_addr(&row_bar[b][r]), static_cast<uint32_t>(T));
+    cta_broken = 0;
+    fence_mbar_init();
+  }
+  if (wid == 0) tmem_alloc_all(smem_addr(&tmem_base_slot));
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem_warp = tmem_base_slot + ((32u * static_cast<uint32_t>(wid & 3)) << 16) +
+                             128u * static_cast<uint32_t>(wid >> 2);
 
   auto row_of = [&](int64_t it) -> int64_t {
     return (static_cast<int64_t>(blockIdx.x) + it * gridDim.x) * R + row_local;
@@ -201,7 +313,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   };
   auto mine = [&](int64_t it) { return has_role && row_of(it) < p.M; };
 
-  bool broken = false;   // a wait timed out: stop touching memory, keep the barriers
+  bool broken = false;   // stop touching memory and waiting
   int64_t issued = 0;    // this warp's iterations handed to TMA: 0 .. issued-1
   if constexpr (MODE == kLoadTma) {
     if (lane == 0) {
@@ -215,27 +327,41 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
       issued = s + 1;
     }
   }
+  auto fail = [&](int64_t from) {  // record the fault, drain this warp's copies, stop
+    if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+    cta_broken = 1;
+    if constexpr (MODE == kLoadTma)
+      for (int64_t m = from; m < issued; ++m)
+        mbar_wait(bar0 + static_cast<int>(m % kI8Stages) * 8, static_cast<uint32_t>((m / kI8Stages) & 1));
+    broken = true;
+  };
 
   const int64_t first_rows = static_cast<int64_t>(blockIdx.x) * R;
-  for (int64_t it = 0; first_rows + it * gridDim.x * R < p.M; ++it) {
-    const int64_t r = row_of(it);
-    const int buf = static_cast<int>(it & 1);
-    const bool active = mine(it);
-    Lane4 t;
-    float sign = 1.0f;
-    float amax = 0.0f;
-    if (active) {
-      if constexpr (MODE == kLoadTma) {
-        const int slot = static_cast<int>(it % kI8Stages);
-        const bool ok = !broken && mbar_wait(bar0 + slot * 8, static_cast<uint32_t>((it / kI8Stages) & 1));
-        if (!broken && !__all_sync(0xFFFFFFFFu, ok)) {
-          if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
-          // wait (bounded) for the copies still in flight: iterations it .. issued-1
-          for (int64_t m = it; m < issued; ++m)
-            mbar_wait(bar0 + static_cast<int>(m % kI8Stages) * 8, static_cast<uint32_t>((m / kI8Stages) & 1));
-          broken = true;
-        }
-        if (!broken) {
+  int64_t n_it = 0;  // iterations of this CTA
+  if (first_rows < p.M) n_it = (p.M - first_rows + static_cast<int64_t>(gridDim.x) * R - 1) /
+                               (static_cast<int64_t>(gridDim.x) * R);
+  int64_t drained_from = 0;  // first iteration whose copy may still be in flight
+  constexpr float kSign = (G == 64) ? -1.0f : 1.0f;  // the registers hold kSign * y
+  for (int64_t it = 0; has_role && it <= n_it; ++it) {
+    if (!broken && cta_broken) {
+      fail(drained_from);
+      break;
+    }
+    if (broken) break;
+    // ---- A: rotate tile it, publish its amax, park it in TMEM ----
+    if (it < n_it) {
+      const bool active = mine(it);
+      const int buf = static_cast<int>(it % kBufs);
+      Lane4 t;
+      float amax = 0.0f;
+      if (active) {
+        if constexpr (MODE == kLoadTma) {
+          const int slot = static_cast<int>(it % kI8Stages);
+          const bool ok = mbar_wait(bar0 + slot * 8, static_cast<uint32_t>((it / kI8Stages) & 1));
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            fail(it);
+            break;
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t bl = i8_in_block<G>(lane, j);
@@ -252,6 +378,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
             put_block(t, j, f);
           }
           __syncwarp();
+          drained_from = it + 1;
           if (mine(it + kI8Stages)) {
             if (lane == 0) {
               fence_proxy_async_smem();
@@ -259,75 +386,101 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
             }
             issued = it + kI8Stages + 1;
           }
-        }
-      } else {
-        const uint8_t* rowp = p.x + r * p.ldx_bytes + chunk0 * es;
+        } else {
+          const uint8_t* rowp = p.x + row_of(it) * p.ldx_bytes + chunk0 * es;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t bl = i8_in_block<G>(lane, j);
-          const bool ok = block_ok(bl);
-          uint4 w4[BF16 ? 2 : 4];
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t bl = i8_in_block<G>(lane, j);
+            const bool ok = block_ok(bl);
+            uint4 w4[BF16 ? 2 : 4];
 #pragma unroll
-          for (int k = 0; k < (BF16 ? 2 : 4); ++k)
-            w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + k)
-                       : make_uint4(0u, 0u, 0u, 0u);
-          float f[16];
-          widen<BF16>(w4, f);
-          put_block(t, j, f);
+            for (int k = 0; k < (BF16 ? 2 : 4); ++k)
+              w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + k)
+                         : make_uint4(0u, 0u, 0u, 0u);
+            float f[16];
+            widen<BF16>(w4, f);
+            put_block(t, j, f);
+          }
         }
-      }
-      if (!broken) {
-        sign = rotate_regular<G>(t);
+        rotate_regular<G>(t);
 #pragma unroll
         for (int k = 0; k < 2; ++k)
           amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
+        uint32_t v[64];
+        lane4_to_words(t, v);
+        tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(it & 1), v);
+      }
+      amax = warp_max_nonneg(amax);
+      if (lane == 0) {
+        tile_max[buf][wid] = amax;
+        mbar_arrive(smem_addr(&row_bar[buf][row_local]));
       }
     }
-    // amax of the row: warp max, then the row's T warps through shared memory.
+    // ---- B: quantize tile it - 1 once its row is complete ----
+    if (it >= 1) {
+      const int64_t jt = it - 1;
+      const int buf = static_cast<int>(jt % kBufs);
+      const bool ok = mbar_wait(smem_addr(&row_bar[buf][row_local]), static_cast<uint32_t>((jt / kBufs) & 1));
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        fail(drained_from);
+        break;
+      }
+      if (mine(jt)) {
+        const int64_t r = row_of(jt);
+        // T <= 16: each half-warp reads the row's T tile maxima.
+        const int c = lane & 15;
+        const float row_amax = warp_max_nonneg(c < T ? tile_max[buf][row_local * T + c] : 0.0f);
+        const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
+        const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
+        if (chunk == 0 && lane == 0) p.scales[r] = scale;
+        uint32_t v[64];
+        tmem_wait_st();
+        tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(jt & 1), v);
+        tmem_wait_ld();
+        Lane4 t;
+        words_to_lane4(v, t);
+        const float2 inv2 = make_float2(inv, inv);
+        // rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
+        // rounds (half to even) to an integer held, two's complement, in the low bits.
+        // The sum is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA
+        // 13.0, -O3) fuses a packed multiply whose only use is a packed add into one
+        // fused multiply-add even when both carry an explicit .rn, and rint of the
+        // unrounded product differs where RN(y * inv) is exactly k + 1/2.
+        const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+        const float2 one2 = make_float2(1.0f, 1.0f);
+        int8_t* qrow = p.q + r * p.K + chunk0;
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
-    if (lane == 0) tile_max[buf][wid] = amax;
-    __syncthreads();
-    if (active && !broken) {
-      // T <= 16: each half-warp reads the row's T tile maxima and reduces them.
-      const int c = lane & 15;
-      float row_amax = c < T ? tile_max[buf][row_local * T + c] : 0.0f;
+        for (int k = 0; k < 2; ++k) {
+          uint32_t bx[16], by[16];
 #pragma unroll
-      for (int m = 8; m >= 1; m >>= 1) row_amax = max_nan(row_amax, __shfl_xor_sync(0xFFFFFFFFu, row_amax, m));
-      const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
-      const float inv = __fdiv_rn(1.0f, scale) * sign;  // -inv when the registers hold -y
-      if (chunk == 0 && lane == 0) p.scales[r] = scale;
-      const float2 inv2 = make_float2(inv, inv);
-      // rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
-      // rounds (half to even) to an integer held, two's complement, in the low bits.
-      // The sum is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA
-      // 13.0, -O3) fuses a packed multiply whose only use is a packed add into one
-      // fused multiply-add even when both carry an explicit .rn, and rint of the
-      // unrounded product differs where RN(y * inv) is exactly k + 1/2.
-      const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
-      const float2 one2 = make_float2(1.0f, 1.0f);
-      int8_t* qrow = p.q + r * p.K + chunk0;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint32_t bx[16], by[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 v = fma2(mul2(t.P[k][i], inv2), one2, magic2);
-          bx[i] = __float_as_uint(v.x);
-          by[i] = __float_as_uint(v.y);
+          for (int i = 0; i < 16; ++i) {
+            const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+            bx[i] = __float_as_uint(w.x);
+            by[i] = __float_as_uint(w.y);
+          }
+          const uint32_t box = i8_out_block<G>(lane, 2 * k);
+          const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
+          if (block_ok(box))
+            __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
+                   make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
+                              pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
+          if (block_ok(boy))
+            __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
+                   make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
+                              pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
         }
-        const uint32_t box = i8_out_block<G>(lane, 2 * k);
-        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
-        if (block_ok(box))
-          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
-                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
-                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
-        if (block_ok(boy))
-          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
-                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
-                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
       }
     }
+  }
+  // Wait for this thread's TMEM traffic (a warp that stopped early may have a store
+  // in flight), then free the columns.
+  tmem_wait_st();
+  tmem_wait_ld();
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (wid == 0) {
+    tmem_fence_after_sync();
+    tmem_dealloc_all(tmem_base_slot);
   }
 }
 
