@@ -15,6 +15,26 @@
 #include "hq_internal.h"
 #include "hq_kernels.cuh"
 
+namespace hq {
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one warp waits on an mbarrier that nothing
+// completes; the wait gives up after about kWaitLimitNs and the fault is recorded.
+// ---------------------------------------------------------------------------
+__global__ void k_selftest_bounded_wait() {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(b, 0);  // phase 0 never completes
+  if (!__all_sync(0xFFFFFFFFu, ok) && threadIdx.x == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+}
+
+}  // namespace hq
+
 namespace {
 thread_local int g_last_cuda_error = 0;
 }  // namespace
@@ -447,7 +467,22 @@ hq_status hq_read_fault(unsigned int* fault, int clear) {
     e = cudaMemcpyToSymbol(g_hq_fault, &zero, sizeof(unsigned int));
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  unsigned int int8_word = 0;  // the int8 kernels' copy (hq_int8.cu)
+  e = hq::int8_fault_word(&int8_word, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *fault |= int8_word;
   return HQ_OK;
+}
+
+hq_status hq_selftest_bounded_wait(int unit, hq_stream stream) {
+  if (unit != 0 && unit != 1) return HQ_ERR_SHAPE;
+  if (unit == 1) {
+    const cudaError_t e = hq::int8_selftest_bounded_wait(static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HQ_OK : cuda_fail(e);
+  }
+  hq::k_selftest_bounded_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? HQ_OK : cuda_fail(e);
 }
 
 int hq_version(void) { return 100; }

@@ -48,6 +48,35 @@ hq_status dispatch_int8(const hq::I8Params& p, bool bf16, hq_stream s) {
 
 }  // namespace
 
+namespace hq {
+// The bounded-wait self-test in this translation unit (see k_selftest_bounded_wait in hq.cu).
+__global__ void k_int8_selftest_bounded_wait() {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(b, 0);  // phase 0 never completes
+  if (!__all_sync(0xFFFFFFFFu, ok) && threadIdx.x == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+}
+}  // namespace hq
+
+cudaError_t hq::int8_selftest_bounded_wait(cudaStream_t stream) {
+  k_int8_selftest_bounded_wait<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t hq::int8_fault_word(unsigned int* fault, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(fault, g_hq_fault, sizeof(unsigned int));
+  if (e == cudaSuccess && clear && *fault) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_hq_fault, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
 extern "C" {
 
 hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,

@@ -56,7 +56,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
 
 }  // namespace hq
 
-// Device-side fault word of the library (one per device that loads it).
+// Device-side fault word.  The library is compiled without relocatable device
+// code, so every translation unit that includes this header has its own copy
+// (one per device that loads the library); hq_read_fault() combines them.
 __device__ unsigned int g_hq_fault;
 
 namespace hq {

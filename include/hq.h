@@ -237,6 +237,19 @@ HQ_API int hq_last_cuda_error(void);
 HQ_API hq_status hq_read_fault(unsigned int* fault, int clear);
 
 /*
+ * hq_selftest_bounded_wait -- a test of the failure detection above, not part of the
+ * quantization path (the pages have no counterpart).  Launches one warp on `stream` that waits,
+ * through the same bounded mbarrier wait as the kernels' tile pipelines, on a barrier that nothing
+ * ever completes.  After about one second the wait gives up, the kernel sets bit 0 of the fault
+ * word and returns; no memory is touched and the context stays usable.  Returns once the launch
+ * is enqueued (read the result with hq_read_fault).
+ *   unit : 0 runs the wait in the translation unit of the NVFP4 / MXFP4 kernels, 1 in that of
+ *          the INT8 kernel (each has its own copy of the fault word; hq_read_fault reads both).
+ *          Anything else: HQ_ERR_SHAPE.
+ */
+HQ_API hq_status hq_selftest_bounded_wait(int unit, hq_stream stream);
+
+/*
  * Host pipeline -- quantize tensors that live in (pinned) host memory.
  *   Not a step of the method itself: the transport around it.  One submission copies x to the
  *   device, runs hq_rot_amax and hq_rotate_quant_nvfp4 there, and copies the codes, the scales

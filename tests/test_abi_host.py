@@ -225,3 +225,7 @@ def test_swizzled_argument_checks_and_size(lib):
     assert lib.hq_swizzled_scales_bytes(32768, 28672) == 32768 * 1792
     assert lib.hq_swizzled_scales_bytes(0, 0) == 0
     assert lib.hq_swizzled_scales_bytes(4, 24) == -1 and lib.hq_swizzled_scales_bytes(-1, 16) == -1
+
+
+def test_selftest_argument_check(lib):
+    assert lib.hq_selftest_bounded_wait(2, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
