@@ -219,6 +219,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
       : "memory");
 }
 
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
           amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
         uint32_t v[64];
         lane4_to_words(t, v);
-        tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(it & 1), v);
+        const uint32_t ta = tmem_warp + 64u * static_cast<uint32_t>(it & 1);
+        tmem_st64(ta, v);
       }
       amax = warp_max_nonneg(amax);
       if (lane == 0) {
@@ -435,7 +437,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
         if (chunk == 0 && lane == 0) p.scales[r] = scale;
         uint32_t v[64];
         tmem_wait_st();
-        tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(jt & 1), v);
+        const uint32_t ta = tmem_warp + 64u * static_cast<uint32_t>(jt & 1);
+        tmem_ld64(ta, v);
         tmem_wait_ld();
         Lane4 t;
         words_to_lane4(v, t);
