@@ -1,12 +1,15 @@
 // hq_host.cu -- host pipeline of libhq: quantize tensors that live in host memory.
 //
 // One submission = copy x host -> device, pass 1 (hq_rot_amax), pass 2
-// (hq_rotate_quant_nvfp4), copy codes, scales and s_global device -> host.
+// (hq_rotate_quant_nvfp4), codes, scales and s_global device -> host.
 // Consecutive submissions overlap: two buffer sets in the caller's device
 // workspace alternate, and the three phases run on three streams ordered by
 // events, so the input copy of submission n+1 runs while submission n computes
-// and while its outputs travel back (the two copy directions use separate copy
-// engines).
+// and while its outputs travel back.  The input moves by a copy engine; the
+// outputs are stored into the host buffers by a kernel (k_copy_out) wherever the
+// device can write them (pinned or registered memory, or pageable memory on a
+// device that reaches it through the host page tables), else copied.  Separate
+// device-to-host copies had shared a copy engine with the next input copy.
 //
 //   in stream      H2D(n) ........ H2D(n+1) ........ H2D(n+2)
 //   compute stream        pass1,2(n)         pass1,2(n+1)
@@ -42,11 +45,46 @@ struct hq_host_pipeline {
   } slot[2];
   cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
   uint64_t submitted = 0;
+  bool pageable_writable = false;  // the device writes pageable host memory through the host page tables
+  int copy_out_ctas = 0;
 };
 
 namespace {
 
 hq_status fail(cudaError_t e) { return hq::cuda_fail(e); }
+
+// Results to host memory by SMs rather than a copy engine.  Several device-to-host
+// copies per submission shared a copy engine with the next submission's host-to-device
+// copy and serialised with it; SM stores to host memory run beside that copy.
+__global__ void k_copy_out(const uint8_t* __restrict__ q, uint8_t* __restrict__ q_host, size_t q_bytes,
+                           const uint8_t* __restrict__ s, uint8_t* __restrict__ s_host, size_t s_bytes,
+                           const float* __restrict__ sg, float* __restrict__ sg_host) {
+  const size_t i0 = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  auto copy = [&](const uint8_t* src, uint8_t* dst, size_t n) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0;
+    const size_t nv = vec ? n / 16 : 0;
+    for (size_t k = i0; k < nv; k += stride)
+      reinterpret_cast<uint4*>(dst)[k] = __ldcs(reinterpret_cast<const uint4*>(src) + k);
+    for (size_t k = nv * 16 + i0; k < n; k += stride) dst[k] = src[k];
+  };
+  copy(q, q_host, q_bytes);
+  copy(s, s_host, s_bytes);
+  if (i0 == 0) sg_host[0] = sg[0];
+}
+
+// The device address through which a kernel may write host buffer p, or nullptr if
+// it may not (then a copy engine moves the data).
+void* device_view(const void* p, bool pageable_writable) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;  // pinned or registered
+  if (a.type == cudaMemoryTypeUnregistered && pageable_writable) return const_cast<void*>(p);
+  return nullptr;
+}
 
 constexpr size_t kAlign = 256;
 
@@ -137,6 +175,17 @@ hq_status hq_host_pipeline_create(int64_t M, int64_t K, hq_dtype dtype, int grou
       return fail(e);
     }
   }
+  int pma = 0, host_tables = 0, sms = 0;
+  if ((e = cudaDeviceGetAttribute(&pma, cudaDevAttrPageableMemoryAccess, p->device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                                  p->device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device)) != cudaSuccess) {
+    destroy_objects(p);
+    delete p;
+    return fail(e);
+  }
+  p->pageable_writable = pma && host_tables;
+  p->copy_out_ctas = sms;
   if ((e = cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking)) != cudaSuccess ||
       (e = cudaStreamCreateWithFlags(&p->compute, cudaStreamNonBlocking)) != cudaSuccess ||
       (e = cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking)) != cudaSuccess) {
@@ -175,18 +224,28 @@ hq_status hq_host_pipeline_submit(hq_host_pipeline* p, const void* x_host, uint8
                                s.sglobal, p->compute);
   if (st == HQ_OK && (e = cudaEventRecord(s.compute_done, p->compute)) != cudaSuccess)
     st = fail(e);
-  // output copies
+  // outputs to the host: stored by a kernel where the device can write the buffers,
+  // otherwise copied
   if (st == HQ_OK && (e = cudaStreamWaitEvent(p->out, s.compute_done, 0)) != cudaSuccess)
     st = fail(e);
-  if (st == HQ_OK &&
-      (e = cudaMemcpyAsync(q_host, s.q, p->q_bytes, cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
-    st = fail(e);
-  if (st == HQ_OK && (e = cudaMemcpyAsync(scales_host, s.s, p->s_bytes, cudaMemcpyDeviceToHost,
-                                          p->out)) != cudaSuccess)
-    st = fail(e);
-  if (st == HQ_OK && (e = cudaMemcpyAsync(s_global_host, s.sglobal, sizeof(float),
-                                          cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
-    st = fail(e);
+  void* qv = device_view(q_host, p->pageable_writable);
+  void* sv = device_view(scales_host, p->pageable_writable);
+  void* gv = device_view(s_global_host, p->pageable_writable);
+  if (st == HQ_OK && qv && sv && gv) {
+    k_copy_out<<<p->copy_out_ctas, 512, 0, p->out>>>(s.q, static_cast<uint8_t*>(qv), p->q_bytes, s.s,
+                                                     static_cast<uint8_t*>(sv), p->s_bytes, s.sglobal,
+                                                     static_cast<float*>(gv));
+    if ((e = cudaGetLastError()) != cudaSuccess) st = fail(e);
+  } else if (st == HQ_OK) {
+    if ((e = cudaMemcpyAsync(q_host, s.q, p->q_bytes, cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+      st = fail(e);
+    if (st == HQ_OK && (e = cudaMemcpyAsync(scales_host, s.s, p->s_bytes, cudaMemcpyDeviceToHost,
+                                            p->out)) != cudaSuccess)
+      st = fail(e);
+    if (st == HQ_OK && (e = cudaMemcpyAsync(s_global_host, s.sglobal, sizeof(float),
+                                            cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+      st = fail(e);
+  }
   if (st == HQ_OK && (e = cudaEventRecord(s.out_done, p->out)) != cudaSuccess) st = fail(e);
   if (st == HQ_OK) {
     s.used = true;

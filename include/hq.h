@@ -252,11 +252,14 @@ HQ_API hq_status hq_selftest_bounded_wait(int unit, hq_stream stream);
 /*
  * Host pipeline -- quantize tensors that live in (pinned) host memory.
  *   Not a step of the method itself: the transport around it.  One submission copies x to the
- *   device, runs hq_rot_amax and hq_rotate_quant_nvfp4 there, and copies the codes, the scales
+ *   device, runs hq_rot_amax and hq_rotate_quant_nvfp4 there, and moves the codes, the scales
  *   and s_global back.  Consecutive submissions overlap: the pipeline alternates between two
  *   buffer sets in the caller's device workspace and runs input copies, kernels and output
- *   copies on three streams of its own, ordered by events, so the input copy of one submission
- *   runs while the previous one computes and copies its results back.
+ *   transfers on three streams of its own, ordered by events, so the input copy of one
+ *   submission runs while the previous one computes and sends its results back.  The outputs
+ *   are written into the host buffers by a small kernel when the device can address them
+ *   (pinned or registered memory, or any host memory on a device that reaches pageable memory
+ *   through the host page tables), and copied otherwise.
  *
  *   The pipeline object is host memory owned by the library (freed by _destroy); it also owns
  *   three CUDA streams and six events on the device that is current at _create.  It allocates

@@ -244,6 +244,29 @@ def test_host_pipeline_matches_oracle_over_overlapping_submissions():
     hqz.close()
 
 
+@pytest.mark.parametrize("pinned_outputs", [True, False])
+def test_host_pipeline_output_buffers_of_any_kind(pinned_outputs):
+    """Outputs into pinned buffers (stored by the pipeline's copy-out kernel) and into plain
+    pageable buffers (stored the same way where the device reaches pageable memory through the
+    host page tables, else copied), with odd sizes and offsets: all equal the oracle."""
+    M, K = 333, 1040
+    hqz = hq.HostQuantizer(M, K, torch.bfloat16, 16)
+    x = rand_input(M, K, torch.bfloat16, seed=77).pin_memory()
+    # buffers that start 1 byte into a larger allocation: no 16-byte alignment
+    qa = torch.empty(M * (K // 2) + 1, dtype=torch.uint8, pin_memory=pinned_outputs)
+    sa = torch.empty(M * (K // 16) + 1, dtype=torch.uint8, pin_memory=pinned_outputs)
+    q, s = qa[1:].view(M, K // 2), sa[1:].view(M, K // 16)
+    sg = torch.empty(1, dtype=torch.float32, pin_memory=pinned_outputs)
+    for _ in range(3):
+        hqz.submit(x, q, s, sg)
+    hqz.wait()
+    oq, os_, oamax, osg = oracle.quantize(synth.as_oracle_array(x), 16)
+    assert_bytes_equal("pipeline codes", q.numpy(), oq)
+    assert_bytes_equal("pipeline scales", s.numpy(), os_)
+    assert np.float32(sg.item()) == osg
+    hqz.close()
+
+
 def test_host_quantizer_matches_oracle_on_a_workload():
     w = synth.WORKLOADS["bf16_4096x4096"]
     x_host = synth.generate(w).pin_memory()
