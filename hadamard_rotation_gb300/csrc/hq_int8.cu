@@ -17,7 +17,8 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // INT8 per-token rotate-quant: one CTA of kI8Threads per SM, looping over row groups.
 template <int G, bool BF16, int MODE, bool FULL>
 hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
-  auto kernel = hq::k_rotate_quant_int8<G, BF16, MODE, FULL>;
+  // G = 16 is bound by memory: fixed warp places (L = 1); G = 64, 256: round robin.
+  auto kernel = hq::k_rotate_quant_int8<G, BF16, MODE, FULL, (G > 16)>;
   const size_t smem = (MODE == hq::kLoadTma) ? static_cast<size_t>(hq::kI8RingBytes) : 0;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -28,7 +29,7 @@ hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
       (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem))) != cudaSuccess)
     return cuda_fail(e);
-  const int64_t row_groups = (p.M + p.rows_per_iter - 1) / p.rows_per_iter;
+  const int64_t row_groups = (p.M + p.rows_per_block - 1) / p.rows_per_block;
   const unsigned grid = static_cast<unsigned>(row_groups < sms ? row_groups : sms);
   kernel<<<grid, hq::kI8Threads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();
@@ -95,7 +96,20 @@ hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t
   p.M = M;
   p.K = K;
   p.tiles_per_row = static_cast<int>((K + hq::kI8TileElems - 1) / hq::kI8TileElems);
-  p.rows_per_iter = hq::kI8Warps / p.tiles_per_row;
+  int a = p.tiles_per_row, b = hq::kI8Warps;  // lcm(T, 16) = T * 16 / gcd(T, 16)
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  const int lcm = p.tiles_per_row / a * hq::kI8Warps;
+  if (group == 16) {  // memory-bound: whole rows, one tile per warp (see hq_int8.cuh)
+    p.rows_per_block = hq::kI8Warps / p.tiles_per_row;
+    p.tiles_per_warp = 1;
+  } else {
+    p.rows_per_block = lcm / p.tiles_per_row;
+    p.tiles_per_warp = lcm / hq::kI8Warps;
+  }
   p.q = q;
   p.scales = scales;
   const bool bf16 = dtype == HQ_BF16;

@@ -12,8 +12,13 @@
 // S = (v0 + v1) + (v2 + v3) (H4 = J - 2P, P the exchange matrix).
 //
 // Work decomposition.  A CTA of 16 warps handles whole rows: a row of K channels
-// is T = ceil(K / 2048) warp tiles (K <= 32768), the CTA takes R = 16 / T rows at
-// a time, and warp w handles tile (w mod T) of row (w / T).  Within a tile the
+// is T = ceil(K / 2048) warp tiles (K <= 32768).  The CTA takes rows in blocks of
+// B rows, B T tiles numbered row by row, and warp w handles the tiles w, w + 16,
+// ..., L of them.  For G = 64 and 256, which are bound by instruction issue,
+// B = lcm(T, 16) / T and L = lcm(T, 16) / 16, so all 16 warps have work whatever T
+// is (T = 14: 8 rows, 7 tiles per warp).  For G = 16, bound by memory, B =
+// floor(16 / T) and L = 1: whole rows per CTA step, some warps idle when T does not
+// divide 16 (finer row blocks balance the grid better).  Within a tile the
 // lane holds 4 blocks of 16 channels (G = 16: blocks 32j + lane; G = 64, 256: the
 // 4 lanes of a quad hold 16 consecutive blocks, lane % 4 being the block's digit
 // 2, in the lane-dependent slot order of i8_d3).  Every value stays in registers
@@ -47,8 +52,9 @@ struct I8Params {
   int64_t ldx_bytes;
   int64_t M;
   int64_t K;
-  int tiles_per_row;  // T
-  int rows_per_iter;  // R
+  int tiles_per_row;   // T
+  int rows_per_block;  // B = lcm(T, 16) / T
+  int tiles_per_warp;  // L = lcm(T, 16) / 16 (per block)
   int8_t* q;          // [M, K]
   float* scales;      // [M]
 };
@@ -255,33 +261,32 @@ __device__ __forceinline__ float warp_max_nonneg(float v) {
 // FULL: every warp tile of a row is complete (K a multiple of the tile), so no
 // block needs a bounds check.
 //
-// Software pipeline.  Step it rotates this warp's tile of iteration it, publishes
-// its amax and parks the rotated values in TMEM (slot it % 2); then it waits for
-// the row of iteration it - 1 to be complete, takes that tile back from TMEM and
-// quantizes it.  A row's T warps meet on an mbarrier (T arrivals), not a CTA
-// barrier, so while one warp waits the others rotate.  Tile maxima and row
-// barriers rotate over 4 buffers: a warp reuses buffer b at iteration i + 4 only
-// after the row of iteration i + 2 is complete, that is after every warp of the row
-// has passed iteration i + 2 and so has read buffer b (it reads it at i + 1).
-template <int G, bool BF16, int MODE, bool FULL>
+// Software pipeline.  Step i rotates this warp's tile i, publishes its amax and
+// parks the rotated values in TMEM (slot i % 2); then it waits for the row of tile
+// i - 1 to be complete, takes that tile back from TMEM and quantizes it.  A row's
+// T tiles meet on an mbarrier (T arrivals), not a CTA barrier, so while one warp
+// waits the others rotate.  Row barriers and tile maxima come in 4 sets, one per
+// row block modulo 4.  A random-interleaving model of this protocol (parity-only
+// waits, as the hardware checks them) finds no deadlock, no set reused before every
+// warp has read it, and no barrier two phases ahead of a waiter, for every T from 1
+// to 16; with 2 or 3 sets it fails.
+// RR: tiles dealt round robin over the warps (L >= 1); otherwise L = 1 and each warp
+// has a fixed place in the row block.
+template <int G, bool BF16, int MODE, bool FULL, bool RR>
 __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p) {
   constexpr int es = BF16 ? 2 : 4;
   constexpr int kTileBytes = kI8TileElems * es;
-  constexpr int kBufs = 4;
+  constexpr int kSets = 4;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
-  const int R = p.rows_per_iter;
-  const int row_local = wid / T;
-  const int chunk = wid % T;
-  const bool has_role = row_local < R;
-  const int64_t chunk0 = static_cast<int64_t>(chunk) * kI8TileElems;
-  const int64_t nvalid =
-      FULL ? kI8TileElems : (has_role ? (p.K - chunk0 < kI8TileElems ? p.K - chunk0 : kI8TileElems) : 0);
-  auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < nvalid; };
+  const int B = p.rows_per_block;
+  const int L = RR ? p.tiles_per_warp : 1;
 
-  __shared__ float tile_max[kBufs][kI8Warps];
-  __shared__ __align__(8) uint64_t row_bar[kBufs][kI8Warps];  // [buffer][row_local], T arrivals
+  // Row barriers and tile maxima come in 4 sets, one per block modulo 4: a warp
+  // reuses a set only after every warp has read it (see the pipeline note above).
+  __shared__ float tile_max[kSets][kI8Warps][kI8Warps];      // [set][row in block][tile]
+  __shared__ __align__(8) uint64_t row_bar[kSets][kI8Warps];  // [set][row in block], T arrivals
   __shared__ uint32_t tmem_base_slot;
   __shared__ volatile int cta_broken;  // a wait ran out somewhere in the CTA: everyone stops
   extern __shared__ __align__(1024) uint8_t hq_smem[];
@@ -291,8 +296,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   const uint64_t policy = l2_stream_policy();
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kBufs; ++b)
-      for (int r = 0; r < R; ++r) mbar_init(smem_addr(&row_bar[b][r]), static_cast<uint32_t>(T));
+    for (int st = 0; st < kSets; ++st)
+      for (int b = 0; b < B; ++b) mbar_init(smem_addr(&row_bar[st][b]), static_cast<uint32_t>(T));
     cta_broken = 0;
     fence_mbar_init();
   }
@@ -303,30 +308,76 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   const uint32_t tmem_warp = tmem_base_slot + ((32u * static_cast<uint32_t>(wid & 3)) << 16) +
                              128u * static_cast<uint32_t>(wid >> 2);
 
-  auto row_of = [&](int64_t it) -> int64_t {
-    return (static_cast<int64_t>(blockIdx.x) + it * gridDim.x) * R + row_local;
+  // Tile i of this warp: block q = i / L, tile g = wid + 16 (i % L) of the block, row
+  // b = g / T of the block, chunk g % T of the row.  Cursors walk i with (q, k = i % L)
+  // carried along; g / T is (g * ceil(2^16 / T)) >> 16, exact for g < 256 and T <= 16.
+  struct TileRef {
+    int64_t row;
+    int set, parity, b, chunk;
+    int64_t nvalid;  // channels of the chunk inside the row
   };
-  auto issue = [&](int64_t it) {  // TMA copy of this warp's tile of iteration it
-    const int64_t r = row_of(it);
-    tma_load(ring_s + static_cast<int>(it % kI8Stages) * kTileBytes,
-             p.x + r * p.ldx_bytes + chunk0 * es, static_cast<uint32_t>(nvalid * es),
-             bar0 + static_cast<int>(it % kI8Stages) * 8, policy);
+  struct Cursor {
+    int64_t i, q;
+    int k;
   };
-  auto mine = [&](int64_t it) { return has_role && row_of(it) < p.M; };
+  const uint32_t inv_T = (65536u + static_cast<uint32_t>(T) - 1u) / static_cast<uint32_t>(T);
+  auto advance = [&](Cursor& c) {
+    ++c.i;
+    if (++c.k == L) {
+      c.k = 0;
+      ++c.q;
+    }
+  };
+  // Without round robin (L = 1) the warp's tile of every block is the same.
+  const int b1 = static_cast<int>((static_cast<uint32_t>(wid) * inv_T) >> 16);
+  const int c1 = wid - b1 * T;
+  auto tile = [&](const Cursor& c) {
+    TileRef r;
+    if constexpr (!RR) {
+      r.b = b1;
+      r.chunk = c1;
+    } else {
+      const uint32_t g = static_cast<uint32_t>(wid + 16 * c.k);
+      r.b = static_cast<int>((g * inv_T) >> 16);
+      r.chunk = static_cast<int>(g) - r.b * T;
+    }
+    r.row = (static_cast<int64_t>(blockIdx.x) + c.q * gridDim.x) * B + r.b;
+    r.set = static_cast<int>(c.q & (kSets - 1));
+    r.parity = static_cast<int>((c.q >> 2) & 1);
+    const int64_t c0 = static_cast<int64_t>(r.chunk) * kI8TileElems;
+    r.nvalid = FULL ? kI8TileElems : (p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems);
+    return r;
+  };
+  const int64_t row_blocks = (p.M + B - 1) / B;
+  int64_t n_blocks = 0;  // row blocks of this CTA
+  if (blockIdx.x < row_blocks) n_blocks = (row_blocks - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  // With L = 1 and B T < 16 (one tile per warp and row block) the warps past B T
+  // have no tiles; otherwise B T = 16 L and every warp has L tiles per block.
+  const int64_t n_it = (wid < B * T) ? n_blocks * L : 0;  // tiles of this warp
 
   bool broken = false;   // stop touching memory and waiting
-  int64_t issued = 0;    // this warp's iterations handed to TMA: 0 .. issued-1
+  int64_t issued = 0;    // this warp's tiles 0 .. issued-1 handed to TMA (rows only increase
+                         // with i, so once a tile lies past M every later one does too)
+  Cursor ci = {0, 0, 0};  // the next tile to hand to TMA
+  auto issue_ahead = [&](int64_t upto) {
+    for (; ci.i < upto && ci.i < n_it; advance(ci)) {
+      const TileRef r = tile(ci);
+      if (r.row >= p.M) break;
+      if (lane == 0)
+        tma_load(ring_s + static_cast<int>(ci.i % kI8Stages) * kTileBytes,
+                 p.x + r.row * p.ldx_bytes + static_cast<int64_t>(r.chunk) * kI8TileElems * es,
+                 static_cast<uint32_t>(r.nvalid * es), bar0 + static_cast<int>(ci.i % kI8Stages) * 8,
+                 policy);
+      issued = ci.i + 1;
+    }
+  };
   if constexpr (MODE == kLoadTma) {
     if (lane == 0) {
-      for (int s = 0; s < kI8Stages; ++s) mbar_init(bar0 + s * 8, 1);
+      for (int st = 0; st < kI8Stages; ++st) mbar_init(bar0 + st * 8, 1);
       fence_mbar_init();
     }
     __syncwarp();
-    for (int s = 0; s < kI8Stages; ++s) {
-      if (!mine(s)) break;  // mine() is monotone in the iteration
-      if (lane == 0) issue(s);
-      issued = s + 1;
-    }
+    issue_ahead(kI8Stages);
   }
   auto fail = [&](int64_t from) {  // record the fault, drain this warp's copies, stop
     if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
@@ -337,13 +388,11 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
     broken = true;
   };
 
-  const int64_t first_rows = static_cast<int64_t>(blockIdx.x) * R;
-  int64_t n_it = 0;  // iterations of this CTA
-  if (first_rows < p.M) n_it = (p.M - first_rows + static_cast<int64_t>(gridDim.x) * R - 1) /
-                               (static_cast<int64_t>(gridDim.x) * R);
-  int64_t drained_from = 0;  // first iteration whose copy may still be in flight
+  int64_t drained_from = 0;  // first tile whose copy may still be in flight
   constexpr float kSign = (G == 64) ? -1.0f : 1.0f;  // the registers hold kSign * y
-  for (int64_t it = 0; has_role && it <= n_it; ++it) {
+  Cursor ca = {0, 0, 0};  // tile it (rotate)
+  Cursor cb = {0, 0, 0};  // tile it - 1 (quantize)
+  for (int64_t it = 0; it <= n_it; ++it) {
     if (!broken && cta_broken) {
       fail(drained_from);
       break;
@@ -351,8 +400,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
     if (broken) break;
     // ---- A: rotate tile it, publish its amax, park it in TMEM ----
     if (it < n_it) {
-      const bool active = mine(it);
-      const int buf = static_cast<int>(it % kBufs);
+      const TileRef r = tile(ca);
+      advance(ca);
+      const bool active = r.row < p.M;
+      auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < r.nvalid; };
       Lane4 t;
       float amax = 0.0f;
       if (active) {
@@ -380,15 +431,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
           }
           __syncwarp();
           drained_from = it + 1;
-          if (mine(it + kI8Stages)) {
-            if (lane == 0) {
-              fence_proxy_async_smem();
-              issue(it + kI8Stages);
-            }
-            issued = it + kI8Stages + 1;
-          }
+          if (lane == 0) fence_proxy_async_smem();
+          issue_ahead(it + 1 + kI8Stages);
         } else {
-          const uint8_t* rowp = p.x + row_of(it) * p.ldx_bytes + chunk0 * es;
+          const uint8_t* rowp = p.x + r.row * p.ldx_bytes + static_cast<int64_t>(r.chunk) * kI8TileElems * es;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t bl = i8_in_block<G>(lane, j);
@@ -409,36 +455,35 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
           amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
         uint32_t v[64];
         lane4_to_words(t, v);
-        const uint32_t ta = tmem_warp + 64u * static_cast<uint32_t>(it & 1);
-        tmem_st64(ta, v);
+        tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(it & 1), v);
       }
       amax = warp_max_nonneg(amax);
       if (lane == 0) {
-        tile_max[buf][wid] = amax;
-        mbar_arrive(smem_addr(&row_bar[buf][row_local]));
+        tile_max[r.set][r.b][r.chunk] = amax;
+        mbar_arrive(smem_addr(&row_bar[r.set][r.b]));
       }
     }
     // ---- B: quantize tile it - 1 once its row is complete ----
     if (it >= 1) {
       const int64_t jt = it - 1;
-      const int buf = static_cast<int>(jt % kBufs);
-      const bool ok = mbar_wait(smem_addr(&row_bar[buf][row_local]), static_cast<uint32_t>((jt / kBufs) & 1));
+      const TileRef r = tile(cb);
+      advance(cb);
+      auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < r.nvalid; };
+      const bool ok = mbar_wait(smem_addr(&row_bar[r.set][r.b]), static_cast<uint32_t>(r.parity));
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         fail(drained_from);
         break;
       }
-      if (mine(jt)) {
-        const int64_t r = row_of(jt);
+      if (r.row < p.M) {
         // T <= 16: each half-warp reads the row's T tile maxima.
         const int c = lane & 15;
-        const float row_amax = warp_max_nonneg(c < T ? tile_max[buf][row_local * T + c] : 0.0f);
+        const float row_amax = warp_max_nonneg(c < T ? tile_max[r.set][r.b][c] : 0.0f);
         const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
         const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
-        if (chunk == 0 && lane == 0) p.scales[r] = scale;
+        if (r.chunk == 0 && lane == 0) p.scales[r.row] = scale;
         uint32_t v[64];
         tmem_wait_st();
-        const uint32_t ta = tmem_warp + 64u * static_cast<uint32_t>(jt & 1);
-        tmem_ld64(ta, v);
+        tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(jt & 1), v);
         tmem_wait_ld();
         Lane4 t;
         words_to_lane4(v, t);
@@ -451,7 +496,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
         // unrounded product differs where RN(y * inv) is exactly k + 1/2.
         const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
         const float2 one2 = make_float2(1.0f, 1.0f);
-        int8_t* qrow = p.q + r * p.K + chunk0;
+        int8_t* qrow = p.q + r.row * p.K + static_cast<int64_t>(r.chunk) * kI8TileElems;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           uint32_t bx[16], by[16];
