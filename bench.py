@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--group", type=int, default=None, help="rotation group (default: the workload's first)")
     ap.add_argument("--e2e-steps", type=int, default=None, help="steps of the host-buffer run (default: min(steps, 200))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="only the first ROWS rows of the workload (same K, distribution and "
+                         "seed): small cases of the same row shape for profiling; not a metric line")
     return ap.parse_args()
 
 
@@ -473,6 +476,14 @@ def main():
     from hadamard_rotation_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
+    if args.rows is not None:
+        if not 0 < args.rows <= w.M:
+            raise SystemExit(f"--rows must be in 1..{w.M}")
+        import dataclasses
+
+        # the first rows of the named tensor: row chunks are drawn from their own seeded streams
+        w = dataclasses.replace(w, name=f"{w.name}_rows{args.rows}", M=args.rows,
+                                zero_rows=min(w.zero_rows, args.rows))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
