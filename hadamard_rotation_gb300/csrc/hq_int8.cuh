@@ -21,10 +21,10 @@
 // divide 16 (finer row blocks balance the grid better).  Within a tile the
 // lane holds 4 blocks of 16 channels (G = 16: blocks 32j + lane; G = 64, 256: the
 // 4 lanes of a quad hold 16 consecutive blocks, lane % 4 being the block's digit
-// 2, in the lane-dependent slot order of i8_d3).  Every value stays in registers
-// from load to store: the row's amax is reduced through shared memory between
-// the two halves, so x is read once.  bf16 rows stream through the per-warp TMA
-// ring.
+// 2, in the lane-dependent slot order of i8_d3).  The rotated values never go to
+// global memory: between the rotation and the quantization, which needs the whole
+// row's amax, they wait in tensor memory (the pipeline note at the kernel), so x
+// is read once.  bf16 rows stream through the per-warp TMA ring.
 //
 // The 4-point steps run on negated values: new_k = fma(S, -1/2, a_(3-k)) =
 // RN(a_(3-k) - S/2) = -out_k, one FFMA2 per two values and no negation; the sign
