@@ -463,11 +463,11 @@ enum LoadMode : int {
 // contiguous as a plain tile) go to one warp in order.
 // Units run over column chunks fastest, then k, then row tiles rt = 0 ..
 // ceil(M / 128) - 1; rows past M give empty tiles.
-struct RgTile {
-  uint64_t row;     // row of the tile (may be >= M)
-  uint64_t rt;      // row tile (128 rows)
+struct RgTile {      // 32-bit fields: the host keeps units below 2^29, so rows below 2^32
+  uint32_t row;     // row of the tile (may be >= M)
+  uint32_t rt;      // row tile (128 rows)
   uint32_t k;       // row pair within a 32-row band
-  uint64_t c0;      // first column (block) of the chunk
+  uint32_t c0;      // first column (block) of the chunk
   uint32_t ncols;   // blocks of the chunk inside the row: 1..128
   int rs;           // tile within the unit
   bool present;     // row < M
@@ -587,9 +587,9 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
     g.k = s.rg & 15u;
     g.rs = rs;
     g.row = g.rt * 128u + 2u * g.k + static_cast<uint32_t>(rs & 1) + 32u * static_cast<uint32_t>(rs >> 1);
-    g.c0 = static_cast<uint64_t>(s.cc) * kTileBlocks;
-    const uint64_t left = p.nbr - g.c0;
-    g.ncols = static_cast<uint32_t>(left < kTileBlocks ? left : kTileBlocks);
+    g.c0 = s.cc * static_cast<uint32_t>(kTileBlocks);
+    const uint32_t left = p.nbr - g.c0;
+    g.ncols = left < kTileBlocks ? left : kTileBlocks;
     g.present = g.row < p.rows;
     return g;
   };
@@ -601,7 +601,8 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
   const uint64_t policy = l2_stream_policy();
   auto issue = [&](const RgTile& g, int slot) {
     if (g.present)
-      tma_load(ring_s + slot * R::kTileBytes, p.x + g.row * p.ldx_bytes + g.c0 * 16u * R::kElemBytes,
+      tma_load(ring_s + slot * R::kTileBytes,
+               p.x + static_cast<uint64_t>(g.row) * p.ldx_bytes + g.c0 * 16u * R::kElemBytes,
                g.ncols * 16u * R::kElemBytes, bar0 + slot * 8, policy);
     else
       mbar_expect_tx(bar0 + slot * 8, 0);  // an empty tile: the phase completes at once
@@ -1035,13 +1036,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
     } else {
       // Row-group unit tile (base = tile index): one row segment, as a flat tile.
       const RgTile& g = tile;
+      uint8_t* q_tile = p.q + (static_cast<uint64_t>(g.row) * p.nbr + g.c0) * 8u;  // codes of block c0
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (!valid[j]) continue;
-        const uint64_t b = g.row * p.nbr + g.c0 + lane_block<G>(lane, j);
         const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
         const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;
-        __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep, w[j][1] & keep));
+        __stcs(reinterpret_cast<uint2*>(q_tile + lane_block<G>(lane, j) * 8u),
+               make_uint2(w[j][0] & keep, w[j][1] & keep));
       }
       // Scales.  Row r, column c of the scale matrix sits at 512 * (row tile *
       // swz_col_tiles + c / 4) + (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4, so the
@@ -1073,8 +1075,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
       if (g.rs == 7) {
         const uint64_t ct = g.c0 / 4 + lane;
         if (ct < p.swz_col_tiles)
-          st_v8(p.s + (g.rt * p.swz_col_tiles + ct) * 512u + 32u * g.k, swz_acc[0], swz_acc[2], swz_acc[4],
-                swz_acc[6], swz_acc[1], swz_acc[3], swz_acc[5], swz_acc[7]);
+          st_v8(p.s + (static_cast<uint64_t>(g.rt) * p.swz_col_tiles + ct) * 512u + 32u * g.k, swz_acc[0],
+                swz_acc[2], swz_acc[4], swz_acc[6], swz_acc[1], swz_acc[3], swz_acc[5], swz_acc[7]);
       }
     }
   };
