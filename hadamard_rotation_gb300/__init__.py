@@ -8,13 +8,18 @@ from .api import (  # noqa: F401
     HostQuantizer,
     hq_dequant_mxfp4,
     hq_dequant_nvfp4,
+    hq_quantize_nvfp4_host_noalloc,
+    hq_read_fault,
     hq_rot_amax,
     hq_rotate_quant_int8,
     hq_rotate_quant_mxfp4,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
     hq_rotate_quant_nvfp4_swizzled,
+    hq_selftest_bounded_wait,
+    hq_status_string,
     hq_swizzled_scales_bytes,
+    hq_version,
     quantize_nvfp4,
 )
 
@@ -23,13 +28,18 @@ __all__ = [
     "HostQuantizer",
     "hq_dequant_mxfp4",
     "hq_dequant_nvfp4",
+    "hq_quantize_nvfp4_host_noalloc",
+    "hq_read_fault",
     "hq_rot_amax",
     "hq_rotate_quant_int8",
     "hq_rotate_quant_mxfp4",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
     "hq_rotate_quant_nvfp4_swizzled",
+    "hq_selftest_bounded_wait",
+    "hq_status_string",
     "hq_swizzled_scales_bytes",
+    "hq_version",
     "lib_path",
     "load",
     "quantize_nvfp4",

@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
         lib.hq_host_pipeline_destroy.restype = i32
         lib.hq_read_fault.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.hq_read_fault.restype = i32
+        lib.hq_quantize_nvfp4_host_noalloc.argtypes = [p, i32, i64, i64, i32, p, p, p, p]
+        lib.hq_quantize_nvfp4_host_noalloc.restype = i32
         lib.hq_selftest_bounded_wait.argtypes = [i32, p]
         lib.hq_selftest_bounded_wait.restype = i32
         lib.hq_version.argtypes = []

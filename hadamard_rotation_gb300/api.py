@@ -192,6 +192,57 @@ def quantize_nvfp4(x: torch.Tensor, group: int, stream: torch.cuda.Stream | None
     return q, s, sg, amax
 
 
+def hq_quantize_nvfp4_host_noalloc(x_host: torch.Tensor, group: int,
+                                   q_host: torch.Tensor | None = None,
+                                   s_host: torch.Tensor | None = None,
+                                   sg_host: torch.Tensor | None = None,
+                                   stream: torch.cuda.Stream | None = None):
+    """One host tensor through both passes with no device allocation (the library's fixed
+    staging array; see include/hq.h for its size limit and sharing rules).  Outputs default to
+    new pinned host tensors; they are complete once ``stream`` (default: current) is
+    synchronised.  Returns (q_host, s_host, sg_host)."""
+    if not isinstance(x_host, torch.Tensor) or x_host.is_cuda or x_host.dim() != 2 \
+            or x_host.dtype not in _DTYPES or not x_host.is_contiguous():
+        raise ValueError("x_host must be a contiguous 2-D float32 or bfloat16 host tensor")
+    M, K = x_host.shape
+    outs = []
+    for t, shape, dt, name in ((q_host, (M, K // 2), torch.uint8, "q_host"),
+                               (s_host, (M, K // 16), torch.uint8, "s_host"),
+                               (sg_host, (1,), torch.float32, "sg_host")):
+        if t is None:
+            t = torch.empty(shape, dtype=dt, pin_memory=True)
+        elif t.is_cuda or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host {dt} tensor {shape}")
+        outs.append(t)
+    check(_lib.load().hq_quantize_nvfp4_host_noalloc(
+        _ptr(x_host), _DTYPES[x_host.dtype], M, K, group, _ptr(outs[0]), _ptr(outs[1]),
+        _ptr(outs[2]), _stream_handle(stream)), "hq_quantize_nvfp4_host_noalloc")
+    return tuple(outs)
+
+
+def hq_read_fault(clear: bool = False) -> int:
+    """The device fault word (waits for the device to be idle); bit 0: a kernel's bounded wait
+    for one of its own tile copies ran out.  ``clear`` resets it after reading."""
+    v = ctypes.c_uint(0)
+    check(_lib.load().hq_read_fault(ctypes.byref(v), 1 if clear else 0), "hq_read_fault")
+    return v.value
+
+
+def hq_selftest_bounded_wait(unit: int = 0, stream: torch.cuda.Stream | None = None) -> None:
+    """Enqueue the bounded-wait self-test (one warp waits on a barrier nothing completes, gives
+    up after about a second and records bit 0 of the fault word).  unit 0: the NVFP4 / MXFP4
+    kernels' translation unit, 1: the INT8 kernel's."""
+    check(_lib.load().hq_selftest_bounded_wait(unit, _stream_handle(stream)), "hq_selftest_bounded_wait")
+
+
+def hq_version() -> int:
+    return int(_lib.load().hq_version())
+
+
+def hq_status_string(status: int) -> str:
+    return _lib.load().hq_status_string(status).decode()
+
+
 class HostQuantizer:
     """Quantize tensors that live in pinned host memory, through the library's host pipeline.
 

@@ -229,3 +229,17 @@ def test_swizzled_argument_checks_and_size(lib):
 
 def test_selftest_argument_check(lib):
     assert lib.hq_selftest_bounded_wait(2, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
+
+
+def test_binding_has_every_abi_call_under_the_same_name():
+    """The Python binding mirrors include/hq.h: one function per C entry point, same name.
+    The host pipeline calls are the methods of HostQuantizer; hq_last_cuda_error is carried by
+    HQError."""
+    import hadamard_rotation_gb300 as hq
+
+    wrapped_elsewhere = {"hq_host_pipeline_create", "hq_host_pipeline_destroy", "hq_host_pipeline_submit",
+                         "hq_host_pipeline_wait", "hq_host_pipeline_workspace_bytes", "hq_last_cuda_error"}
+    missing = [n for n in declared_functions() if n not in wrapped_elsewhere and not callable(getattr(hq, n, None))]
+    assert not missing, missing
+    assert hq.hq_version() == 100
+    assert hq.hq_status_string(0).startswith("HQ_OK")

@@ -6,7 +6,6 @@ bit 0 in the device fault word that hq_read_fault returns, and leave the context
 quantization right after it is bit-exact and records no fault.  (The file name sorts last so
 that the fault word it sets, then clears, is not seen by other tests.)
 """
-import ctypes
 import time
 
 import numpy as np
@@ -21,9 +20,7 @@ pytestmark = pytest.mark.gpu
 
 
 def read_fault(clear):
-    v = ctypes.c_uint(0)
-    assert hq.load().hq_read_fault(ctypes.byref(v), 1 if clear else 0) == 0
-    return v.value
+    return hq.hq_read_fault(clear=clear)
 
 
 @pytest.mark.parametrize("unit", [0, 1])  # the NVFP4/MXFP4 kernels' unit, the INT8 kernel's
@@ -32,10 +29,10 @@ def test_bounded_wait_gives_up_and_is_reported(unit):
 
     build.build()
     oracle.build()
-    lib = hq.load()
+    hq.load()
     assert read_fault(clear=True) == 0            # nothing recorded before
     t0 = time.perf_counter()
-    assert lib.hq_selftest_bounded_wait(unit, None) == 0
+    hq.hq_selftest_bounded_wait(unit)
     fault = read_fault(clear=True)                  # synchronises: the wait has ended
     elapsed = time.perf_counter() - t0
     assert fault == 1, fault
