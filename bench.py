@@ -47,7 +47,7 @@ L2_BYTES = 126 * 1024 * 1024
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.88 GB read + 0.49771 GB written
-    ("2a27d6b9985a982a", "bf16_32768x28672", 16): 1.88e9 + 0.49771e9,
+    ("3a2c2589aa759ffa", "bf16_32768x28672", 16): 1.88e9 + 0.49771e9,
 }
 
 
@@ -100,23 +100,32 @@ def throughput_gbs(bytes_per_step_per_rank: int, steps: int, world: int, region_
 
 
 def time_launches(fn, K: int, stream, dev, flush) -> float:
-    """Average milliseconds of one call of fn over K back-to-back calls (CUDA events on the
-    launching stream, 3 untimed calls first; the L2 flush, when given, runs between calls)."""
+    """Average milliseconds of one call of fn over K calls (CUDA events on the launching
+    stream, 3 untimed calls first).  Without a flush the calls run back to back between two
+    events; with one, the L2 flush runs between calls and each call has its own event pair,
+    so the flush is not timed."""
     import torch
 
     for _ in range(3):
         fn()
     torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(K):
+    if flush is None:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / K
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        flush.fill_(1.0)
+        a.record(stream)
         fn()
-        if flush is not None:
-            flush.fill_(1.0)
-    b.record(stream)
+        b.record(stream)
     torch.cuda.synchronize(dev)
-    return a.elapsed_time(b) / K
+    return sum(a.elapsed_time(b) for a, b in ev) / K
 
 
 def load_peaks():
@@ -336,23 +345,17 @@ def run_ours(args, w):
     value = throughput_gbs(step_bytes, K, world, region_ms)
 
     # ---- single-pass mode (delayed amax): one kernel per step, reported beside the step ----
+    # each call quantizes with the amax the previous call reduced (two buffers alternate)
     amax_b = torch.empty(1, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        hq.hq_rotate_quant_nvfp4_delayed(x, group, amax, amax_next=amax_b, q=q, scales=s,
-                                         s_global=sg, stream=stream)
-    torch.cuda.synchronize(dev)
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for i in range(K):
-        src, dst = (amax, amax_b) if i % 2 == 0 else (amax_b, amax)
+    calls = [0]
+
+    def delayed_call():
+        src, dst = (amax, amax_b) if calls[0] % 2 == 0 else (amax_b, amax)
+        calls[0] += 1
         hq.hq_rotate_quant_nvfp4_delayed(x, group, src, amax_next=dst, q=q, scales=s,
                                          s_global=sg, stream=stream)
-        if flush is not None:
-            flush.fill_(1.0)
-    d1.record(stream)
-    torch.cuda.synchronize(dev)
-    single_ms = d0.elapsed_time(d1) / K
+
+    single_ms = time_launches(delayed_call, K, stream, dev, flush)
 
     # ---- pass 2 with the block scales in the swizzled GEMM layout, same tensor ----
     s_sw = torch.empty(hq.hq_swizzled_scales_bytes(w.M, w.K), dtype=torch.uint8, device=dev)
