@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     HostQuantizer,
     hq_dequant_mxfp4,
     hq_dequant_nvfp4,
+    hq_quantize_nvfp4,
     hq_quantize_nvfp4_host_noalloc,
     hq_read_fault,
     hq_rot_amax,
@@ -28,6 +29,7 @@ __all__ = [
     "HostQuantizer",
     "hq_dequant_mxfp4",
     "hq_dequant_nvfp4",
+    "hq_quantize_nvfp4",
     "hq_quantize_nvfp4_host_noalloc",
     "hq_read_fault",
     "hq_rot_amax",

@@ -79,6 +79,48 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     return q, scales, s_global
 
 
+# hq_quantize_nvfp4's workspaces kept by this binding, one per (device, stream).
+_WORKSPACES: dict[tuple[int, int], torch.Tensor] = {}
+HQ_QUANTIZE_WORKSPACE_WORDS = 4
+HQ_QUANTIZE_FUSED_MAX_BYTES = 64 * 1024 * 1024
+
+
+def _workspace(device: torch.device, stream: torch.cuda.Stream | None) -> torch.Tensor:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index if device.index is not None else torch.cuda.current_device(), s.cuda_stream)
+    w = _WORKSPACES.get(key)
+    if w is None:
+        w = torch.zeros(HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=device)
+        _WORKSPACES[key] = w
+    return w
+
+
+def hq_quantize_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor | None = None,
+                      q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                      s_global: torch.Tensor | None = None, fused: bool = True,
+                      workspace: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None):
+    """Both passes in one call: (q, scales, s_global, amax), as hq_rot_amax then
+    hq_rotate_quant_nvfp4.  With ``fused`` (default), an x of contiguous rows and at most
+    HQ_QUANTIZE_FUSED_MAX_BYTES runs as one cooperative kernel; its workspace (int32
+    [HQ_QUANTIZE_WORKSPACE_WORDS], zero before first use) defaults to one this binding keeps
+    per device and stream."""
+    dt, M, K, ldx = _x_args(x)
+    amax = _need(amax, (1,), torch.float32, x.device, "amax")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    if fused:
+        workspace = _workspace(x.device, stream) if workspace is None else _need(
+            workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
+    else:
+        workspace = None
+    check(_lib.load().hq_quantize_nvfp4(_ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q),
+                                        _ptr(scales), _ptr(s_global), _ptr(workspace),
+                                        _stream_handle(stream)), "hq_quantize_nvfp4")
+    return q, scales, s_global, amax
+
+
 def hq_swizzled_scales_bytes(M: int, K: int) -> int:
     """Bytes of the swizzled scale buffer for an [M, K] tensor (128-row x 4-column tiles)."""
     n = _lib.load().hq_swizzled_scales_bytes(M, K)
@@ -186,10 +228,8 @@ def hq_dequant_nvfp4(q: torch.Tensor, scales: torch.Tensor, s_global: torch.Tens
 
 
 def quantize_nvfp4(x: torch.Tensor, group: int, stream: torch.cuda.Stream | None = None):
-    """Both passes: (q, scales, s_global, amax), all on x's device."""
-    amax = hq_rot_amax(x, group, stream=stream)
-    q, s, sg = hq_rotate_quant_nvfp4(x, group, amax, stream=stream)
-    return q, s, sg, amax
+    """Both passes: (q, scales, s_global, amax), all on x's device (hq_quantize_nvfp4)."""
+    return hq_quantize_nvfp4(x, group, stream=stream)
 
 
 def hq_quantize_nvfp4_host_noalloc(x_host: torch.Tensor, group: int,
@@ -222,16 +262,24 @@ def hq_quantize_nvfp4_host_noalloc(x_host: torch.Tensor, group: int,
 
 def hq_read_fault(clear: bool = False) -> int:
     """The device fault word (waits for the device to be idle); bit 0: a kernel's bounded wait
-    for one of its own tile copies ran out.  ``clear`` resets it after reading."""
+    (for one of its own tile copies, or at hq_quantize_nvfp4's grid barrier) ran out.  ``clear``
+    resets it after reading, and zeroes the hq_quantize_nvfp4 workspaces this binding keeps on
+    the current device (a fault can leave one non-zero)."""
     v = ctypes.c_uint(0)
     check(_lib.load().hq_read_fault(ctypes.byref(v), 1 if clear else 0), "hq_read_fault")
+    if clear:
+        dev = torch.cuda.current_device()
+        for (d, _), w in _WORKSPACES.items():
+            if d == dev:
+                w.zero_()
+        torch.cuda.synchronize()
     return v.value
 
 
 def hq_selftest_bounded_wait(unit: int = 0, stream: torch.cuda.Stream | None = None) -> None:
     """Enqueue the bounded-wait self-test (one warp waits on a barrier nothing completes, gives
     up after about a second and records bit 0 of the fault word).  unit 0: the NVFP4 / MXFP4
-    kernels' translation unit, 1: the INT8 kernel's."""
+    kernels' translation unit, 1: the INT8 kernel's, 2: hq_quantize_nvfp4's grid barrier."""
     check(_lib.load().hq_selftest_bounded_wait(unit, _stream_handle(stream)), "hq_selftest_bounded_wait")
 
 

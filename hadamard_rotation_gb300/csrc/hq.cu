@@ -33,6 +33,15 @@ __global__ void k_selftest_bounded_wait() {
   if (!__all_sync(0xFFFFFFFFu, ok) && threadIdx.x == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
 }
 
+// The grid barrier of k_quant_nvfp4_fused with one arrival more than the grid
+// can give: the wait runs out.
+__device__ unsigned g_selftest_count;
+
+__global__ void k_selftest_grid_barrier() {
+  if (threadIdx.x == 0) atomicExch(&g_selftest_count, 0u);
+  grid_barrier(&g_selftest_count, gridDim.x + 1);
+}
+
 }  // namespace hq
 
 namespace {
@@ -231,6 +240,24 @@ hq_status dispatch_quant_swizzled(const hq::Params& p, bool bf16, hq_stream s) {
                 ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, false));
 }
 
+// Both passes in one cooperative launch (k_quant_nvfp4_fused): the dynamic shared
+// memory holds the larger of the two TMA rings.
+template <int G>
+hq_status launch_fused(hq::Params p, bool bf16, hq_stream s) {
+  void (*fn)(hq::Params) = bf16 ? hq::k_quant_nvfp4_fused<G, true> : hq::k_quant_nvfp4_fused<G, false>;
+  const size_t r1 = ring_bytes<HQ_PASS1_STAGES>(hq::kLoadTma, bf16);
+  const size_t r2 = ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, bf16);
+  const size_t smem = r1 > r2 ? r1 : r2;
+  unsigned grid = 0;
+  cudaError_t e = persistent_grid(reinterpret_cast<const void*>(fn), p.n_tiles, smem, &grid);
+  if (e != cudaSuccess) return cuda_fail(e);
+  void* args[] = {&p};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(hq::kThreads),
+                                  args, smem, static_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -277,6 +304,38 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
     case 0: return dispatch_quant<0, false>(p, bf16, strided, stream);
     case 16: return dispatch_quant<16, false>(p, bf16, strided, stream);
     default: return dispatch_quant<256, false>(p, bf16, strided, stream);
+  }
+}
+
+hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                            int group, float* amax, uint8_t* q, uint8_t* scales,
+                            float* s_global, uint32_t* workspace, hq_stream stream) {
+  hq_status st = check_x(x, dtype, M, K, ldx, group);
+  if (st != HQ_OK) return st;
+  if (!amax) return HQ_ERR_NULL;
+  if (!aligned(amax, 4) || (workspace && !aligned(workspace, 4))) return HQ_ERR_ALIGN;
+  const bool fused = workspace && M > 0 && K > 0 && !is_strided(M, K, ldx) &&
+                     M * K * elem_size(dtype) <= HQ_QUANTIZE_FUSED_MAX_BYTES;
+  if (!fused) {
+    st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
+    if (st != HQ_OK) return st;
+    return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
+  }
+  if (!q || !scales) return HQ_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(scales, 4) || (s_global && !aligned(s_global, 4)))
+    return HQ_ERR_ALIGN;
+  hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.q = q;
+  p.s = scales;
+  p.sglobal_out = s_global;
+  p.sync = workspace;
+  p.amax_out = reinterpret_cast<float*>(workspace + 1);
+  p.amax_copy = amax;
+  const bool bf16 = dtype == HQ_BF16;
+  switch (group) {
+    case 0: return launch_fused<0>(p, bf16, stream);
+    case 16: return launch_fused<16>(p, bf16, stream);
+    default: return launch_fused<256>(p, bf16, stream);
   }
 }
 
@@ -475,12 +534,15 @@ hq_status hq_read_fault(unsigned int* fault, int clear) {
 }
 
 hq_status hq_selftest_bounded_wait(int unit, hq_stream stream) {
-  if (unit != 0 && unit != 1) return HQ_ERR_SHAPE;
+  if (unit < 0 || unit > 2) return HQ_ERR_SHAPE;
   if (unit == 1) {
     const cudaError_t e = hq::int8_selftest_bounded_wait(static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? HQ_OK : cuda_fail(e);
   }
-  hq::k_selftest_bounded_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  if (unit == 2)
+    hq::k_selftest_grid_barrier<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  else
+    hq::k_selftest_bounded_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? HQ_OK : cuda_fail(e);
 }

@@ -98,6 +98,9 @@ struct Params {
   uint64_t rows;           // M (row-group tiles)
   uint32_t n_cc;           // row-group tiles: column chunks of 16 blocks per row, ceil(K/256)
   FastDiv div_ncc;         // divider for n_cc
+  // both passes in one launch (k_quant_nvfp4_fused)
+  unsigned* sync;          // [0] CTAs past pass 1, [1] amax bits, [2] CTAs done; 0 on entry and exit
+  float* amax_copy;        // the tensor's amax, written once it is known
   // dequant
   const uint8_t* dq_q;
   const uint8_t* dq_s;
@@ -240,6 +243,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // x is streamed once: its lines are the first to leave L2.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ uint64_t l2_stream_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -476,7 +485,9 @@ struct RgTile {      // 32-bit fields: the host keeps units below 2^29, so rows 
 
 // Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
 // values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
-template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, typename Body>
+// KEEP_L2: read x with an L2 evict-last hint (it is read again soon) instead of
+// evict-first.
+template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool KEEP_L2 = false, typename Body>
 __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -496,7 +507,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
     uint8_t* ring = hq_smem + wid * R::kStages * R::kTileBytes;
     const uint32_t ring_s = smem_addr(ring);
     const uint32_t bar0 = smem_addr(hq_smem + R::kDataBytes) + wid * R::kStages * 8;
-    const uint64_t policy = l2_stream_policy();
+    const uint64_t policy = KEEP_L2 ? l2_keep_policy() : l2_stream_policy();
 
     auto issue = [&](uint64_t seq, int slot) {
       const uint64_t first = seq * kTileBlocks;
@@ -774,13 +785,15 @@ __device__ __forceinline__ float absmax256_order1(Lane4& t, int lane) {
   return m;
 }
 
-template <int G, bool BF16, int MODE, bool WRITE_Y>
-__global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params p) {
+// This thread's max |z| (unscaled butterfly output) over its tiles of x; y is
+// written too when WRITE_Y.
+template <int G, bool BF16, int MODE, bool WRITE_Y, bool KEEP_L2 = false>
+__device__ __forceinline__ float rot_amax_tiles(const Params& p) {
   // Without a rotated output, the 256-group takes slot order 1 and skips the
   // last stage's outputs (absmax256_order1).
   constexpr bool kAbsTrick = G == 256 && !WRITE_Y;
   float zmax = 0.0f;
-  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0>(
+  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, KEEP_L2>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kAbsTrick) {
       zmax = max_nan(zmax, absmax256_order1(t, lane));
@@ -812,9 +825,14 @@ __global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params
       }
     }
   });
+  return zmax;
+}
+
+template <int G, bool BF16, int MODE, bool WRITE_Y>
+__global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params p) {
   // |y| = RN(|z| / sqrt(G)) is monotone in |z|, so max |y| = RN(max |z| / sqrt(G))
   // exactly; the scaling commutes with the max over the CTA.
-  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), p.amax_out);
+  cta_amax_to_global(__fmul_rn(rot_amax_tiles<G, BF16, MODE, WRITE_Y>(p), inv_sqrt_g<G>()), p.amax_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -904,6 +922,41 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
 }
 
 // ---------------------------------------------------------------------------
+// Grid barrier for a cooperative launch (every CTA resident).  Thread 0 of each
+// CTA adds 1 to *count after its earlier global writes and waits, about one
+// second at most, until *count reaches `target` (gridDim.x: all CTAs arrived).
+// Returns false to every thread of the CTA when the wait ran out
+// (kFaultWaitTimeout is recorded).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned* count, unsigned target) {
+  __shared__ int ok_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(count, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(count) < target) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(&g_hq_fault, kFaultWaitTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
+// ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
 // SWZ: write the scales in the swizzled tile layout of block-scaled NVFP4 GEMMs
@@ -913,9 +966,8 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
 // 4 + c.  The tiles of this mode are row groups (RgTile), so that every scale
 // store fills whole 32-byte pieces of that layout, padding included.
 template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
-__global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
+__device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float amax) {
   // s_global = amax / (448 * 6), or 1 if that is 0.
-  const float amax = *p.amax_in;
   float s_global = __fdiv_rn(amax, 2688.0f);
   if (s_global == 0.0f) s_global = 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.sglobal_out) *p.sglobal_out = s_global;
@@ -1085,6 +1137,43 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   else
     for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(p, tile_body);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
+}
+
+template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
+__global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
+  rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ>(p, *p.amax_in);
+}
+
+// Both passes in one cooperative launch, for an x that L2 holds: pass 1 reads x
+// through the TMA ring with an evict-last hint and reduces the amax into
+// p.sync[1]; the CTAs meet at a grid barrier; pass 2 reads x again (from L2, now
+// evict-first) with that amax.  The last CTA to finish zeroes p.sync[0..2] for the
+// next call.  Results are those of k_rot_amax followed by k_rotate_quant_nvfp4.
+template <int G, bool BF16>
+__global__ void __launch_bounds__(kThreads, BF16 ? 2 : 1) k_quant_nvfp4_fused(Params p) {
+  __shared__ float amax_s;
+  unsigned* const arrived = p.sync;
+  unsigned* const amax_bits = p.sync + 1;
+  unsigned* const done = p.sync + 2;
+  const float zmax = rot_amax_tiles<G, BF16, kLoadTma, false, true>(p);
+  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), reinterpret_cast<float*>(amax_bits));
+  const bool ok = grid_barrier(arrived, gridDim.x);
+  if (threadIdx.x == 0) {
+    const float a = __uint_as_float(ld_acquire_gpu(amax_bits));
+    amax_s = a;
+    if (ok && blockIdx.x == 0) *p.amax_copy = a;
+    // Every read of p.sync by this CTA is done: count it out.
+    __threadfence();
+    if (atomicAdd(done, 1u) == gridDim.x - 1) {
+      __threadfence();
+      atomicExch(arrived, 0u);
+      atomicExch(amax_bits, 0u);
+      atomicExch(done, 0u);
+    }
+  }
+  __syncthreads();
+  if (!ok) return;
+  rotate_quant_tiles<G, BF16, kLoadTma, false>(p, amax_s);
 }
 
 // ---------------------------------------------------------------------------

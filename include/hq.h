@@ -109,6 +109,37 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
+/* Tensors of x of at most this many bytes take hq_quantize_nvfp4's one-launch path. */
+#define HQ_QUANTIZE_FUSED_MAX_BYTES (64ll * 1024 * 1024)
+/* Size of hq_quantize_nvfp4's workspace, in 32-bit words. */
+#define HQ_QUANTIZE_WORKSPACE_WORDS 4
+
+/*
+ * hq_quantize_nvfp4 -- both passes in one call: *amax, then codes, scales and s_global exactly as
+ *   hq_rot_amax followed by hq_rotate_quant_nvfp4 on the same stream.
+ *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2: the global scale needs the
+ *    amax of the whole rotated tensor before any block is quantized, hence two passes over x.)
+ *
+ *   When x's rows are back to back, x takes at most HQ_QUANTIZE_FUSED_MAX_BYTES and `workspace`
+ *   is given, the two passes run as one cooperative kernel: the first reads x with an L2
+ *   evict-last hint, all CTAs meet at a grid-wide barrier once the amax is reduced, and the
+ *   second reads x back from L2.  Otherwise the call is hq_rot_amax then hq_rotate_quant_nvfp4.
+ *
+ *   x, dtype, M, K, ldx, group : as for hq_rot_amax.
+ *   amax      : 1 float on the device (written; 0 for an empty tensor).
+ *   q, scales, s_global : as for hq_rotate_quant_nvfp4.
+ *   workspace : NULL (two launches), or HQ_QUANTIZE_WORKSPACE_WORDS uint32 on the device, 4-byte
+ *               aligned, all 0 before its first use (e.g. cudaMemset).  Each call that records
+ *               no fault leaves it 0 again.  Calls that may run at the same time (different
+ *               streams) need different workspaces.
+ *   A grid barrier that waits about a second without all CTAs arriving records bit 0 of the
+ *   fault word (hq_read_fault); those CTAs skip the second pass and the outputs are undefined.
+ */
+HQ_API hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                   int64_t ldx, int group, float* amax, uint8_t* q,
+                                   uint8_t* scales, float* s_global, uint32_t* workspace,
+                                   hq_stream stream);
+
 /*
  * hq_rotate_quant_nvfp4_swizzled -- pass 2 exactly as hq_rotate_quant_nvfp4, with the E4M3 block
  * scales written straight into the tiled layout that block-scaled NVFP4 GEMMs read.
@@ -244,8 +275,9 @@ HQ_API hq_status hq_read_fault(unsigned int* fault, int clear);
  * word and returns; no memory is touched and the context stays usable.  Returns once the launch
  * is enqueued (read the result with hq_read_fault).
  *   unit : 0 runs the wait in the translation unit of the NVFP4 / MXFP4 kernels, 1 in that of
- *          the INT8 kernel (each has its own copy of the fault word; hq_read_fault reads both).
- *          Anything else: HQ_ERR_SHAPE.
+ *          the INT8 kernel (each has its own copy of the fault word; hq_read_fault reads both),
+ *          2 is hq_quantize_nvfp4's grid-barrier wait, in one CTA waiting for one arrival more
+ *          than the grid holds.  Anything else: HQ_ERR_SHAPE.
  */
 HQ_API hq_status hq_selftest_bounded_wait(int unit, hq_stream stream);
 

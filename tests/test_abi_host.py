@@ -228,7 +228,7 @@ def test_swizzled_argument_checks_and_size(lib):
 
 
 def test_selftest_argument_check(lib):
-    assert lib.hq_selftest_bounded_wait(2, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
+    assert lib.hq_selftest_bounded_wait(3, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
 
 
 def test_binding_has_every_abi_call_under_the_same_name():
@@ -243,3 +243,25 @@ def test_binding_has_every_abi_call_under_the_same_name():
     assert not missing, missing
     assert hq.hq_version() == 100
     assert hq.hq_status_string(0).startswith("HQ_OK")
+
+
+def test_quantize_argument_checks(lib):
+    def qz(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, a=FAKE, q=FAKE, s=FAKE, sg=None, ws=FAKE + 256):
+        return lib.hq_quantize_nvfp4(
+            P(x) if x else None, dt, M, K, ldx, G, P(a) if a else None, P(q) if q else None,
+            P(s) if s else None, P(sg) if sg else None, P(ws) if ws else None, None)
+    assert qz(x=0) == 1 and qz(a=0) == 1 and qz(q=0) == 1 and qz(s=0) == 1
+    assert qz(G=32) == 5 and qz(dt=2) == 4 and qz(K=24, ldx=24) == 2 and qz(M=-1) == 2
+    assert qz(a=FAKE + 2) == 3 and qz(ws=FAKE + 2) == 3
+    assert qz(q=FAKE + 8) == 3 and qz(s=FAKE + 2) == 3 and qz(x=FAKE + 8) == 3
+    assert qz(sg=FAKE + 1) == 3
+
+
+def test_binding_constants_match_the_header():
+    from hadamard_rotation_gb300 import api
+
+    text = open(HEADER).read()
+    words = re.search(r"#define HQ_QUANTIZE_WORKSPACE_WORDS (\d+)", text)
+    limit = re.search(r"#define HQ_QUANTIZE_FUSED_MAX_BYTES \((\d+)ll \* 1024 \* 1024\)", text)
+    assert words and int(words.group(1)) == api.HQ_QUANTIZE_WORKSPACE_WORDS
+    assert limit and int(limit.group(1)) * 1024 * 1024 == api.HQ_QUANTIZE_FUSED_MAX_BYTES

@@ -1,0 +1,184 @@
+"""hq_quantize_nvfp4, both passes in one call, against the CPU oracle.
+
+For an x of contiguous rows that fits in L2 the call runs both passes as one cooperative kernel
+with a grid barrier between them; otherwise it is the two launches.  Either way amax, s_global,
+codes and scales must be bit-exact with the oracle, and the workspace must be back to zero after
+every call (the next call relies on it).
+"""
+import numpy as np
+import pytest
+import torch
+
+import hadamard_rotation_gb300 as hq
+import oracle
+from hadamard_rotation_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+LIMIT = hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from hadamard_rotation_gb300 import build
+
+    build.build()
+    oracle.build()
+    hq.load()
+
+
+def f32_bits(a) -> np.ndarray:
+    return np.asarray(a, np.float32).view(np.uint32)
+
+
+def rand_input(M, K, dtype, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32) * np.float32(scale)
+    if K >= 64:
+        cols = rng.choice(K, max(1, K // 64), replace=False)
+        x[:, cols] *= 30.0
+    if M > 3:
+        x[2] = 0.0
+    t = torch.from_numpy(x)
+    return t if dtype == torch.float32 else t.to(dtype)
+
+
+def check(x_host, group, got, label):
+    q, s, sg, amax = (t.cpu().numpy() for t in got)
+    oq, os_, oamax, osg = oracle.quantize(synth.as_oracle_array(x_host), group)
+    assert f32_bits(amax)[0] == f32_bits([oamax])[0], (label, amax, oamax)
+    assert f32_bits(sg)[0] == f32_bits([osg])[0], (label, sg, osg)
+    for name, a, b in (("scales", s, os_), ("codes", q, oq)):
+        if not np.array_equal(a, b):
+            idx = np.argwhere(a != b)[:5]
+            raise AssertionError(f"{label} {name}: {int(np.count_nonzero(a != b))} differ, first {idx.tolist()}")
+
+
+def kernels_launched(fn):
+    """Names of the CUDA kernels `fn` launches (torch's profiler); None if it sees none."""
+    from torch.profiler import ProfilerActivity, profile
+
+    with profile(activities=[ProfilerActivity.CUDA]):  # the first session can miss events
+        torch.ones(1, device="cuda").add_(1)
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    return names or None
+
+
+SHAPES = [(1, 256), (2, 16 * 16), (129, 256), (77, 4096), (1000, 1024), (4099, 512)]
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("group", [0, 16, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fused_matches_oracle(M, K, group, dtype):
+    x_host = rand_input(M, K, dtype, seed=M * 3 + K + group)
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    got = hq.hq_quantize_nvfp4(x_host.cuda(), group, workspace=ws)
+    torch.cuda.synchronize()
+    check(x_host, group, got, f"{M}x{K} {dtype}")
+    assert not ws.any().item(), ws
+
+
+@pytest.mark.parametrize("group", [0, 16, 256])
+def test_named_4096x4096_workload(group):
+    w = synth.WORKLOADS["bf16_4096x4096"]
+    x_host = synth.generate(w)
+    x = x_host.cuda()
+    got = hq.quantize_nvfp4(x, group)
+    torch.cuda.synchronize()
+    check(x_host, group, got, f"bf16 [4096, 4096] group {group}")
+    names = kernels_launched(lambda: hq.quantize_nvfp4(x, group))
+    if names is None:
+        pytest.skip("the profiler sees no CUDA kernels here")
+    assert any("k_quant_nvfp4_fused" in n for n in names), names
+
+
+def test_repeated_calls_reuse_the_workspace():
+    """A large-amax tensor, then a small-amax one, then the first again, with one workspace:
+    each amax is exact, so the accumulator and the barrier count were reset in between."""
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    xs = [rand_input(300, 2048, torch.bfloat16, seed=5, scale=100.0),
+          rand_input(300, 2048, torch.bfloat16, seed=6, scale=0.01),
+          rand_input(300, 2048, torch.bfloat16, seed=5, scale=100.0)]
+    for i, x_host in enumerate(xs):
+        for group in (16, 256):
+            got = hq.hq_quantize_nvfp4(x_host.cuda(), group, workspace=ws)
+            torch.cuda.synchronize()
+            check(x_host, group, got, f"call {i} group {group}")
+            assert not ws.any().item()
+
+
+@pytest.mark.parametrize("rows", [8192, 8193])
+def test_size_limit_both_sides(rows):
+    """bf16 [8192, 4096] is exactly the one-launch limit; one row more takes two launches.
+    Both are exact."""
+    K = 4096
+    x_host = rand_input(rows, K, torch.bfloat16, seed=rows)
+    x = x_host.cuda()
+    assert (rows * K * 2 <= LIMIT) == (rows == 8192)
+    got = hq.quantize_nvfp4(x, 16)
+    torch.cuda.synchronize()
+    check(x_host, 16, got, f"bf16 [{rows}, {K}]")
+    names = kernels_launched(lambda: hq.quantize_nvfp4(x, 16))
+    if names is None:
+        pytest.skip("the profiler sees no CUDA kernels here")
+    fused = any("k_quant_nvfp4_fused" in n for n in names)
+    assert fused == (rows == 8192), names
+
+
+def test_two_launch_modes_agree():
+    """fused=False (no workspace: the two launches) and strided rows (always two launches) give
+    the same bytes as the one-launch path."""
+    x_host = rand_input(640, 3072, torch.bfloat16, seed=17)
+    x = x_host.cuda()
+    a = hq.hq_quantize_nvfp4(x, 16)
+    b = hq.hq_quantize_nvfp4(x, 16, fused=False)
+    big = torch.zeros(640, 3072 + 256, dtype=torch.bfloat16, device="cuda")
+    big[:, :3072] = x
+    c = hq.hq_quantize_nvfp4(big[:, :3072], 16)
+    torch.cuda.synchronize()
+    for other in (b, c):
+        for u, v in zip(a, other):
+            assert torch.equal(u, v)
+    check(x_host, 16, a, "640x3072")
+
+
+def test_zero_empty_and_nonfinite():
+    x = torch.zeros(64, 256, device="cuda")
+    q, s, sg, amax = hq.quantize_nvfp4(x, 16)
+    torch.cuda.synchronize()
+    assert amax.item() == 0.0 and sg.item() == 1.0 and not q.any().item() and not s.any().item()
+    e = torch.empty(0, 64, device="cuda", dtype=torch.bfloat16)
+    q, s, sg, amax = hq.quantize_nvfp4(e, 16)
+    torch.cuda.synchronize()
+    assert amax.item() == 0.0 and q.numel() == 0
+    x = torch.ones(64, 256, device="cuda")
+    x[33, 7] = float("inf")
+    for group in (0, 16, 256):
+        assert torch.isinf(hq.quantize_nvfp4(x, group)[3]).item()
+    x[12, 200] = float("nan")
+    for group in (0, 16, 256):
+        assert torch.isnan(hq.quantize_nvfp4(x, group)[3]).item()
+    assert hq.hq_read_fault() == 0
+
+
+def test_two_streams_at_once():
+    """Calls on two streams, in flight together, each with the workspace the binding keeps for
+    its stream."""
+    xs = [rand_input(2048, 2048, torch.bfloat16, seed=40 + i) for i in range(2)]
+    xd = [x.cuda() for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [None, None]
+    for _ in range(4):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                outs[i] = hq.quantize_nvfp4(xd[i], 16, stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        check(xs[i], 16, outs[i], f"stream {i}")
