@@ -1,16 +1,18 @@
 """Benchmark: fused Hadamard rotation + NVFP4 quantization on GB300.
 
-One step = the whole hot path over one activation tensor already resident in HBM:
-hq_rot_amax (pass 1: rotate, global amax) then hq_rotate_quant_nvfp4 (pass 2: rotate, block
-scales, codes).  The metric is GB/s of algorithmic bytes in + out per step:
+One step = the whole hot path over one activation tensor already resident in HBM, as
+hq_quantize_nvfp4 runs it: pass 1 (rotate, global amax) then pass 2 (rotate, block scales,
+codes).  For an x of more than 64 MiB these are two launches, hq_rot_amax then
+hq_rotate_quant_nvfp4; a smaller x runs both as one cooperative kernel.  The metric is GB/s
+of algorithmic bytes in + out per step:
     bytes = M*K*sizeof(x)  (x read)  +  M*K/2 (codes)  +  M*K/16 (E4M3 scales).
 Default workload: x bf16 [32768, 28672] (1.88 GB, larger than L2, so no flush is needed
 between steps), N(0,1) with 0.5% outlier channels x100, seed 3, rotation group 16.
 
 Also reported on the same JSON line:
-  roofline      pass 2 (the dominant kernel): its algorithmic bytes / its average launch time
-                (CUDA events around every launch in the timed region), against the measured
-                HBM copy bandwidth;
+  roofline      the dominant kernel (pass 2, or the one kernel of a one-launch step): its
+                algorithmic bytes / its average launch time (CUDA events around every launch
+                in the timed region), against the measured HBM copy bandwidth;
   e2e           the same metric through the public API with host buffers: pinned host x ->
                 device, both passes, codes + scales + s_global -> pinned host, every step;
   cpu_baseline  the CPU oracle on a bounded sample of the workload, on this host's cores;
@@ -42,12 +44,14 @@ DEFAULT_WORKLOAD = "bf16_32768x28672"
 METRIC = "rotate+NVFP4-quant GB/s (bytes in+out) and % of GB300 HBM peak"
 L2_BYTES = 126 * 1024 * 1024
 
-# Pass-2 DRAM traffic per launch from a one-pass ncu capture of the bench workload
-# itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
+# DRAM traffic per launch of the dominant kernel from a one-pass ncu capture of the bench
+# workload itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879111 GB read + 0.497604 GB written
     ("0438e4140e61a082", "bf16_32768x28672", 16): 1879111424 + 497603840,
+    # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.609 MB read, nothing written back yet
+    ("0438e4140e61a082", "bf16_4096x4096", 16): 33609472 + 0,
 }
 
 
@@ -298,9 +302,28 @@ def run_ours(args, w):
     if bytes_in + bytes_out < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step():
+    # The step is what hq_quantize_nvfp4 runs: for an x of at most 64 MiB one cooperative
+    # kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two launches
+    # (called here as the two entry points, so that each pass has its own events).
+    fused = bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev) if fused else None
+
+    def pass1():
         hq.hq_rot_amax(x, group, amax=amax, stream=stream)
+
+    def pass2():
         hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
+
+    def one_call():
+        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, workspace=ws,
+                             stream=stream)
+
+    def step():
+        if fused:
+            one_call()
+        else:
+            pass1()
+            pass2()
 
     for _ in range(args.warmup):
         step()
@@ -323,9 +346,12 @@ def run_ours(args, w):
     for i in range(K):
         e0, e1, e2 = ev[i]
         e0.record(stream)
-        hq.hq_rot_amax(x, group, amax=amax, stream=stream)
-        e1.record(stream)
-        hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
+        if fused:
+            one_call()
+        else:
+            pass1()
+            e1.record(stream)
+            pass2()
         e2.record(stream)
         if flush is not None:
             flush.fill_(1.0)
@@ -334,12 +360,18 @@ def run_ours(args, w):
     clocks = sampler.stop()
     if pg:
         pg.barrier()
-    pass1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    pass2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_launch_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    if fused:
+        # the passes on their own, beside the step (the step runs them as one kernel)
+        pass1_ms = [time_launches(pass1, K, stream, dev, flush)]
+        pass2_ms = [time_launches(pass2, K, stream, dev, flush)]
+    else:
+        pass1_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+        pass2_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     region_ms = t_start.elapsed_time(t_end)
     if flush is not None:
         # steps are timed launch to launch; the L2 flush between them is not part of a step
-        region_ms = sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(K))
+        region_ms = sum(step_launch_ms)
     region_ms = max_over_ranks(region_ms)
     step_ms = region_ms / K
     value = throughput_gbs(step_bytes, K, world, region_ms)
@@ -356,19 +388,6 @@ def run_ours(args, w):
                                          s_global=sg, stream=stream)
 
     single_ms = time_launches(delayed_call, K, stream, dev, flush)
-
-    # ---- both passes in one call (hq_quantize_nvfp4): one cooperative kernel when x fits in L2 ----
-    one_call = None
-    if bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES:
-        ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
-        oc_ms = time_launches(lambda: hq.hq_quantize_nvfp4(
-            x, group, amax=amax, q=q, scales=s, s_global=sg, workspace=ws, stream=stream),
-            K, stream, dev, flush)
-        one_call = {"group": group, "ms_per_step": oc_ms, "bytes_per_step": step_bytes,
-                    "gbs": step_bytes / (oc_ms / 1e3) / 1e9,
-                    "note": "hq_quantize_nvfp4: both passes as one cooperative kernel (x re-read "
-                            "from L2 after a grid barrier); the same bytes as the step"}
-        del ws
 
     # ---- pass 2 with the block scales in the swizzled GEMM layout, same tensor ----
     s_sw = torch.empty(hq.hq_swizzled_scales_bytes(w.M, w.K), dtype=torch.uint8, device=dev)
@@ -432,15 +451,16 @@ def run_ours(args, w):
     if mx is not None:
         mx["frac_of_peak"] = mx["gbs"] / peak
     swz["frac_of_peak"] = swz["gbs"] / peak
-    if one_call is not None:
-        one_call["frac_of_peak"] = one_call["gbs"] / peak
-    p2 = sum(pass2) / K
-    p1 = sum(pass1) / K
-    achieved = step_bytes / (p2 / 1e3) / 1e9
+    p2 = sum(pass2_ms) / len(pass2_ms)
+    p1 = sum(pass1_ms) / len(pass1_ms)
+    # the dominant kernel: pass 2, or the one kernel of the step
+    dom_ms = sum(step_launch_ms) / K if fused else p2
+    achieved = step_bytes / (dom_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((src_hash, w.name, group))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "kernel": "k_rotate_quant_nvfp4",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "k_quant_nvfp4_fused" if fused else "k_rotate_quant_nvfp4",
                 "peak_source": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
@@ -454,24 +474,27 @@ def run_ours(args, w):
                           else "L2 flushed between steps (256 MB write, outside the step time)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
+        "step_path": ("hq_quantize_nvfp4: one cooperative kernel (x at most 64 MiB)" if fused
+                      else "hq_quantize_nvfp4: pass 1 then pass 2, two launches"),
         "passes": {"pass1_ms": p1, "pass2_ms": p2,
                    "pass1_gbs_read": bytes_in / (p1 / 1e3) / 1e9,
-                   "pass2_gbs": achieved,
-                   "pass2_frac_of_nominal_8000": achieved / 8000.0},
+                   "pass2_gbs": step_bytes / (p2 / 1e3) / 1e9,
+                   "pass2_frac_of_nominal_8000": step_bytes / (p2 / 1e3) / 1e9 / 8000.0,
+                   "timed": "beside the step, as separate launches" if fused else "inside the step",
+                   "two_launch_step_ms": p1 + p2 if fused else None},
         "single_pass_delayed": {
             "ms_per_step": single_ms, "gbs": step_bytes / (single_ms / 1e3) / 1e9,
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
             "note": "hq_rotate_quant_nvfp4_delayed: quantize with the previous step's amax while "
                     "reducing this one (one read of x); not the metric's two-pass step"},
         "swizzled_scales": swz,
-        "one_call_fused": one_call,
         "mxfp4": mx,
         "int8_per_token": int8,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": hqz.h2d_bytes,
                 "d2h_bytes_per_step": hqz.d2h_bytes, "steps": e2e_steps,
                 "ms_per_step": e2e_ms / e2e_steps, "api": "HostQuantizer (hq_host_pipeline_*)",
                 "timer": "host clock, wait() at the end"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K if fused else 2 * K,
         "clocks": clocks,
         "kernel_source": src_hash,
     }
