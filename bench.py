@@ -215,15 +215,16 @@ def device_uuid(dev) -> str | None:
 
 # --------------------------------------------------------------------- CPU oracle ------
 
-def oracle_sample_run(w, rows: int, reps: int, warm: int = 1):
-    """Time the CPU oracle (both passes) on the first `rows` rows of the workload."""
+def oracle_sample_run(w, rows: int, reps: int, warm: int = 1, threads: int | None = None):
+    """Time the CPU oracle (both passes) on the first `rows` rows of the workload, on `threads`
+    threads (default: every core)."""
     import oracle
     from hadamard_rotation_gb300 import synth
 
     oracle.build()
     x = synth.as_oracle_array(synth.generate(w, rows=slice(0, rows)))
     group = w.groups[0]
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     for _ in range(warm):
         oracle.quantize(x, group, nthreads=threads)
     times = []
@@ -502,10 +503,14 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = min(w.M, max(1, (8192 * 28672) // w.K))
         nbytes, times, threads = oracle_sample_run(w, rows, reps=2)
+        rows1 = max(1, rows // 16)
+        nbytes1, times1, _ = oracle_sample_run(w, rows1, reps=2, threads=1)
         line["cpu_baseline"] = {
             "value": nbytes * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of {w.name} ({rows}x{w.K}), both passes, 2 timed runs"}
+            "sample": f"rows 0..{rows - 1} of {w.name} ({rows}x{w.K}), both passes, 2 timed runs",
+            "single_thread": {"value": nbytes1 * len(times1) / sum(times1) / 1e9, "unit": "GB/s",
+                              "cores": 1, "sample": f"rows 0..{rows1 - 1}, both passes, 2 timed runs"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
