@@ -481,6 +481,7 @@ def run_ours(args, w):
                    "pass1_gbs_read": bytes_in / (p1 / 1e3) / 1e9,
                    "pass2_gbs": step_bytes / (p2 / 1e3) / 1e9,
                    "pass2_frac_of_nominal_8000": step_bytes / (p2 / 1e3) / 1e9 / 8000.0,
+                   "step_gbs_both_reads": (2 * bytes_in + bytes_out) / (step_ms / 1e3) / 1e9,
                    "timed": "beside the step, as separate launches" if fused else "inside the step",
                    "two_launch_step_ms": p1 + p2 if fused else None},
         "single_pass_delayed": {
