@@ -182,3 +182,33 @@ def test_two_streams_at_once():
     torch.cuda.synchronize()
     for i in range(2):
         check(xs[i], 16, outs[i], f"stream {i}")
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_cuda_graph_capture_and_replay(fused):
+    """Both paths captured in a CUDA graph and replayed on new contents of the same input
+    buffer: every replay is exact (the one-launch workspace is zero again after each)."""
+    xs = [rand_input(1024, 2048, torch.bfloat16, seed=70 + i, scale=10.0 ** (i - 1)) for i in range(3)]
+    x = xs[0].cuda()
+    amax = torch.empty(1, device="cuda")
+    q = torch.empty((1024, 1024), dtype=torch.uint8, device="cuda")
+    s = torch.empty((1024, 128), dtype=torch.uint8, device="cuda")
+    sg = torch.empty(1, device="cuda")
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture (grid sizes, attributes)
+        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
+                             workspace=ws if fused else None, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
+                             workspace=ws if fused else None)
+    for i, x_host in enumerate(xs):
+        x.copy_(x_host.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        check(x_host, 16, (q, s, sg, amax), f"replay {i} fused={fused}")
+        assert not ws.any().item()
