@@ -979,6 +979,25 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
+
+  // The fast path's divisor pair for each E4M3 block scale, indexed by its byte
+  // (0..126; the NaN 0x7F never comes out of the satfinite conversion):
+  // d = RN(s_f * sqrt(G)) and nr = -RN(1 / d), with s_f = RN(s_block * s_global).
+  // On the fast path's domain s_f is a normal float for every non-zero s_block, so
+  // s_f == 0 exactly for byte 0, whose entry is d = 1, nr = -1 (its codes are then
+  // masked to 0).  The entries are what each block would compute for its own scale,
+  // computed once per CTA instead of once per block.
+  __shared__ float tab_d[128];
+  __shared__ float tab_nr[128];
+  if (q_fast) {  // the same for every thread of the grid
+    for (int e = threadIdx.x; e < 128; e += kThreads) {
+      const float sfe = __fmul_rn(e4m3x2_to_f32(static_cast<uint32_t>(e)).x, s_global);
+      const float d = (sfe == 0.0f) ? 1.0f : __fmul_rn(sfe, sq);
+      tab_d[e] = d;
+      tab_nr[e] = -__frcp_rn(d);
+    }
+    __syncthreads();
+  }
   float next_amax = 0.0f;  // max of the block amaxes this thread saw (REDUCE_NEXT)
   uint32_t swz_acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // SWZ: scale words of the unit's rows
 
@@ -1013,13 +1032,9 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
       for (int j = 0; j < 4; ++j) v[j] = __fdiv_rn(__fdiv_rn(am[j], 6.0f), s_global);
     }
     uint32_t sb2[2];    // two E4M3 patterns per pair
-    float2 sf[2];       // s_f = s_block * s_global
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      sb2[k] = e4m3x2(v[2 * k], v[2 * k + 1]);
-      const float2 sbf = e4m3x2_to_f32(sb2[k]);
-      sf[k] = mul2(sbf, make_float2(s_global, s_global));
-    }
+    for (int k = 0; k < 2; ++k) sb2[k] = e4m3x2(v[2 * k], v[2 * k + 1]);
+    uint32_t keep[4];   // all ones, or 0 where s_f == 0 (every code of the block is 0)
 
     // Fast path: q = RN(y / s_f) = RN(z / D), D = s_f * sqrt(G), by Markstein's
     // correction with r = RN(1/D) (as div_markstein).  The domain s_f in
@@ -1037,10 +1052,11 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
     if (q_fast) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const float dx = (sf[k].x == 0.0f) ? 1.0f : __fmul_rn(sf[k].x, sq);
-        const float dy = (sf[k].y == 0.0f) ? 1.0f : __fmul_rn(sf[k].y, sq);
-        const float2 nr = make_float2(-__frcp_rn(dx), -__frcp_rn(dy));
-        const float2 d = make_float2(dx, dy);
+        const uint32_t ex = sb2[k] & 0xFFu, ey = (sb2[k] >> 8) & 0xFFu;
+        const float2 nr = make_float2(tab_nr[ex], tab_nr[ey]);
+        const float2 d = make_float2(tab_d[ex], tab_d[ey]);
+        keep[2 * k] = ex ? 0xFFFFFFFFu : 0u;
+        keep[2 * k + 1] = ey ? 0xFFFFFFFFu : 0u;
         float2 qv[16];  // -q
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1059,7 +1075,9 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
       // The definition, literally: y = RN(z / sqrt(G)), q = RN(y / s_f).
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
+        const float sbf = e4m3x2_to_f32(sb2[j >> 1] >> ((j & 1) * 8)).x;
+        const float sfj = __fmul_rn(sbf, s_global);
+        keep[j] = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;
         float qv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1079,9 +1097,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
       for (int j = 0; j < 4; ++j) {
         if (!valid[j]) continue;
         const uint64_t b = base + lane_block<G>(lane, j);
-        const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
-        const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;  // s_f == 0: all codes 0
-        __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep, w[j][1] & keep));
+        __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep[j], w[j][1] & keep[j]));
         const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
         __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
       }
@@ -1092,10 +1108,8 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (!valid[j]) continue;
-        const float sfj = (j & 1) ? sf[j >> 1].y : sf[j >> 1].x;
-        const uint32_t keep = (sfj == 0.0f) ? 0u : 0xFFFFFFFFu;
         __stcs(reinterpret_cast<uint2*>(q_tile + lane_block<G>(lane, j) * 8u),
-               make_uint2(w[j][0] & keep, w[j][1] & keep));
+               make_uint2(w[j][0] & keep[j], w[j][1] & keep[j]));
       }
       // Scales.  Row r, column c of the scale matrix sits at 512 * (row tile *
       // swz_col_tiles + c / 4) + (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4, so the
