@@ -377,12 +377,28 @@ __device__ __forceinline__ void put_block(Lane4& t, int j, const float (&f)[16])
   }
 }
 
-// Register slot of the lane's block j (slot s is P[s >> 1], component s & 1).
-// ORDER 0: slot j.  ORDER 1: the two bits of j swapped, so that blocks j and
-// j ^ 1 sit in P[0] and P[1] (a packed pair) and blocks j and j ^ 2 in .x / .y.
+// The tile block held in register slot s of a lane (slot s is P[s >> 1], component
+// s & 1), and whether its two halves (positions 0..7 and 8..15) sit swapped.
+//   ORDER 0: slot j holds block lane_block<G>(lane, j), halves in place.
+//   ORDER 1 (pass 1 of the 256-group, see absmax256_x): lane l of quad q = l / 4
+//   (the tile's 256-group q), with A = l & 1 and B = (l >> 1) & 1, holds the four
+//   blocks of the group whose block-index bits 0 and 2 are A and B: slot 2k + c holds
+//   block A + 2 (k ^ B) + 4 B + 8 c of the group, its halves swapped when
+//   A ^ (q & 1) = 1.  (Within a warp, each 16-byte shared-memory load then covers
+//   all eight 16-byte columns of a 128-byte row: no bank conflict for bf16.)
+template <int G, int ORDER>
+__device__ __forceinline__ uint32_t slot_block(int lane, int s) {
+  if constexpr (ORDER == 1) {
+    const int A = lane & 1, B = (lane >> 1) & 1, k = s >> 1, c = s & 1;
+    return static_cast<uint32_t>((lane >> 2) * 16 + A + 2 * (k ^ B) + 4 * B + 8 * c);
+  } else {
+    return lane_block<G>(lane, s);
+  }
+}
+
 template <int ORDER>
-__device__ __forceinline__ constexpr int slot_of(int j) {
-  return ORDER == 0 ? j : (((j & 1) << 1) | (j >> 1));
+__device__ __forceinline__ bool halves_swapped(int lane) {
+  return ORDER == 1 && ((lane ^ (lane >> 2)) & 1);
 }
 
 // Direct global loads (strided rows).
@@ -391,22 +407,23 @@ __device__ __forceinline__ void load_tile_global(const Params& p, uint64_t tile_
                                                  bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
   constexpr int n16 = BF16 ? 2 : 4;
+  const int hx = halves_swapped<ORDER>(lane) ? n16 / 2 : 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint64_t b = tile_base + lane_block<G>(lane, j);
-    valid[j] = b < p.nb;
+  for (int s = 0; s < 4; ++s) {
+    const uint64_t b = tile_base + slot_block<G, ORDER>(lane, s);
+    valid[s] = b < p.nb;
     uint4 w4[n16];
-    if (valid[j]) {
+    if (valid[s]) {
       const uint4* src = reinterpret_cast<const uint4*>(block_ptr<STRIDED>(p, b, es));
 #pragma unroll
-      for (int k = 0; k < n16; ++k) w4[k] = __ldg(src + k);
+      for (int k = 0; k < n16; ++k) w4[k] = __ldg(src + (k ^ hx));
     } else {
 #pragma unroll
       for (int k = 0; k < n16; ++k) w4[k] = make_uint4(0u, 0u, 0u, 0u);
     }
     float f[16];
     widen<BF16>(w4, f);
-    put_block(t, slot_of<ORDER>(j), f);
+    put_block(t, s, f);
   }
 }
 
@@ -416,22 +433,23 @@ __device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t til
                                                int lane, bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
   constexpr int n16 = BF16 ? 2 : 4;
+  const int hx = halves_swapped<ORDER>(lane) ? n16 / 2 : 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t bl = lane_block<G>(lane, j);
-    valid[j] = tile_base + bl < nb;
+  for (int s = 0; s < 4; ++s) {
+    const uint32_t bl = slot_block<G, ORDER>(lane, s);
+    valid[s] = tile_base + bl < nb;
     uint4 w4[n16];
-    if (valid[j]) {
+    if (valid[s]) {
       const uint4* src = reinterpret_cast<const uint4*>(slot + bl * 16u * es);
 #pragma unroll
-      for (int k = 0; k < n16; ++k) w4[k] = src[k];
+      for (int k = 0; k < n16; ++k) w4[k] = src[k ^ hx];
     } else {
 #pragma unroll
       for (int k = 0; k < n16; ++k) w4[k] = make_uint4(0u, 0u, 0u, 0u);
     }
     float f[16];
     widen<BF16>(w4, f);
-    put_block(t, slot_of<ORDER>(j), f);
+    put_block(t, s, f);
   }
 }
 
@@ -675,9 +693,10 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
 // The butterfly.  Stage h maps (a, b) = (z[i], z[i+h]) -> (a + b, a - b).
 // Result: the unscaled transform z; the caller applies 1/sqrt(G).
 // ---------------------------------------------------------------------------
+template <int HEND = 16>  // stages h = 1, 2, ... below HEND
 __device__ __forceinline__ void butterfly16(float2 (&v)[16]) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h < HEND; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if ((i & h) == 0) {
@@ -756,24 +775,67 @@ __device__ __forceinline__ constexpr float sqrt_g() {
 // ---------------------------------------------------------------------------
 // Pass 1: rotate + amax.
 // ---------------------------------------------------------------------------
-// max |z| over the lane's 4 blocks of a 256-group tile loaded in slot order 1,
-// without forming the outputs of the last stage.  Stages h = 1..32 as in
-// rotate_tile; h = 64 pairs blocks j, j ^ 1, here P[0] against P[1] (packed);
-// h = 128 pairs blocks j, j ^ 2, here the .x and .y halves, and only feeds the
-// max: for any a, b, max(|RN(a + b)|, |RN(a - b)|) = RN(|a| + |b|) (one of a + b,
-// a - b has magnitude |a| + |b|, the other at most that, and RN is monotone and
-// odd), which holds with a NaN too.  (An a, b = +-inf of opposite signs gives inf
-// where the stage gives a NaN, so non-finite input still surfaces.)
-__device__ __forceinline__ float absmax256_order1(Lane4& t, int lane) {
-  butterfly16(t.P[0]);
-  butterfly16(t.P[1]);
-  cross_lane_stages(t, lane);
+// One butterfly stage on a register pair whose order may be swapped: with
+// s = (1, 1) the pair holds (a, b) = (lower, upper index) and becomes (a + b, a - b);
+// with s = (-1, -1) it holds (b, a) and becomes (a - b, a + b), i.e. the swap is
+// kept.  Each output is one fma with an exact product (+-1 times a value), so it
+// equals RN(a + b) or RN(a - b) bit for bit, signed zeros included.
+__device__ __forceinline__ void stage_pair(float2& r0, float2& r1, float2 s, float2 ns) {
+  const float2 u = fma2(r0, s, r1);
+  const float2 v = fma2(r1, ns, r0);
+  r0 = u;
+  r1 = v;
+}
+
+// max |z| over the lane's blocks of a 256-group tile loaded in slot order 1
+// (slot_block), without forming the outputs of the last stage.  The two stages
+// whose partner values sit in another lane of the quad (h = 16 across lane bit 0,
+// h = 64 across lane bit 1) each move half of the lane's values instead of all of
+// them: the lane keeps the pairs whose other index bit (position bit 3 for h = 16,
+// the register bit of h = 32 for h = 64) equals its own lane bit, sends the other
+// half and receives the partner's values for the pairs it keeps.  Which register of
+// a pair holds the lower index depends on the lane; stage_pair's sign vector
+// follows it.  Stage order and rounding are those of the definition:
+//   h = 1, 2, 4    in each block (positions in place);
+//   h = 8          positions i, i + 8, halves swapped when A ^ (q & 1) = 1;
+//   h = 16         registers i + 8 exchanged with lane ^ 1, lower index in the lane with A = 0;
+//   h = 32         P[0] against P[1], block bit 1 = k ^ B;
+//   h = 64         P[1] exchanged with lane ^ 2, lower index in the lane with B = 0;
+//   h = 128        .x against .y, and only feeds the max: for any a, b,
+//                  max(|RN(a + b)|, |RN(a - b)|) = RN(|a| + |b|) (one of a + b, a - b
+//                  has magnitude |a| + |b|, the other at most that, and RN is monotone
+//                  and odd), which holds with a NaN too.  (An a, b = +-inf of opposite
+//                  signs gives inf where the stage gives a NaN, so non-finite input
+//                  still surfaces.)
+// The lane ends up with outputs of positions other than the ones it loaded, which
+// does not matter for a maximum.
+__device__ __forceinline__ float absmax256_x(Lane4& t, int lane) {
+  const float sA = (lane & 1) ? -1.0f : 1.0f;
+  const float sB = (lane & 2) ? -1.0f : 1.0f;
+  const float sH = ((lane ^ (lane >> 2)) & 1) ? -1.0f : 1.0f;
+  butterfly16<8>(t.P[0]);
+  butterfly16<8>(t.P[1]);
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      stage_pair(t.P[k][i], t.P[k][i + 8], make_float2(sH, sH), make_float2(-sH, -sH));
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      t.P[k][i + 8].x = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i + 8].x, 1);
+      t.P[k][i + 8].y = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][i + 8].y, 1);
+      stage_pair(t.P[k][i], t.P[k][i + 8], make_float2(sA, sA), make_float2(-sA, -sA));
+    }
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    stage_pair(t.P[0][i], t.P[1][i], make_float2(sB, sB), make_float2(-sB, -sB));
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float2 a = t.P[0][i];
-    const float2 b = t.P[1][i];
-    t.P[0][i] = add2(a, b);
-    t.P[1][i] = sub2(a, b);
+    t.P[1][i].x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 2);
+    t.P[1][i].y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 2);
+    stage_pair(t.P[0][i], t.P[1][i], make_float2(sB, sB), make_float2(-sB, -sB));
   }
   float m = 0.0f;
 #pragma unroll
@@ -790,13 +852,13 @@ __device__ __forceinline__ float absmax256_order1(Lane4& t, int lane) {
 template <int G, bool BF16, int MODE, bool WRITE_Y, bool KEEP_L2 = false>
 __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
   // Without a rotated output, the 256-group takes slot order 1 and skips the
-  // last stage's outputs (absmax256_order1).
+  // last stage's outputs (absmax256_x).
   constexpr bool kAbsTrick = G == 256 && !WRITE_Y;
   float zmax = 0.0f;
   for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, KEEP_L2>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kAbsTrick) {
-      zmax = max_nan(zmax, absmax256_order1(t, lane));
+      zmax = max_nan(zmax, absmax256_x(t, lane));
       return;
     }
     rotate_tile<G>(t, lane);
