@@ -386,13 +386,30 @@ __device__ __forceinline__ void put_block(Lane4& t, int j, const float (&f)[16])
 //   block A + 2 (k ^ B) + 4 B + 8 c of the group, its halves swapped when
 //   A ^ (q & 1) = 1.  (Within a warp, each 16-byte shared-memory load then covers
 //   all eight 16-byte columns of a 128-byte row: no bank conflict for bf16.)
+//   ORDER 2 (pass 2 of the 256-group, see rotate_tile_x256): lane l of quad q with
+//   a = l & 1 and b = (l >> 1) & 1 holds, in slot 2k + c, block
+//   (k ^ a) + 2 (a ^ b) + 4 c + 8 b of group q as loaded, and block
+//   a + 2 (a ^ b) + 4 c + 8 (k ^ b) once rotated (out_block).
 template <int G, int ORDER>
 __device__ __forceinline__ uint32_t slot_block(int lane, int s) {
+  const int a = lane & 1, b = (lane >> 1) & 1, k = s >> 1, c = s & 1;
   if constexpr (ORDER == 1) {
-    const int A = lane & 1, B = (lane >> 1) & 1, k = s >> 1, c = s & 1;
-    return static_cast<uint32_t>((lane >> 2) * 16 + A + 2 * (k ^ B) + 4 * B + 8 * c);
+    return static_cast<uint32_t>((lane >> 2) * 16 + a + 2 * (k ^ b) + 4 * b + 8 * c);
+  } else if constexpr (ORDER == 2) {
+    return static_cast<uint32_t>((lane >> 2) * 16 + (k ^ a) + 2 * (a ^ b) + 4 * c + 8 * b);
   } else {
     return lane_block<G>(lane, s);
+  }
+}
+
+// The tile block whose rotated values register slot s holds after the rotation.
+template <int G, int ORDER>
+__device__ __forceinline__ uint32_t out_block(int lane, int s) {
+  if constexpr (ORDER == 2) {
+    const int a = lane & 1, b = (lane >> 1) & 1, k = s >> 1, c = s & 1;
+    return static_cast<uint32_t>((lane >> 2) * 16 + a + 2 * (a ^ b) + 4 * c + 8 * (k ^ b));
+  } else {
+    return slot_block<G, ORDER>(lane, s);
   }
 }
 
@@ -787,6 +804,52 @@ __device__ __forceinline__ void stage_pair(float2& r0, float2& r1, float2 s, flo
   r1 = v;
 }
 
+// The 256-group rotation on the slot order 2 layout (slot_block), for pass 2.  The
+// quad's lane bits stand for block-index bits 1 ^ 3 (lane bit 0, a) and 3 (lane bit
+// 1, b); the register bit k (P[0] / P[1]) starts as block bit 0, the component as
+// block bit 2.  The two stages whose partners sit in another lane each exchange
+// P[1] only, and the register bit k takes the stage's output bit:
+//   h = 1..8   in each block;
+//   h = 16     P[0] against P[1] (block bit 0 = k ^ a);
+//   h = 32     P[1] exchanged with lane ^ 1 (same bit 3, other bit 1); the lane keeps
+//              the pairs of block bit 0 = a, and P[k] becomes block bit 1 = k ^ a ^ b;
+//   h = 64     .x against .y;
+//   h = 128    P[1] exchanged with lane ^ 2 (same bit 0, other bit 3); the lane keeps
+//              the pairs of block bit 1 = a ^ b, and P[k] becomes block bit 3 = k ^ b.
+// Every lane ends with four whole rotated blocks (out_block), each value the
+// definition's, bit for bit (stage_pair).
+__device__ __forceinline__ void rotate_tile_x256(Lane4& t, int lane) {
+  const float sa = (lane & 1) ? -1.0f : 1.0f;
+  const float sb = (lane & 2) ? -1.0f : 1.0f;
+  const float sab = sa * sb;
+  butterfly16(t.P[0]);
+  butterfly16(t.P[1]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    stage_pair(t.P[0][i], t.P[1][i], make_float2(sa, sa), make_float2(-sa, -sa));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    t.P[1][i].x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 1);
+    t.P[1][i].y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 1);
+    stage_pair(t.P[0][i], t.P[1][i], make_float2(sab, sab), make_float2(-sab, -sab));
+  }
+  // h = 64: (x, y) -> (x + y, x - y) = fma((x, y), (1, -1), (y, x)), one rounding each.
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 v = t.P[k][i];
+      t.P[k][i] = fma2(v, make_float2(1.0f, -1.0f), make_float2(v.y, v.x));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    t.P[1][i].x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 2);
+    t.P[1][i].y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 2);
+    stage_pair(t.P[0][i], t.P[1][i], make_float2(sb, sb), make_float2(-sb, -sb));
+  }
+}
+
 // max |z| over the lane's blocks of a 256-group tile loaded in slot order 1
 // (slot_block), without forming the outputs of the last stage.  The two stages
 // whose partner values sit in another lane of the quad (h = 16 across lane bit 0,
@@ -1041,6 +1104,9 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
+  // Register layout of a tile: the 256-group's exchange form (slot_block order 2),
+  // except for row-group tiles (SWZ), whose scale collection assumes lane_block.
+  constexpr int kOrder = (G == 256 && !SWZ) ? 2 : 0;
 
   // The fast path's divisor pair for each E4M3 block scale, indexed by its byte
   // (0..126; the NaN 0x7F never comes out of the satfinite conversion):
@@ -1065,7 +1131,10 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 
   // tile: the tile's first block (flat tiles) or its RgTile (SWZ).
   auto tile_body = [&](const auto& tile, int lane, bool (&valid)[4], Lane4& t) {
-    rotate_tile<G>(t, lane);
+    if constexpr (kOrder == 2)
+      rotate_tile_x256(t, lane);
+    else
+      rotate_tile<G>(t, lane);
 
     // Block amax of z, then of y = z / sqrt(G): RN(max|z| * c) = max RN(|z| * c).
     float am[4];
@@ -1158,7 +1227,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (!valid[j]) continue;
-        const uint64_t b = base + lane_block<G>(lane, j);
+        const uint64_t b = base + out_block<G, kOrder>(lane, j);
         __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0] & keep[j], w[j][1] & keep[j]));
         const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
         __stcs(reinterpret_cast<unsigned char*>(p.s + b), static_cast<unsigned char>(sbyte));
@@ -1211,7 +1280,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
   if constexpr (SWZ)
     for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body);
   else
-    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(p, tile_body);
+    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder>(p, tile_body);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
 }
 
