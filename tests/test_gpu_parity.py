@@ -119,6 +119,28 @@ def test_shapes_and_ragged_tails(M, K, group, dtype):
     check_against_oracle(x, group, want_y=True, label=f"{M}x{K}")
 
 
+@pytest.mark.parametrize("group", [16, 256])
+def test_first_stage_rounding_cancellation_and_signed_zeros(group):
+    """bf16 rows whose adjacent pairs need rounding in the first butterfly stage (exponent gaps
+    of 0 to 40 between x[2m] and x[2m + 1], magnitudes 2^-60 to 2^60), exact cancellations,
+    signed zeros in every combination and subnormal bf16 values.  The kernels may fold the
+    widening of bf16 into that stage; every rotated value must still equal the definition's
+    (y compared bit for bit), and so must the amax, scales and codes."""
+    rng = np.random.default_rng(4242 + group)
+    M, K = 64, 1024
+    a = (rng.standard_normal((M, K // 2)) * np.exp2(rng.integers(-60, 60, (M, K // 2)))).astype(np.float32)
+    b = a * np.exp2(-rng.integers(0, 40, (M, K // 2))) * rng.choice([-1.0, 1.0], (M, K // 2))
+    x = np.empty((M, K), np.float32)
+    x[:, 0::2] = a
+    x[:, 1::2] = b.astype(np.float32)
+    x[0, 1::2] = -x[0, 0::2]                                    # x[2m] + x[2m + 1] = 0
+    x[1, 1::2] = x[1, 0::2]                                     # x[2m] - x[2m + 1] = 0
+    x[2] = np.where(rng.random(K) < 0.5, np.float32(0.0), np.float32(-0.0))
+    x[3] = (rng.integers(-100, 100, K) * 2.0 ** -133).astype(np.float32)  # bf16 subnormals
+    x[4, 0::2] = -0.0
+    check_against_oracle(torch.from_numpy(x).to(torch.bfloat16), group, want_y=True, label="first stage")
+
+
 @pytest.mark.parametrize("group", [0, 16, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_strided_rows(group, dtype):
