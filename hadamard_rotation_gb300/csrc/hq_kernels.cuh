@@ -1372,12 +1372,28 @@ __global__ void __launch_bounds__(kThreads, BF16 ? 2 : 1) k_quant_nvfp4_fused(Pa
 // whose byte is below 8 (amax below 2^-117, where folding could round subnormal
 // values differently) applies the two steps literally.
 // ---------------------------------------------------------------------------
+//
+// The 256-group takes pass 2's exchange layout (rotate_tile_x256, out_block): there the
+// other half of a 32-block sits in lane ^ 3, in the other register of the P[0] / P[1]
+// pair (block bit 0 is lane bit 0 and block bits 1 and 3 are unchanged), and bf16
+// tiles arrive with the first butterfly stage applied.
 template <int G, bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
   constexpr float c = inv_sqrt_g<G>();
-  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES>(
+  constexpr int kOrder = G == 256 ? 2 : 0;
+  constexpr bool kS1 = BF16 && G == 256;
+  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, false, kS1>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
-    rotate_tile<G>(t, lane);
+    if constexpr (kOrder == 2)
+      rotate_tile_x256<kS1>(t, lane);
+    else
+      rotate_tile<G>(t, lane);
+    float am[4];  // block amax of y, slot 2k + h
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      am[2 * k] = __fmul_rn(block_absmax<false>(t.P[k]), c);
+      am[2 * k + 1] = __fmul_rn(block_absmax<true>(t.P[k]), c);
+    }
     uint32_t code[4];
     float inv[4];
     bool literal = false;
@@ -1386,8 +1402,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int j = 2 * k + h;
-        const float am = __fmul_rn(h ? block_absmax<true>(t.P[k]) : block_absmax<false>(t.P[k]), c);
-        const float a32 = max_nan(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        const float other = kOrder == 2 ? __shfl_xor_sync(0xFFFFFFFFu, am[2 * (1 - k) + h], 3)
+                                        : __shfl_xor_sync(0xFFFFFFFFu, am[j], 1);
+        const float a32 = max_nan(am[j], other);
         const int eb = static_cast<int>(__float_as_uint(a32) >> 23);
         code[j] = static_cast<uint32_t>(eb > 2 ? eb - 2 : 0);
         inv[j] = __uint_as_float((254u - code[j]) << 23);  // 2^(127 - code), normal for code <= 253
@@ -1419,9 +1436,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (!valid[j]) continue;
-      const uint64_t b = base + lane_block<G>(lane, j);
+      const uint64_t b = base + out_block<G, kOrder>(lane, j);
       __stcs(reinterpret_cast<uint2*>(p.q + b * 8u), make_uint2(w[j][0], w[j][1]));
-      if ((lane & 1) == 0)  // the even half writes the 32-block's scale byte
+      if ((lane & 1) == 0)  // the even half (block bit 0 = lane bit 0) writes the scale byte
         __stcs(reinterpret_cast<unsigned char*>(p.s + (b >> 1)), static_cast<unsigned char>(code[j]));
     }
   });
