@@ -550,17 +550,21 @@ struct RgTile {      // 32-bit fields: the host keeps units below 2^29, so rows 
 // Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
 // values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
 // KEEP_L2: read x with an L2 evict-last hint (it is read again soon) instead of
-// evict-first.
+// evict-first.  REVERSE: the k-th tile of the sequence is tile n_tiles - 1 - k, so
+// the pass walks x from its end (pass 1 of the two-launch path: pass 2 walks it
+// from the start, and each pass then begins where the previous one ended, with
+// that part of x still in L2).
 template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool KEEP_L2 = false, bool S1 = false,
-          typename Body>
+          bool REVERSE = false, typename Body>
 __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + wid;
   const uint64_t nw = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
+  auto tile_of = [&](uint64_t seq) { return REVERSE ? p.n_tiles - 1 - seq : seq; };
   if constexpr (MODE != kLoadTma) {
     for (uint64_t seq = gw; seq < p.n_tiles; seq += nw) {
-      const uint64_t base = seq * kTileBlocks;
+      const uint64_t base = tile_of(seq) * kTileBlocks;
       bool valid[4];
       Lane4 t;
       load_tile_global<G, BF16, MODE == kLoadStrided, ORDER, S1>(p, base, lane, valid, t);
@@ -575,7 +579,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
     const uint64_t policy = KEEP_L2 ? l2_keep_policy() : l2_stream_policy();
 
     auto issue = [&](uint64_t seq, int slot) {
-      const uint64_t first = seq * kTileBlocks;
+      const uint64_t first = tile_of(seq) * kTileBlocks;
       const uint64_t nblk = (p.nb - first < kTileBlocks) ? (p.nb - first) : kTileBlocks;
       tma_load(ring_s + slot * R::kTileBytes, p.x + first * 16u * R::kElemBytes,
                static_cast<uint32_t>(nblk * 16u * R::kElemBytes), bar0 + slot * 8, policy);
@@ -606,7 +610,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
                     static_cast<uint32_t>((m / R::kStages) & 1));
         return;
       }
-      const uint64_t base = seq * kTileBlocks;
+      const uint64_t base = tile_of(seq) * kTileBlocks;
       bool valid[4];
       Lane4 t;
       load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
@@ -954,7 +958,9 @@ __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
   // (widen_stage1_bf16), with or without a rotated output.
   constexpr bool kS1 = BF16 && G == 256;
   float zmax = 0.0f;
-  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, KEEP_L2, kS1>(
+  // Two launches: walk x from its end (for_each_tile, REVERSE).  One launch (KEEP_L2):
+  // x stays in L2 either way.
+  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, KEEP_L2, kS1, !KEEP_L2>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kAbsTrick) {
       zmax = max_nan(zmax, absmax256_x<kS1>(t, lane));
@@ -1020,9 +1026,12 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
   constexpr int kWords = BF16 ? 8 : 16;  // 32-bit words per 16-element block
   const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;
   uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  // The k-th block of the walk is block nb - 1 - k: x is read from its end, where pass
+  // 2 (which walks it from the start) of the previous call stopped and part of it is
+  // still in L2.
   auto load = [&](uint64_t blk, uint32_t (&w)[kWords]) {
     if (blk < p.nb) {
-      const uint8_t* src = p.x + blk * (16u * (BF16 ? 2u : 4u));
+      const uint8_t* src = p.x + (p.nb - 1 - blk) * (16u * (BF16 ? 2u : 4u));
 #pragma unroll
       for (int k = 0; k < kWords; k += 8) ld_v8_stream(src + 4 * k, w + k);
     } else {
