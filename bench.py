@@ -48,10 +48,10 @@ L2_BYTES = 126 * 1024 * 1024
 # workload itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879270 GB read + 0.497605 GB written
-    ("f388d9cb75159f51", "bf16_32768x28672", 16): 1879270400 + 497604864,
-    # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.610 MB read, nothing written back yet
-    ("f388d9cb75159f51", "bf16_4096x4096", 16): 33609728 + 0,
+    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879111 GB read + 0.497822 GB written
+    ("1e62e4b1b5744728", "bf16_32768x28672", 16): 1879111168 + 497821952,
+    # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.609 MB read, nothing written back yet
+    ("1e62e4b1b5744728", "bf16_4096x4096", 16): 33609472 + 0,
 }
 
 
