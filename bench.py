@@ -303,9 +303,8 @@ def run_ours(args, w):
     if bytes_in + bytes_out < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # The step is what hq_quantize_nvfp4 runs: for an x of at most 64 MiB one cooperative
-    # kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two launches
-    # (called here as the two entry points, so that each pass has its own events).
+    # The step is one hq_quantize_nvfp4 call: for an x of at most 64 MiB one cooperative
+    # kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two launches.
     fused = bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev) if fused else None
 
@@ -315,16 +314,9 @@ def run_ours(args, w):
     def pass2():
         hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
 
-    def one_call():
-        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, workspace=ws,
-                             stream=stream)
-
     def step():
-        if fused:
-            one_call()
-        else:
-            pass1()
-            pass2()
+        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
+                             workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -333,7 +325,12 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # The timed region holds the steps and nothing else: a CUDA event recorded between two
+    # launches costs the GPU about 2 us, so per-pass events would lengthen a step (6 us per
+    # step with three of them).  Without an L2 flush the region is timed by one event pair;
+    # with one, each step has its own pair so that the flush between steps is not timed.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)] if flush is not None else None
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -342,40 +339,47 @@ def run_ours(args, w):
     time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    flush_ms = 0.0
     t_start.record(stream)
     for i in range(K):
-        e0, e1, e2 = ev[i]
-        e0.record(stream)
-        if fused:
-            one_call()
+        if flush is None:
+            step()
         else:
-            pass1()
-            e1.record(stream)
-            pass2()
-        e2.record(stream)
-        if flush is not None:
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
             flush.fill_(1.0)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     if pg:
         pg.barrier()
-    step_launch_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    region_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        # steps are timed launch to launch; the L2 flush between them is not part of a step
+        region_ms = sum(a.elapsed_time(b) for a, b in ev)
+    region_ms = max_over_ranks(region_ms)
+    step_ms = region_ms / K
+    value = throughput_gbs(step_bytes, K, world, region_ms)
+
+    # ---- the passes, from a second run of the same step with an event between them ----
     if fused:
         # the passes on their own, beside the step (the step runs them as one kernel)
         pass1_ms = [time_launches(pass1, K, stream, dev, flush)]
         pass2_ms = [time_launches(pass2, K, stream, dev, flush)]
     else:
-        pass1_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-        pass2_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    region_ms = t_start.elapsed_time(t_end)
-    if flush is not None:
-        # steps are timed launch to launch; the L2 flush between them is not part of a step
-        region_ms = sum(step_launch_ms)
-    region_ms = max_over_ranks(region_ms)
-    step_ms = region_ms / K
-    value = throughput_gbs(step_bytes, K, world, region_ms)
+        evp = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            evp[i][0].record(stream)
+            pass1()
+            evp[i][1].record(stream)
+            pass2()
+            evp[i][2].record(stream)
+            if flush is not None:
+                flush.fill_(1.0)
+        torch.cuda.synchronize(dev)
+        pass1_ms = [evp[i][0].elapsed_time(evp[i][1]) for i in range(K)]
+        pass2_ms = [evp[i][1].elapsed_time(evp[i][2]) for i in range(K)]
+        instrumented_step_ms = sum(evp[i][0].elapsed_time(evp[i][2]) for i in range(K)) / K
 
     # ---- single-pass mode (delayed amax): one kernel per step, reported beside the step ----
     # each call quantizes with the amax the previous call reduced (two buffers alternate)
@@ -455,7 +459,7 @@ def run_ours(args, w):
     p2 = sum(pass2_ms) / len(pass2_ms)
     p1 = sum(pass1_ms) / len(pass1_ms)
     # the dominant kernel: pass 2, or the one kernel of the step
-    dom_ms = sum(step_launch_ms) / K if fused else p2
+    dom_ms = step_ms if fused else p2
     achieved = step_bytes / (dom_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((src_hash, w.name, group))
@@ -482,8 +486,11 @@ def run_ours(args, w):
                    "pass2_gbs": step_bytes / (p2 / 1e3) / 1e9,
                    "pass2_frac_of_nominal_8000": step_bytes / (p2 / 1e3) / 1e9 / 8000.0,
                    "step_gbs_both_reads": (2 * bytes_in + bytes_out) / (step_ms / 1e3) / 1e9,
-                   "timed": "beside the step, as separate launches" if fused else "inside the step",
-                   "two_launch_step_ms": p1 + p2 if fused else None},
+                   "timed": ("beside the step, as separate launches" if fused else
+                             "a second run of the step, CUDA events before, between and after "
+                             "the passes (each event adds about 2 us)"),
+                   "two_launch_step_ms": p1 + p2 if fused else None,
+                   "instrumented_step_ms": None if fused else instrumented_step_ms},
         "single_pass_delayed": {
             "ms_per_step": single_ms, "gbs": step_bytes / (single_ms / 1e3) / 1e9,
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
