@@ -312,3 +312,43 @@ def test_pass1_on_16_byte_aligned_input(group):
     x_dev.copy_(x_host)
     assert x_dev.data_ptr() % 32 == 16
     check_against_oracle(x_host, group, x_dev=x_dev, label="16B-aligned")
+
+
+# ---------------------------------------------------------------- beyond 32-bit indices -----
+
+@pytest.mark.parametrize("group", [16, 256])
+def test_more_than_2_pow_32_elements(group):
+    """bf16 [65537, 65536]: 2^32 + 65536 elements (8.6 GB), so element and byte offsets pass
+    2^32 and 2^33.  Every value lies in [-1, 1) except one planted 1024 in the last row: any
+    other rotation group has |y| < 16 (at most G values under 1, times 1/sqrt(G)), while the
+    planted group has max |y| >= 64 (the rotation is orthonormal), so the tensor's amax is the
+    last row's, which the oracle computes.  Rows on both sides of element 2^32 and a few others
+    are then compared with the oracle byte for byte (codes, scales), with that amax; so are
+    MXFP4's codes and scales (no global scale)."""
+    M, K = 65537, 65536
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2024 + group)
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, M, 4096):
+        r1 = min(M, r0 + 4096)
+        x[r0:r1] = (torch.rand((r1 - r0, K), generator=gen, device=dev) * 2 - 1).to(torch.bfloat16)
+    x[M - 1, K - 200] = 1024.0
+    amax = hq.hq_rot_amax(x, group)
+    q, s, sg = hq.hq_rotate_quant_nvfp4(x, group, amax)
+    torch.cuda.synchronize()
+    rows = [0, 1, 12345, 32768, 65534, 65535, 65536]   # row 65536 starts at element 2^32
+    xs = synth.as_oracle_array(x[rows].cpu())
+    _, _, last_amax, _ = oracle.quantize(xs[-1:], group)
+    assert f32_bits(amax.cpu().numpy())[0] == f32_bits([last_amax])[0]
+    oq, os_, _, osg = oracle.quantize(xs, group, amax=float(last_amax))
+    assert f32_bits(sg.cpu().numpy())[0] == f32_bits([osg])[0]
+    assert_bytes_equal("scales", s[rows].cpu().numpy(), os_)
+    assert_bytes_equal("codes", q[rows].cpu().numpy(), oq)
+    del s
+    smx = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
+    hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=smx)
+    torch.cuda.synchronize()
+    mq, ms = oracle.quantize_mxfp4(xs, group)
+    assert_bytes_equal("mxfp4 scales", smx[rows].cpu().numpy(), ms)
+    assert_bytes_equal("mxfp4 codes", q[rows].cpu().numpy(), mq)
