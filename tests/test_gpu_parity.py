@@ -323,8 +323,9 @@ def test_more_than_2_pow_32_elements(group):
     other rotation group has |y| < 16 (at most G values under 1, times 1/sqrt(G)), while the
     planted group has max |y| >= 64 (the rotation is orthonormal), so the tensor's amax is the
     last row's, which the oracle computes.  Rows on both sides of element 2^32 and a few others
-    are then compared with the oracle byte for byte (codes, scales), with that amax; so are
-    MXFP4's codes and scales (no global scale)."""
+    are then compared with the oracle byte for byte (codes, scales, and the scales of the
+    swizzled pass at their tile positions), with that amax; so are MXFP4's codes and scales
+    (no global scale)."""
     M, K = 65537, 65536
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
@@ -345,7 +346,21 @@ def test_more_than_2_pow_32_elements(group):
     assert f32_bits(sg.cpu().numpy())[0] == f32_bits([osg])[0]
     assert_bytes_equal("scales", s[rows].cpu().numpy(), os_)
     assert_bytes_equal("codes", q[rows].cpu().numpy(), oq)
+    # swizzled scales: row r, column c at 512 (r / 128 * col_tiles + c / 4) + (r % 32) 16 +
+    # (r / 32 % 4) 4 + c % 4 of the padded buffer
     del s
+    s_sw = torch.empty(hq.hq_swizzled_scales_bytes(M, K), dtype=torch.uint8, device=dev)
+    q.fill_(0)
+    hq.hq_rotate_quant_nvfp4_swizzled(x, group, amax, q=q, scales=s_sw)
+    torch.cuda.synchronize()
+    col_tiles = (K // 16 + 3) // 4
+    c = np.arange(K // 16)
+    offs = np.stack([512 * ((r // 128) * col_tiles + c // 4) + (r % 32) * 16 + (r // 32 % 4) * 4 + c % 4
+                     for r in rows])
+    got = s_sw.cpu().numpy()[offs]
+    assert_bytes_equal("swizzled scales", got, os_)
+    assert_bytes_equal("swizzled-pass codes", q[rows].cpu().numpy(), oq)
+    del s_sw
     smx = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
     hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=smx)
     torch.cuda.synchronize()
