@@ -49,18 +49,30 @@ L2_BYTES = 126 * 1024 * 1024
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879111 GB read + 0.497822 GB written
-    ("1e62e4b1b5744728", "bf16_32768x28672", 16): 1879111168 + 497821952,
+    ("b5557f25bfc38dca", "bf16_32768x28672", 16): 1879111168 + 497821952,
     # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.609 MB read, nothing written back yet
-    ("1e62e4b1b5744728", "bf16_4096x4096", 16): 33609472 + 0,
+    ("b5557f25bfc38dca", "bf16_4096x4096", 16): 33609472 + 0,
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank space, so that only code changes move the hash
+    (C/C++ // and /* */ comments; Python # comments and docstrings are kept as they are)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernels' code (comments excluded), the launch code and the build script."""
     h = hashlib.sha256()
     for rel in ("hadamard_rotation_gb300/csrc/hq_kernels.cuh", "hadamard_rotation_gb300/csrc/hq.cu",
                 "hadamard_rotation_gb300/build.py"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        h.update((_code_only(text) if rel.endswith((".cuh", ".cu")) else text).encode())
     return h.hexdigest()[:16]
 
 

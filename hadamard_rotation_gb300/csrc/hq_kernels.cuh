@@ -1,21 +1,27 @@
 // hq_kernels.cuh -- device code of libhq (sm_103a).
 //
-// The three kernels of the fused Hadamard rotation + NVFP4 quantization
-// ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §1 "The format,
-// precisely" and §2 "The kernel"):
+// The kernels of the fused Hadamard rotation + NVFP4 quantization ("A Fused
+// Hadamard + NVFP4 Quantization Kernel in Triton", §1 "The format, precisely" and
+// §2 "The kernel"):
 //
-//   k_rot_amax            pass 1: stream x, rotate, reduce max |y| into one float.
+//   k_rot_amax_stream     pass 1 for G <= 16 on contiguous rows: stream x, rotate,
+//                         reduce max |y| into one float.
+//   k_rot_amax            pass 1 in tiles (G = 256, strided rows, or a rotated output).
 //   k_rotate_quant_nvfp4  pass 2: stream x once, rotate in registers, block amax,
 //                         E4M3 block scale, E2M1 codes, write codes + scales once.
+//   k_quant_nvfp4_fused   both passes in one cooperative launch, for an x L2 holds.
+//   k_rotate_quant_mxfp4  MXFP4 (E8M0 scale per 32 values), one pass.
 //   k_dequant_nvfp4       round trip: codes * scales, optional inverse rotation.
 //
 // Work decomposition.  A warp owns a "tile" of 128 NVFP4 blocks (2048 elements,
 // 4 KB of bf16); each lane holds 4 whole blocks (64 values) in registers.  Which
 // 4 blocks a lane holds depends on the rotation group:
 //   G <= 16 : block 32*j + lane of the tile (j = 0..3);
-//   G == 256: block 16*(lane/4) + (lane%4) + 4*j -- the 4 lanes of a quad hold
-//             the 16 blocks of one 256-group; index bits 4,5 of the group are the
-//             lane bits, bits 6,7 select the register block j.
+//   G == 256: the 4 lanes of a quad hold the 16 blocks of one 256-group.  In the
+//             plain layout (dequant, swizzled scales) block 16*(lane/4) + (lane%4)
+//             + 4*j: index bits 4,5 of the group are the lane bits, bits 6,7 the
+//             register block j.  Pass 1, pass 2 and MXFP4 use exchange layouts
+//             (slot_block) in which each cross-lane stage moves half of the values.
 // The 64 values sit in float2 pairs (block 0 with block 1, block 2 with block 3)
 // so the butterfly and the division run on the packed fp32x2 pipe of sm_100-
 // family parts (FADD2/FFMA2/FMUL2): one instruction per two values.
@@ -24,19 +30,19 @@
 // warp runs its own TMA pipeline: a ring of kStages tile slots in shared memory,
 // each filled by one cp.async.bulk global->shared copy that completes on the
 // slot's mbarrier.  A warp keeps kStages tiles in flight while it computes
-// (pass 1: 8 warps x 4 x 4 KB = 128 KB per SM, pass 2: 16 warps x 2 x 4 KB) without
-// spending registers on them.  Strided rows (ldx != K) load directly into registers
-// (LoadMode below).
+// (pass 1: 16 warps x 3 x 4 KB = 192 KB per SM, pass 2: 16 warps x 2 x 4 KB)
+// without spending registers on them.  Strided rows (ldx != K) load directly into
+// registers (LoadMode below).
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait that
 // runs out records kFaultWaitTimeout in g_hq_fault, waits (bounded) for the
 // warp's copies still in flight and leaves the loop, so nothing can hang.
 //
 // Bit-exactness.  The butterfly performs the stages h = 1, 2, 4, 8 (inside a
-// block), then for G = 256 h = 16, 32 (across the quad's lanes), 64, 128
-// (across the lane's register blocks), each stage an fp32 add/sub with one
-// rounding, exactly as the definition.  The final multiply by 1/sqrt(G) is
-// folded into the division (see k_rotate_quant_nvfp4); that fold is exact on the
-// fast path's domain, and the slow path evaluates the definition literally.
+// block), then for G = 256 h = 16, 32, 64, 128 (across blocks: in registers, or
+// across the quad's lanes), each stage an fp32 add/sub with one rounding, exactly
+// as the definition.  The final multiply by 1/sqrt(G) is folded into the division
+// (see k_rotate_quant_nvfp4); that fold is exact on the fast path's domain, and the
+// slow path evaluates the definition literally.
 #pragma once
 
 #include <cuda_fp16.h>
