@@ -1325,24 +1325,19 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
       // in word 4 (rs & 1) + (rs >> 1).  Lane L collects column group L (columns
       // c0 + 4L .. + 3) of the unit's rows and writes its 32 bytes after the last
       // tile.  Blocks outside the tensor carry scale 0, which the padding must hold.
-      // The 4 bytes of 4 consecutive columns (lanes 4m .. 4m+3) first go to lane 4m.
-      uint32_t word[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t sbyte = (sb2[j >> 1] >> ((j & 1) * 8)) & 0xFFu;
-        const uint32_t w2 = sbyte | (__shfl_down_sync(0xFFFFFFFFu, sbyte, 1) << 8);
-        word[j] = w2 | (__shfl_down_sync(0xFFFFFFFFu, w2, 2) << 16);
-      }
-      // Column group L sits in lane 4 (L % 8), slot L / 8 (G <= 16: block 32 j + lane),
-      // or in lane 4 (L / 4), slot L % 4 (G = 256: block 16 (lane / 4) + lane % 4 + 4 j).
+      // Column group L sits in lanes 4 (L % 8) + m, slot L / 8 (G <= 16: block 32 j + lane),
+      // or in lanes 4 (L / 4) + m, slot L % 4 (G = 256: block 16 (lane / 4) + lane % 4 + 4 j),
+      // m = 0..3 for its 4 columns.  Each lane packs its 4 slot bytes into one word; lane L
+      // reads the words of its 4 source lanes and keeps byte `want` of each (byte permutes).
+      const uint32_t all4 = __byte_perm(sb2[0], sb2[1], 0x5410);  // slot j in byte j
       const int src = (G == 256) ? (lane & ~3) : 4 * (lane & 7);
-      const int want = (G == 256) ? (lane & 3) : (lane >> 3);
-      uint32_t mine = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v = __shfl_sync(0xFFFFFFFFu, word[j], src);
-        if (j == want) mine = v;
-      }
+      const uint32_t want = (G == 256) ? (lane & 3) : (lane >> 3);
+      const uint32_t sel = want | ((want + 4u) << 4);
+      const uint32_t r0 = __shfl_sync(0xFFFFFFFFu, all4, src);
+      const uint32_t r1 = __shfl_sync(0xFFFFFFFFu, all4, src + 1);
+      const uint32_t r2 = __shfl_sync(0xFFFFFFFFu, all4, src + 2);
+      const uint32_t r3 = __shfl_sync(0xFFFFFFFFu, all4, src + 3);
+      const uint32_t mine = __byte_perm(__byte_perm(r0, r1, sel), __byte_perm(r2, r3, sel), 0x5410);
 #pragma unroll
       for (int i = 0; i < 7; ++i) swz_acc[i] = swz_acc[i + 1];
       swz_acc[7] = mine;  // swz_acc[rs] holds row rs once rs = 7
