@@ -16,9 +16,22 @@ from ._lib import HQ_BF16, HQ_F32, check
 _DTYPES = {torch.float32: HQ_F32, torch.bfloat16: HQ_BF16}
 
 
-def _stream_handle(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream_handle(stream: torch.cuda.Stream | None,
+                   device: torch.device | None = None) -> ctypes.c_void_p:
+    """The cudaStream_t to pass: ``stream``, or the current stream of ``device`` (default: the
+    current device).  A given stream must belong to ``device``."""
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(device: torch.device, name: str, *args, stream: torch.cuda.Stream | None = None) -> None:
+    """Call the C entry point ``name`` with ``device`` current (the library launches on the
+    current device), on ``stream`` or that device's current stream; raise on a non-OK status."""
+    with torch.cuda.device(device):
+        check(getattr(_lib.load(), name)(*args, _stream_handle(stream, device)), name)
 
 
 def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p | None:
@@ -58,8 +71,8 @@ def hq_rot_amax(x: torch.Tensor, group: int, amax: torch.Tensor | None = None,
     amax = _need(amax, (1,), torch.float32, x.device, "amax")
     if y is not None:
         y = _need(y, (M, K), torch.float32, x.device, "y")
-    check(_lib.load().hq_rot_amax(_ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(y),
-                                  _stream_handle(stream)), "hq_rot_amax")
+    _call(x.device, "hq_rot_amax", _ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(y),
+          stream=stream)
     return amax
 
 
@@ -73,9 +86,8 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
     scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
     s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
-    check(_lib.load().hq_rotate_quant_nvfp4(_ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q),
-                                            _ptr(scales), _ptr(s_global), _stream_handle(stream)),
-          "hq_rotate_quant_nvfp4")
+    _call(x.device, "hq_rotate_quant_nvfp4", _ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q),
+          _ptr(scales), _ptr(s_global), stream=stream)
     return q, scales, s_global
 
 
@@ -115,9 +127,8 @@ def hq_quantize_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor | None = N
             workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
     else:
         workspace = None
-    check(_lib.load().hq_quantize_nvfp4(_ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q),
-                                        _ptr(scales), _ptr(s_global), _ptr(workspace),
-                                        _stream_handle(stream)), "hq_quantize_nvfp4")
+    _call(x.device, "hq_quantize_nvfp4", _ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q),
+          _ptr(scales), _ptr(s_global), _ptr(workspace), stream=stream)
     return q, scales, s_global, amax
 
 
@@ -143,9 +154,8 @@ def hq_rotate_quant_nvfp4_swizzled(x: torch.Tensor, group: int, amax: torch.Tens
     n = hq_swizzled_scales_bytes(M, K)
     scales = _need(scales, (n,), torch.uint8, x.device, "scales")
     s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
-    check(_lib.load().hq_rotate_quant_nvfp4_swizzled(
-        _ptr(x), dt, M, K, ldx, group, _ptr(amax), _ptr(q), _ptr(scales), _ptr(s_global),
-        _stream_handle(stream)), "hq_rotate_quant_nvfp4_swizzled")
+    _call(x.device, "hq_rotate_quant_nvfp4_swizzled", _ptr(x), dt, M, K, ldx, group, _ptr(amax),
+          _ptr(q), _ptr(scales), _ptr(s_global), stream=stream)
     return q, scales, s_global
 
 
@@ -163,9 +173,8 @@ def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.
     q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
     scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
     s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
-    check(_lib.load().hq_rotate_quant_nvfp4_delayed(
-        _ptr(x), dt, M, K, ldx, group, _ptr(amax_prev), _ptr(amax_next), _ptr(q), _ptr(scales),
-        _ptr(s_global), _stream_handle(stream)), "hq_rotate_quant_nvfp4_delayed")
+    _call(x.device, "hq_rotate_quant_nvfp4_delayed", _ptr(x), dt, M, K, ldx, group,
+          _ptr(amax_prev), _ptr(amax_next), _ptr(q), _ptr(scales), _ptr(s_global), stream=stream)
     return q, scales, s_global, amax_next
 
 
@@ -176,8 +185,8 @@ def hq_rotate_quant_mxfp4(x: torch.Tensor, group: int, q: torch.Tensor | None = 
     dt, M, K, ldx = _x_args(x)
     q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
     scales = _need(scales, (M, K // 32), torch.uint8, x.device, "scales")
-    check(_lib.load().hq_rotate_quant_mxfp4(_ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
-                                            _stream_handle(stream)), "hq_rotate_quant_mxfp4")
+    _call(x.device, "hq_rotate_quant_mxfp4", _ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
+          stream=stream)
     return q, scales
 
 
@@ -192,8 +201,8 @@ def hq_dequant_mxfp4(q: torch.Tensor, scales: torch.Tensor, group: int, unrotate
     q = _need(q, (M, K2), torch.uint8, q.device, "q")
     scales = _need(scales, (M, K // 32), torch.uint8, q.device, "scales")
     out = _need(out, (M, K), torch.float32, q.device, "out")
-    check(_lib.load().hq_dequant_mxfp4(_ptr(q), _ptr(scales), M, K, group, 1 if unrotate else 0,
-                                       _ptr(out), _stream_handle(stream)), "hq_dequant_mxfp4")
+    _call(q.device, "hq_dequant_mxfp4", _ptr(q), _ptr(scales), M, K, group, 1 if unrotate else 0,
+          _ptr(out), stream=stream)
     return out
 
 
@@ -204,8 +213,8 @@ def hq_rotate_quant_int8(x: torch.Tensor, group: int, q: torch.Tensor | None = N
     dt, M, K, ldx = _x_args(x)
     q = _need(q, (M, K), torch.int8, x.device, "q")
     scales = _need(scales, (M,), torch.float32, x.device, "scales")
-    check(_lib.load().hq_rotate_quant_int8(_ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
-                                           _stream_handle(stream)), "hq_rotate_quant_int8")
+    _call(x.device, "hq_rotate_quant_int8", _ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
+          stream=stream)
     return q, scales
 
 
@@ -221,9 +230,8 @@ def hq_dequant_nvfp4(q: torch.Tensor, scales: torch.Tensor, s_global: torch.Tens
     scales = _need(scales, (M, K // 16), torch.uint8, q.device, "scales")
     s_global = _need(s_global, (1,), torch.float32, q.device, "s_global")
     out = _need(out, (M, K), torch.float32, q.device, "out")
-    check(_lib.load().hq_dequant_nvfp4(_ptr(q), _ptr(scales), _ptr(s_global), M, K, group,
-                                       1 if unrotate else 0, _ptr(out), _stream_handle(stream)),
-          "hq_dequant_nvfp4")
+    _call(q.device, "hq_dequant_nvfp4", _ptr(q), _ptr(scales), _ptr(s_global), M, K, group,
+          1 if unrotate else 0, _ptr(out), stream=stream)
     return out
 
 
