@@ -141,6 +141,20 @@ def test_binding_rejects_host_tensors():
         hq.hq_rotate_quant_nvfp4(x, 16, torch.zeros(1))
 
 
+def test_binding_refuses_a_stream_of_another_device():
+    # The library launches on the current device; the binding makes the tensors' device
+    # current and must not hand it a stream that belongs to another device.
+    from hadamard_rotation_gb300 import api
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        api._stream_handle(FakeStream(), torch.device("cuda", 0))
+    assert api._stream_handle(FakeStream(), torch.device("cuda", 1)).value is None  # handle 0
+
+
 def test_read_fault_rejects_null(lib):
     assert lib.hq_read_fault(None, 0) == 1
 
