@@ -127,13 +127,33 @@ cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, size_t smem, unsig
 }
 
 // Launch with `smem` bytes of dynamic shared memory (the TMA ring of the
-// contiguous-row kernels; 0 for the others).
+// contiguous-row kernels; 0 for the others).  pdl: allow programmatic dependent launch,
+// so that the grid may be launched while the kernel before it on the stream is still
+// running; the kernel must then execute griddepcontrol.wait before it touches global
+// memory (pass 2 does so first thing), which makes it wait for that kernel's completion
+// and memory, exactly as without the attribute.  Only the launch and the CTAs' start
+// overlap the previous kernel's end.
 template <typename Kernel>
-hq_status launch(Kernel kernel, const hq::Params& p, hq_stream stream, size_t smem = 0) {
+hq_status launch(Kernel kernel, const hq::Params& p, hq_stream stream, size_t smem = 0, bool pdl = false) {
   unsigned grid = 0;
   cudaError_t e = persistent_grid(reinterpret_cast<const void*>(kernel), p.n_tiles, smem, &grid);
   if (e != cudaSuccess) return cuda_fail(e);
-  kernel<<<grid, hq::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  if (pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(hq::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+  } else {
+    kernel<<<grid, hq::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return HQ_OK;
@@ -220,12 +240,12 @@ hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream
   using hq::k_rotate_quant_nvfp4;
   constexpr int kMode = HQ_PASS2_MODE;
   if (bf16)
-    return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided, NEXT>, p, s)
+    return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided, NEXT>, p, s, 0, true)
                    : launch(k_rotate_quant_nvfp4<G, true, kMode, NEXT>, p, s,
-                            ring_bytes<HQ_PASS2_STAGES>(kMode, true));
-  return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided, NEXT>, p, s)
+                            ring_bytes<HQ_PASS2_STAGES>(kMode, true), true);
+  return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided, NEXT>, p, s, 0, true)
                  : launch(k_rotate_quant_nvfp4<G, false, kMode, NEXT>, p, s,
-                          ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+                          ring_bytes<HQ_PASS2_STAGES>(kMode, false), true);
 }
 
 // Pass 2 with swizzled scales: row-group tiles through the TMA ring, one bulk copy

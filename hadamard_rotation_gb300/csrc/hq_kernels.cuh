@@ -1012,6 +1012,8 @@ __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
 
 template <int G, bool BF16, int MODE, bool WRITE_Y>
 __global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params p) {
+  // As k_rot_amax_stream: the next kernel may be launched now.
+  asm volatile("griddepcontrol.launch_dependents;");
   // |y| = RN(|z| / sqrt(G)) is monotone in |z|, so max |y| = RN(max |z| / sqrt(G))
   // exactly; the scaling commutes with the max over the CTA.
   cta_amax_to_global(__fmul_rn(rot_amax_tiles<G, BF16, MODE, WRITE_Y>(p), inv_sqrt_g<G>()), p.amax_out);
@@ -1038,6 +1040,9 @@ __device__ __forceinline__ void ld_v8_stream(const uint8_t* src, uint32_t* w) {
 
 template <int G, bool BF16>
 __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_amax_stream(Params p) {
+  // Let the next kernel on the stream (pass 2) be launched now; it waits for this grid's
+  // completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kWords = BF16 ? 8 : 16;  // 32-bit words per 16-element block
   const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;
   uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -1358,6 +1363,10 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
 
 template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
+  // Launched with programmatic dependent launch: wait for the kernel before this one on
+  // the stream (normally pass 1, which writes *amax_in) to complete before any access to
+  // global memory.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ>(p, *p.amax_in);
 }
 
