@@ -473,8 +473,8 @@ hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_
   const bool strided = is_strided(M, K, ldx);
   using hq::k_rotate_quant_mxfp4;
   constexpr int kMode = HQ_PASS2_MODE;
-  auto go = [&](auto k_strided, auto k_flat, size_t smem) {
-    return strided ? launch(k_strided, p, stream) : launch(k_flat, p, stream, smem);
+  auto go = [&](auto k_strided, auto k_flat, size_t smem) {  // programmatic dependent launch
+    return strided ? launch(k_strided, p, stream, 0, true) : launch(k_flat, p, stream, smem, true);
   };
   switch (group) {
     case 0:

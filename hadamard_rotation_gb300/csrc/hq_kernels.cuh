@@ -1420,6 +1420,9 @@ __global__ void __launch_bounds__(kThreads, BF16 ? 2 : 1) k_quant_nvfp4_fused(Pa
 // tiles arrive with the first butterfly stage applied.
 template <int G, bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
+  // Launched with programmatic dependent launch, as pass 2: wait for the kernel before this
+  // one on the stream to complete before any access to global memory.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr float c = inv_sqrt_g<G>();
   constexpr int kOrder = G == 256 ? 2 : 0;
   constexpr bool kS1 = BF16 && G == 256;
