@@ -48,10 +48,10 @@ L2_BYTES = 126 * 1024 * 1024
 # workload itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879111 GB read + 0.498000 GB written
-    ("0afea1e99abb1aff", "bf16_32768x28672", 16): 1879111168 + 497999872,
+    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879112 GB read + 0.497741 GB written
+    ("013b7eb4bf9db83f", "bf16_32768x28672", 16): 1879111680 + 497740800,
     # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.610 MB read, nothing written back yet
-    ("0afea1e99abb1aff", "bf16_4096x4096", 16): 33609984 + 0,
+    ("013b7eb4bf9db83f", "bf16_4096x4096", 16): 33609984 + 0,
 }
 
 

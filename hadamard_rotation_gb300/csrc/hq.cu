@@ -209,8 +209,8 @@ size_t ring_bytes(int mode, bool bf16) {
 template <int G, bool BF16, int MODE>
 hq_status launch_rot_amax(const hq::Params& p, bool write_y, hq_stream s) {
   const size_t smem = ring_bytes<HQ_PASS1_STAGES>(MODE, BF16);
-  return write_y ? launch(hq::k_rot_amax<G, BF16, MODE, true>, p, s, smem)
-                 : launch(hq::k_rot_amax<G, BF16, MODE, false>, p, s, smem);
+  return write_y ? launch(hq::k_rot_amax<G, BF16, MODE, true>, p, s, smem, p.sync != nullptr)
+                 : launch(hq::k_rot_amax<G, BF16, MODE, false>, p, s, smem, p.sync != nullptr);
 }
 
 // Pass 1 for G <= 16 on contiguous, 32-byte aligned rows uses the streaming kernel
@@ -224,8 +224,8 @@ hq_status dispatch_rot_amax(const hq::Params& p, bool bf16, bool strided, bool w
                             hq_stream s) {
   if constexpr (G <= 16) {
     if (HQ_PASS1_STREAM && !strided && !write_y && aligned(p.x, 32))
-      return bf16 ? launch(hq::k_rot_amax_stream<G, true>, p, s)
-                  : launch(hq::k_rot_amax_stream<G, false>, p, s);
+      return bf16 ? launch(hq::k_rot_amax_stream<G, true>, p, s, 0, p.sync != nullptr)
+                  : launch(hq::k_rot_amax_stream<G, false>, p, s, 0, p.sync != nullptr);
   }
   constexpr int kMode = HQ_PASS1_MODE;
   if (bf16)
@@ -337,7 +337,24 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
   const bool fused = workspace && M > 0 && K > 0 && !is_strided(M, K, ldx) &&
                      M * K * elem_size(dtype) <= HQ_QUANTIZE_FUSED_MAX_BYTES;
   if (!fused) {
-    st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
+    if (workspace && M > 0 && K > 0) {
+      // Pass 1 reduces into the workspace (0 on entry) and its last CTA writes *amax, so no
+      // memset separates it from the kernel before it: it is launched as a programmatic
+      // dependent and waits for that kernel's completion before it reads x.
+      hq::Params p = base_params(x, dtype, M, K, ldx);
+      p.amax_out = reinterpret_cast<float*>(workspace + 1);
+      p.sync = workspace;
+      p.amax_copy = amax;
+      const bool bf16 = dtype == HQ_BF16;
+      const bool strided = is_strided(M, K, ldx);
+      switch (group) {
+        case 0: st = dispatch_rot_amax<0>(p, bf16, strided, false, stream); break;
+        case 16: st = dispatch_rot_amax<16>(p, bf16, strided, false, stream); break;
+        default: st = dispatch_rot_amax<256>(p, bf16, strided, false, stream); break;
+      }
+    } else {
+      st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
+    }
     if (st != HQ_OK) return st;
     return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
   }

@@ -93,7 +93,7 @@ struct Params {
   FastDiv div_nbr;         // divider for nbr (valid when nb < 2^32)
   uint64_t n_tiles;        // ceil(nb / kTileBlocks)
   // pass 1
-  float* amax_out;         // atomically max-reduced (zeroed by the host call)
+  float* amax_out;         // atomically max-reduced (zeroed by the host call, or a workspace word)
   float* y;                // optional fp32 rotated output [M, K]
   // pass 2
   const float* amax_in;
@@ -106,6 +106,7 @@ struct Params {
   FastDiv div_ncc;         // divider for n_cc
   // both passes in one launch (k_quant_nvfp4_fused)
   unsigned* sync;          // [0] CTAs past pass 1, [1] amax bits, [2] CTAs done; 0 on entry and exit
+                           // (pass 1 with a workspace: [1] amax bits, [2] CTAs done)
   float* amax_copy;        // the tensor's amax, written once it is known
   // dequant
   const uint8_t* dq_q;
@@ -154,7 +155,12 @@ __device__ __forceinline__ float block_absmax(const float2 (&v)[16]) {
 // max over the CTA of each thread's `v`, then one atomicMax into *out.  Non-negative
 // floats (and NaN, with the sign bit clear) order like their bit patterns as unsigned
 // integers.  Every thread of the CTA must call this.
-__device__ __forceinline__ void cta_amax_to_global(float v, float* out) {
+// With `count` (pass 1 of hq_quantize_nvfp4 with a workspace): *out is a workspace word
+// that is 0 on entry; each CTA counts itself out in *count after its atomicMax, and the
+// last one moves the tensor's amax to *final_out and puts both words back to 0.  No
+// memset then precedes the launch.
+__device__ __forceinline__ void cta_amax_to_global(float v, float* out, unsigned* count = nullptr,
+                                                   float* final_out = nullptr) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v = max_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
   __shared__ float red[kWarpsPerCta];
@@ -165,6 +171,14 @@ __device__ __forceinline__ void cta_amax_to_global(float v, float* out) {
 #pragma unroll
     for (int w = 1; w < kWarpsPerCta; ++w) m = max_nan(m, red[w]);
     atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(m));
+    if (count) {
+      __threadfence();
+      if (atomicAdd(count, 1u) == gridDim.x - 1) {
+        __threadfence();
+        *final_out = __uint_as_float(atomicExch(reinterpret_cast<unsigned int*>(out), 0u));
+        atomicExch(count, 0u);
+      }
+    }
   }
 }
 
@@ -1016,7 +1030,9 @@ __global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params
   asm volatile("griddepcontrol.launch_dependents;");
   // |y| = RN(|z| / sqrt(G)) is monotone in |z|, so max |y| = RN(max |z| / sqrt(G))
   // exactly; the scaling commutes with the max over the CTA.
-  cta_amax_to_global(__fmul_rn(rot_amax_tiles<G, BF16, MODE, WRITE_Y>(p), inv_sqrt_g<G>()), p.amax_out);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as k_rot_amax_stream
+  cta_amax_to_global(__fmul_rn(rot_amax_tiles<G, BF16, MODE, WRITE_Y>(p), inv_sqrt_g<G>()), p.amax_out,
+                     p.sync ? p.sync + 2 : nullptr, p.amax_copy);
 }
 
 // ---------------------------------------------------------------------------
@@ -1041,8 +1057,11 @@ __device__ __forceinline__ void ld_v8_stream(const uint8_t* src, uint32_t* w) {
 template <int G, bool BF16>
 __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_amax_stream(Params p) {
   // Let the next kernel on the stream (pass 2) be launched now; it waits for this grid's
-  // completion before it reads anything.
+  // completion before it reads anything.  When this grid was itself launched as a
+  // programmatic dependent (hq_quantize_nvfp4 with a workspace), wait for the kernel before
+  // it to complete before reading x.
   asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kWords = BF16 ? 8 : 16;  // 32-bit words per 16-element block
   const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;
   uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -1108,7 +1127,8 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
     consume(ca, cb);
   }
 #endif
-  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), p.amax_out);
+  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), p.amax_out, p.sync ? p.sync + 2 : nullptr,
+                     p.amax_copy);
 }
 
 // ---------------------------------------------------------------------------

@@ -123,12 +123,17 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
  *   When x's rows are back to back, x takes at most HQ_QUANTIZE_FUSED_MAX_BYTES and `workspace`
  *   is given, the two passes run as one cooperative kernel: the first reads x with an L2
  *   evict-last hint, all CTAs meet at a grid-wide barrier once the amax is reduced, and the
- *   second reads x back from L2.  Otherwise the call is hq_rot_amax then hq_rotate_quant_nvfp4.
+ *   second reads x back from L2.  Otherwise the call is two launches, pass 1 then pass 2 as
+ *   hq_rotate_quant_nvfp4.  With `workspace`, pass 1 reduces the amax into the workspace and
+ *   its last CTA writes *amax (no memset before it), and both launches are programmatic
+ *   dependents of the kernel before them on the stream (each waits for that kernel to complete
+ *   before it reads memory); without, pass 1 is hq_rot_amax.
  *
  *   x, dtype, M, K, ldx, group : as for hq_rot_amax.
  *   amax      : 1 float on the device (written; 0 for an empty tensor).
  *   q, scales, s_global : as for hq_rotate_quant_nvfp4.
- *   workspace : NULL (two launches), or HQ_QUANTIZE_WORKSPACE_WORDS uint32 on the device, 4-byte
+ *   workspace : NULL (hq_rot_amax then hq_rotate_quant_nvfp4), or HQ_QUANTIZE_WORKSPACE_WORDS
+ *               uint32 on the device, 4-byte
  *               aligned, all 0 before its first use (e.g. cudaMemset).  Each call that records
  *               no fault leaves it 0 again.  Calls that may run at the same time (different
  *               streams) need different workspaces.

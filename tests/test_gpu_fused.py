@@ -131,6 +131,37 @@ def test_size_limit_both_sides(rows):
     assert fused == (rows == 8192), names
 
 
+def test_two_launches_with_a_workspace_leave_it_zero():
+    """Strided rows always take the two launches; with a workspace, pass 1 reduces the amax
+    into it (no memset before the launch) and its last CTA writes amax.  A large, a small and
+    a large amax in turn, every group and both input types (the streaming pass 1 needs
+    contiguous rows, so the tiled one runs here; the 8193-row case above covers the streaming
+    one): every result exact and the workspace back to 0 after each call."""
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    for dtype in (torch.bfloat16, torch.float32):
+        for i, scale in enumerate((100.0, 0.01, 100.0)):
+            x_host = rand_input(300, 2048, dtype, seed=40 + i, scale=scale)
+            padded = torch.zeros(300, 2048 + 256, dtype=dtype, device="cuda")
+            padded[:, :2048] = x_host.cuda()
+            for group in (0, 16, 256):
+                got = hq.hq_quantize_nvfp4(padded[:, :2048], group, workspace=ws)
+                torch.cuda.synchronize()
+                check(x_host, group, got, f"strided {dtype} call {i} group {group}")
+                assert not ws.any().item()
+
+
+def test_streaming_pass_1_with_a_workspace_in_a_row():
+    """Contiguous bf16 rows above the one-launch limit: the streaming pass 1 reduces into the
+    workspace.  Two different tensors in a row on one workspace, both exact, workspace 0."""
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    for seed, scale in ((51, 7.0), (52, 0.003)):
+        x_host = rand_input(8200, 4096, torch.bfloat16, seed=seed, scale=scale)
+        got = hq.hq_quantize_nvfp4(x_host.cuda(), 16, workspace=ws)
+        torch.cuda.synchronize()
+        check(x_host, 16, got, f"bf16 [8200, 4096] seed {seed}")
+        assert not ws.any().item()
+
+
 def test_two_launch_modes_agree():
     """fused=False (no workspace: the two launches) and strided rows (always two launches) give
     the same bytes as the one-launch path."""
