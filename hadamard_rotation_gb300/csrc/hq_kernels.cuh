@@ -37,6 +37,13 @@
 // runs out records kFaultWaitTimeout in g_hq_fault, waits (bounded) for the
 // warp's copies still in flight and leaves the loop, so nothing can hang.
 //
+// Launch order.  Pass 2 and MXFP4 are launched as programmatic dependents of the
+// kernel before them on the stream, and so is pass 1 when hq_quantize_nvfp4 passes
+// it a workspace: each executes griddepcontrol.wait before it touches global memory,
+// which waits for that kernel to complete.  The pass-1 kernels execute
+// griddepcontrol.launch_dependents as they start, so pass 2's grid is launched while
+// pass 1 runs and its CTAs start as pass 1's leave the SMs.
+//
 // Bit-exactness.  The butterfly performs the stages h = 1, 2, 4, 8 (inside a
 // block), then for G = 256 h = 16, 32, 64, 128 (across blocks: in registers, or
 // across the quad's lanes), each stage an fp32 add/sub with one rounding, exactly
