@@ -279,3 +279,31 @@ def test_binding_constants_match_the_header():
     limit = re.search(r"#define HQ_QUANTIZE_FUSED_MAX_BYTES \((\d+)ll \* 1024 \* 1024\)", text)
     assert words and int(words.group(1)) == api.HQ_QUANTIZE_WORKSPACE_WORDS
     assert limit and int(limit.group(1)) * 1024 * 1024 == api.HQ_QUANTIZE_FUSED_MAX_BYTES
+
+
+def test_noalloc_argument_checks_and_size_limit(lib):
+    # hq_quantize_nvfp4_host_noalloc checks its arguments and the size of its fixed device
+    # array before it makes any CUDA call, so every status below is decided on the host.
+    def na(x=FAKE, dt=1, M=4, K=32, G=16, q=FAKE, s=FAKE, sg=FAKE):
+        return lib.hq_quantize_nvfp4_host_noalloc(
+            P(x) if x else None, dt, M, K, G, P(q) if q else None, P(s) if s else None,
+            P(sg) if sg else None, None)
+    assert na(x=0) == 1 and na(q=0) == 1 and na(s=0) == 1 and na(sg=0) == 1
+    assert na(G=32) == 5 and na(dt=2) == 4
+    assert na(K=24) == 2 and na(K=272, G=256) == 2 and na(M=-1) == 2
+    assert na(M=2 ** 62, K=64) == 2               # M*K overflows
+    assert na(M=0, x=0) == 0                      # empty: nothing to do
+    # The array holds r(n*e) + r(n/2) + r(n/16) + 512 bytes, r() rounding up to 256 bytes.
+    limit = 32 * 1024 * 1024
+    assert "#define HQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)" in open(HEADER).read()
+
+    def need(n, e):
+        r = lambda b: (b + 255) // 256 * 256
+        return r(n * e) + r(n // 2) + r(n // 16) + 512
+
+    for dt, e, rows in ((1, 2, 3196), (0, 4, 1795)):  # the most rows of 4096 that fit
+        assert need(rows * 4096, e) <= limit < need((rows + 1) * 4096, e)
+        assert na(dt=dt, M=rows + 1, K=4096) == 7
+        if not torch.cuda.is_available():
+            assert na(dt=dt, M=rows, K=4096) == 6     # fits: the call reaches the runtime
+    assert na(M=2 ** 41, K=16) == 7
