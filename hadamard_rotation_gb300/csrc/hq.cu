@@ -167,6 +167,8 @@ hq_status check_x(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx,
   if (M < 0 || K < 0 || ldx < K) return HQ_ERR_SHAPE;
   const int64_t unit = group > 16 ? group : 16;
   if (K % unit != 0) return HQ_ERR_SHAPE;
+  // The kernels count the 16-element blocks of one row in 32 bits.
+  if (K / 16 > static_cast<int64_t>(UINT32_MAX)) return HQ_ERR_SHAPE;
   if (K > 0 && M > INT64_MAX / K) return HQ_ERR_SHAPE;
   const int64_t es = elem_size(dt);
   if (ldx > INT64_MAX / es) return HQ_ERR_SHAPE;
@@ -182,7 +184,7 @@ hq::Params base_params(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t
   p.x = static_cast<const uint8_t*>(x);
   p.ldx_bytes = ldx * elem_size(dt);
   p.nb = static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 16);
-  p.nbr = static_cast<uint32_t>(K / 16 > 0xFFFFFFFFll ? 0xFFFFFFFFu : K / 16);
+  p.nbr = static_cast<uint32_t>(K / 16);  // check_x bounds it
   if (p.nbr > 0) p.div_nbr = make_fast_div(p.nbr);
   p.n_tiles = (p.nb + hq::kTileBlocks - 1) / hq::kTileBlocks;
   return p;

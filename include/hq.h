@@ -59,7 +59,9 @@ extern "C" {
 typedef enum {
   HQ_OK = 0,
   HQ_ERR_NULL = 1,  /* a required pointer is NULL (or two that must differ are the same) */
-  HQ_ERR_SHAPE = 2, /* M < 0, K < 0, ldx < K, or K not a multiple of max(16, G) */
+  HQ_ERR_SHAPE = 2, /* M < 0, K < 0, ldx < K, K not a multiple of max(16, G), M * K beyond
+                       int64, or, in the calls that read x, K >= 2^36 (a row of 2^32 or
+                       more 16-element blocks) */
   HQ_ERR_ALIGN = 3, /* a pointer or the row stride breaks the alignment rules below */
   HQ_ERR_DTYPE = 4, /* unknown element type */
   HQ_ERR_GROUP = 5, /* rotation group not in {0, 16, 256} */

@@ -91,6 +91,13 @@ def test_bad_shapes(lib):
     assert rq(lib, K=-16) == 2
     assert rq(lib, ldx=16) == 2                  # ldx < K
     assert rq(lib, M=2 ** 62, K=64, ldx=64) == 2  # M*K overflows
+    big = 2 ** 36                                 # 2^32 blocks in one row: beyond the kernels
+    assert rq(lib, M=1, K=big, ldx=big) == 2 and ra(lib, M=1, K=big, ldx=big) == 2
+    assert lib.hq_rotate_quant_mxfp4(P(FAKE), 1, 1, big, big, 16, P(FAKE), P(FAKE), None) == 2
+    assert lib.hq_quantize_nvfp4(P(FAKE), 1, 1, big, big, 16, P(FAKE), P(FAKE), P(FAKE), None,
+                                 P(FAKE + 256), None) == 2
+    if not torch.cuda.is_available():             # one block less passes the shape checks
+        assert ra(lib, M=1, K=big - 16, ldx=big - 16) == 6
     assert ra(lib, K=48, ldx=48, G=256) == 2
     assert dq(lib, K=24) == 2
     assert dq(lib, K=272, G=256) == 2
