@@ -58,6 +58,8 @@ NCU_TRAFFIC = {
 SAME_KERNELS_AS = {
     # hq.cu: check_x refuses K >= 2^36 (HQ_ERR_SHAPE), so base_params no longer clamps K/16
     "6b929af7aee0bc2f": "013b7eb4bf9db83f",
+    # and hq_quantize_nvfp4 checks q, scales and s_global before it enqueues pass 1
+    "94e8bcdf12bb41d7": "013b7eb4bf9db83f",
 }
 
 

@@ -336,8 +336,14 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
   if (st != HQ_OK) return st;
   if (!amax) return HQ_ERR_NULL;
   if (!aligned(amax, 4) || (workspace && !aligned(workspace, 4))) return HQ_ERR_ALIGN;
+  // Every argument is checked before pass 1 is enqueued.
+  if (M > 0 && K > 0) {
+    if (!q || !scales) return HQ_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(scales, 4) || (s_global && !aligned(s_global, 4)))
+      return HQ_ERR_ALIGN;
+  }
   const bool fused = workspace && M > 0 && K > 0 && !is_strided(M, K, ldx) &&
-                     M * K * elem_size(dtype) <= HQ_QUANTIZE_FUSED_MAX_BYTES;
+                     M * K <= HQ_QUANTIZE_FUSED_MAX_BYTES / elem_size(dtype);
   if (!fused) {
     if (workspace && M > 0 && K > 0) {
       // Pass 1 reduces into the workspace (0 on entry) and its last CTA writes *amax, so no
@@ -360,9 +366,6 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
     if (st != HQ_OK) return st;
     return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
   }
-  if (!q || !scales) return HQ_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(scales, 4) || (s_global && !aligned(s_global, 4)))
-    return HQ_ERR_ALIGN;
   hq::Params p = base_params(x, dtype, M, K, ldx);
   p.q = q;
   p.s = scales;

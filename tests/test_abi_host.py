@@ -276,6 +276,13 @@ def test_quantize_argument_checks(lib):
     assert qz(a=FAKE + 2) == 3 and qz(ws=FAKE + 2) == 3
     assert qz(q=FAKE + 8) == 3 and qz(s=FAKE + 2) == 3 and qz(x=FAKE + 8) == 3
     assert qz(sg=FAKE + 1) == 3
+    # The two-launch cases (strided rows, x above the one-launch limit, no workspace) check
+    # the outputs before pass 1 is enqueued too: without a device these would otherwise
+    # report the failed launch (6).
+    for kw in (dict(ldx=128), dict(M=65536, K=1024, ldx=1024), dict(ws=0)):
+        assert qz(q=0, **kw) == 1 and qz(s=0, **kw) == 1
+        assert qz(q=FAKE + 8, **kw) == 3 and qz(s=FAKE + 2, **kw) == 3 and qz(sg=FAKE + 1, **kw) == 3
+    assert qz(M=2 ** 40, K=2 ** 22, ldx=2 ** 22, q=0) == 1   # M*K*4 would overflow int64
 
 
 def test_binding_constants_match_the_header():
