@@ -93,7 +93,9 @@ size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool sizes(int64_t M, int64_t K, hq_dtype dt, size_t* xb, size_t* qb, size_t* sb) {
   if (M <= 0 || K <= 0 || K % 16 != 0) return false;
   if (M > INT64_MAX / K) return false;
+  if (K / 16 > 0xFFFFFFFFll) return false;  // a row the kernels can index (hq_rot_amax's bound)
   const uint64_t n = static_cast<uint64_t>(M) * static_cast<uint64_t>(K);
+  if (n > (uint64_t{1} << 58)) return false;  // keeps every byte count below from wrapping
   *xb = n * (dt == HQ_BF16 ? 2u : 4u);
   *qb = n / 2;
   *sb = n / 16;

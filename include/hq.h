@@ -309,7 +309,8 @@ HQ_API hq_status hq_selftest_bounded_wait(int unit, hq_stream stream);
  */
 typedef struct hq_host_pipeline hq_host_pipeline;
 
-/* Device workspace bytes for M x K tensors of `dtype` (0 if the sizes are invalid). */
+/* Device workspace bytes for M x K tensors of `dtype`.  0 if the sizes are invalid: M or K not
+ * positive, K not a multiple of 16, K >= 2^36, or more than 2^58 elements. */
 HQ_API size_t hq_host_pipeline_workspace_bytes(int64_t M, int64_t K, hq_dtype dtype);
 
 /* Create a pipeline for M x K row-major tensors (contiguous rows) and rotation `group`. */

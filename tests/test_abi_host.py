@@ -173,6 +173,9 @@ def test_host_pipeline_argument_checks(lib):
     assert lib.hq_host_pipeline_workspace_bytes(0, 32, 1) == 0
     assert lib.hq_host_pipeline_workspace_bytes(4, 24, 1) == 0
     assert lib.hq_host_pipeline_workspace_bytes(4, 32, 7) == 0
+    assert lib.hq_host_pipeline_workspace_bytes(2 ** 40, 2 ** 22, 0) == 0   # bytes would wrap
+    assert lib.hq_host_pipeline_workspace_bytes(1, 2 ** 36, 1) == 0        # row too long
+    assert lib.hq_host_pipeline_create(1, 2 ** 36, 1, 16, P(FAKE), 2 ** 40, ref) == 2
     need = lib.hq_host_pipeline_workspace_bytes(4, 32, 1)
     assert need > 2 * (4 * 32 * 2)
     assert lib.hq_host_pipeline_create(4, 32, 1, 16, None, need, ref) == 1
