@@ -85,9 +85,10 @@ hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t
   if (dtype != HQ_F32 && dtype != HQ_BF16) return HQ_ERR_DTYPE;
   if (group != 16 && group != 64 && group != 256) return HQ_ERR_GROUP;
   if (M < 0 || K < 0 || ldx < K || K % group != 0 || K > hq::kI8MaxK) return HQ_ERR_SHAPE;
+  const int64_t es = dtype == HQ_BF16 ? 2 : 4;
+  if ((K > 0 && M > INT64_MAX / K) || ldx > INT64_MAX / es) return HQ_ERR_SHAPE;
   if (M == 0 || K == 0) return HQ_OK;
   if (!x || !q || !scales) return HQ_ERR_NULL;
-  const int64_t es = dtype == HQ_BF16 ? 2 : 4;
   if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scales, 4)) return HQ_ERR_ALIGN;
   if (M > 1 && (ldx * es) % 16 != 0) return HQ_ERR_ALIGN;
   hq::I8Params p = {};

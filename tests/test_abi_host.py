@@ -215,6 +215,7 @@ def test_int8_argument_checks(lib):
     assert i8(ldx=32) == 2 and i8(M=-1) == 2
     assert i8(x=FAKE + 8) == 3 and i8(q=FAKE + 4) == 3 and i8(s=FAKE + 2) == 3
     assert i8(ldx=68) == 3                     # 136-byte bf16 row stride
+    assert i8(M=2 ** 62) == 2 and i8(ldx=2 ** 62) == 2   # M*K, ldx*2 overflow int64
     assert i8(M=0) == 0
 
 
