@@ -383,9 +383,10 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
 
 int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K) {
   if (M < 0 || K < 0 || K % 16 != 0) return -1;
-  const int64_t rows = (M + 127) / 128 * 128;
+  const int64_t row_tiles = M / 128 + (M % 128 != 0);
   const int64_t cols = (K / 16 + 3) / 4 * 4;
-  return rows * cols;
+  if (cols > 0 && row_tiles > INT64_MAX / 128 / cols) return -1;
+  return row_tiles * 128 * cols;
 }
 
 hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t M, int64_t K,

@@ -169,8 +169,8 @@ HQ_API hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, i
                                                 const float* amax, uint8_t* q, uint8_t* scales,
                                                 float* s_global, hq_stream stream);
 
-/* Size in bytes of the swizzled scale buffer for an [M, K] tensor (-1 if M < 0, K < 0 or
- * K % 16 != 0). */
+/* Size in bytes of the swizzled scale buffer for an [M, K] tensor (-1 if M < 0, K < 0,
+ * K % 16 != 0, or the size does not fit int64). */
 HQ_API int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K);
 
 /*

@@ -250,6 +250,9 @@ def test_swizzled_argument_checks_and_size(lib):
     assert lib.hq_swizzled_scales_bytes(32768, 28672) == 32768 * 1792
     assert lib.hq_swizzled_scales_bytes(0, 0) == 0
     assert lib.hq_swizzled_scales_bytes(4, 24) == -1 and lib.hq_swizzled_scales_bytes(-1, 16) == -1
+    assert lib.hq_swizzled_scales_bytes(2 ** 63 - 1, 16) == -1       # would overflow int64
+    assert lib.hq_swizzled_scales_bytes(2 ** 40, 2 ** 30) == -1
+    assert lib.hq_swizzled_scales_bytes(2 ** 40, 64) == 2 ** 40 * 4  # the largest are exact
 
 
 def test_selftest_argument_check(lib):
