@@ -74,3 +74,17 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_table_aliases_point_at_captures():
+    # A source listed as running the captured kernels must map to a source that has a capture,
+    # and never to itself; the profile summaries name the captured source.
+    sys.path.insert(0, ROOT)
+    import bench
+
+    captured = {key[0] for key in bench.NCU_TRAFFIC}
+    for later, source in bench.SAME_KERNELS_AS.items():
+        assert source in captured and later not in captured and later != source
+    profiles = os.path.join(ROOT, "profiles")
+    text = "".join(open(os.path.join(profiles, f)).read() for f in os.listdir(profiles))
+    assert all(source in text for source in captured)
