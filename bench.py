@@ -48,20 +48,8 @@ L2_BYTES = 126 * 1024 * 1024
 # workload itself (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the kernel source
 # it was taken on: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/k_rotate_quant_nvfp4_g16_bf16.md: 1.879112 GB read + 0.497741 GB written
     ("013b7eb4bf9db83f", "bf16_32768x28672", 16): 1879111680 + 497740800,
-    # profiles/k_quant_nvfp4_fused_g16_bf16.md: 33.610 MB read, nothing written back yet
     ("013b7eb4bf9db83f", "bf16_4096x4096", 16): 33609984 + 0,
-}
-# Later sources whose every difference from a captured one is host code that runs before any
-# launch (so the kernels, their launch configurations and their traffic are the captured ones).
-SAME_KERNELS_AS = {
-    # hq.cu: check_x refuses K >= 2^36 (HQ_ERR_SHAPE), so base_params no longer clamps K/16
-    "6b929af7aee0bc2f": "013b7eb4bf9db83f",
-    # and hq_quantize_nvfp4 checks q, scales and s_global before it enqueues pass 1
-    "94e8bcdf12bb41d7": "013b7eb4bf9db83f",
-    # and hq_swizzled_scales_bytes returns -1 for a size beyond int64
-    "c8d430362acf2a5a": "013b7eb4bf9db83f",
 }
 
 
@@ -96,6 +84,8 @@ def parse_args():
     ap.add_argument("--group", type=int, default=None, help="rotation group (default: the workload's first)")
     ap.add_argument("--e2e-steps", type=int, default=None, help="steps of the host-buffer run (default: min(steps, 200))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload measurements reported under 'configs'")
     ap.add_argument("--rows", type=int, default=None,
                     help="only the first ROWS rows of the workload (same K, distribution and "
                          "seed): small cases of the same row shape for profiling; not a metric line")
@@ -288,6 +278,100 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------------- GPU arm -----
 
+def _median_ms(fn_batch, reps: int) -> float:
+    """Median over `reps` runs of fn_batch(), which returns milliseconds per launch."""
+    return statistics.median(fn_batch() for _ in range(reps))
+
+
+def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: int = 200,
+                    reps: int = 5) -> dict:
+    """Every named workload and rotation mode, timed the same way: pass 2 alone, pass 1 alone and
+    the whole step (hq_quantize_nvfp4 with a workspace), each as `launches` launches back to
+    back between two CUDA events on the launching stream, median of `reps` such runs.
+
+    Inputs larger than L2 are read from HBM by construction.  For an input that L2 holds, the
+    launches cycle through enough copies of x and of the outputs that each launch reads an x
+    last touched at least three L2 capacities earlier; the same kernels are also timed cold, one
+    launch per event pair after an L2 flush (the flush outside the pair), which adds the launch
+    latency to every figure.  `have` maps workload names to device tensors already made."""
+    import torch
+
+    out = {}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for name in synth.WORKLOAD_ORDER:
+        w = synth.WORKLOADS[name]
+        x0 = have.get(name)
+        if x0 is None:
+            x0 = synth.generate(w).to(dev)
+        bin_, bout = w.bytes_in(), w.bytes_out()
+        nb = bin_ + bout
+        small = nb < 2 * L2_BYTES
+        copies = 1
+        if small and nb >= (8 << 20):
+            copies = min(64, -(-3 * L2_BYTES // nb) + 1)
+        xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+        qs = [torch.empty((w.M, w.K // 2), dtype=torch.uint8, device=dev) for _ in range(copies)]
+        ss = [torch.empty((w.M, w.K // 16), dtype=torch.uint8, device=dev) for _ in range(copies)]
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        a1 = torch.empty(1, dtype=torch.float32, device=dev)
+        sg = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
+        entry = {"workload": w.describe(), "M": w.M, "K": w.K, "input_dtype": w.dtype,
+                 "bytes_per_step": nb,
+                 "timing": ("inputs larger than L2, back to back" if not small else
+                            (f"back to back over {copies} copies of x and the outputs "
+                             f"({copies * nb / 1e6:.0f} MB), no flush; cold: L2 flushed before "
+                             "each launch, one event pair per launch" if copies > 1 else
+                             "cold only: L2 flushed before each launch, one event pair per launch")),
+                 "groups": {}}
+        for group in w.groups:
+            hq.hq_rot_amax(x0, group, amax=amax, stream=stream)
+            i = [0]
+
+            def nxt():
+                k = i[0] % copies
+                i[0] += 1
+                return k
+
+            def p2():
+                k = nxt()
+                hq.hq_rotate_quant_nvfp4(xs[k], group, amax, q=qs[k], scales=ss[k], s_global=sg,
+                                         stream=stream)
+
+            def p1():
+                hq.hq_rot_amax(xs[nxt()], group, amax=a1, stream=stream)
+
+            def st():
+                k = nxt()
+                hq.hq_quantize_nvfp4(xs[k], group, amax=a1, q=qs[k], scales=ss[k], s_global=sg,
+                                     fused=True, workspace=ws, stream=stream)
+
+            g = {}
+            for key, fn in (("pass2", p2), ("pass1", p1), ("step", st)):
+                if copies > 1 or not small:
+                    g[f"{key}_ms"] = _median_ms(lambda: time_launches(fn, launches, stream, dev, None), reps)
+                if small:
+                    g[f"{key}_cold_ms"] = time_launches(fn, 50, stream, dev, flush)
+            for suffix in ("", "_cold"):
+                if f"pass2{suffix}_ms" not in g:
+                    continue
+                p2ms, p1ms, stms = (g[f"pass2{suffix}_ms"], g[f"pass1{suffix}_ms"], g[f"step{suffix}_ms"])
+                g[f"pass2{suffix}_gbs"] = nb / (p2ms / 1e3) / 1e9
+                g[f"pass2{suffix}_frac_of_peak"] = g[f"pass2{suffix}_gbs"] / peak
+                g[f"pass2{suffix}_frac_of_nominal_8000"] = g[f"pass2{suffix}_gbs"] / 8000.0
+                g[f"pass1{suffix}_gbs_read"] = bin_ / (p1ms / 1e3) / 1e9
+                g[f"step{suffix}_gbs"] = nb / (stms / 1e3) / 1e9
+                g[f"step{suffix}_gbs_both_reads"] = (2 * bin_ + bout) / (stms / 1e3) / 1e9
+            g["step_path"] = ("one cooperative kernel" if bin_ <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
+                              else "pass 1 then pass 2, two launches")
+            entry["groups"]["off" if group == 0 else str(group)] = g
+        out[name] = entry
+        del xs, qs, ss, x0
+        torch.cuda.empty_cache()
+    return out
+
+
+
 def run_ours(args, w):
     import torch
 
@@ -325,10 +409,11 @@ def run_ours(args, w):
     if bytes_in + bytes_out < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # The step is one hq_quantize_nvfp4 call: for an x of at most 64 MiB one cooperative
-    # kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two launches.
+    # The step is one hq_quantize_nvfp4 call with a workspace: for an x of at most 64 MiB one
+    # cooperative kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two
+    # launches, pass 1 reducing into the workspace (no memset before it).
     fused = bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
-    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev) if fused else None
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
 
     def pass1():
         hq.hq_rot_amax(x, group, amax=amax, stream=stream)
@@ -337,7 +422,7 @@ def run_ours(args, w):
         hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
 
     def step():
-        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
+        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, fused=True,
                              workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
@@ -451,6 +536,15 @@ def run_ours(args, w):
                 "note": "hq_rotate_quant_int8 (x read once, int8 codes + fp32 per-row scales)"}
         del q8, s8
 
+    # ---- every named workload, the same measurement each ----
+    configs = None
+    if not args.no_configs:
+        csampler = ClockSampler(device_uuid(dev))
+        csampler.start()
+        time.sleep(0.3)
+        configs = measure_configs(hq, synth, dev, stream, load_peaks()[0], {w.name: x})
+        configs["clocks"] = csampler.stop()
+
     # ---- end to end through the public API, host buffers ----
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
     del q, s  # the host pipeline holds its own device buffers
@@ -484,11 +578,10 @@ def run_ours(args, w):
     dom_ms = step_ms if fused else p2
     achieved = step_bytes / (dom_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
-    captured_on = SAME_KERNELS_AS.get(src_hash, src_hash)
-    traffic = NCU_TRAFFIC.get((captured_on, w.name, group))
+    traffic = NCU_TRAFFIC.get((src_hash, w.name, group))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "traffic_kernel_source": captured_on if traffic is not None else None,
+                "traffic_kernel_source": src_hash if traffic is not None else None,
                 "kernel": "k_quant_nvfp4_fused" if fused else "k_rotate_quant_nvfp4",
                 "peak_source": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
@@ -527,6 +620,7 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": hqz.d2h_bytes, "steps": e2e_steps,
                 "ms_per_step": e2e_ms / e2e_steps, "api": "HostQuantizer (hq_host_pipeline_*)",
                 "timer": "host clock, wait() at the end"},
+        "configs": configs,
         "gpu_launches": K if fused else 2 * K,
         "clocks": clocks,
         "kernel_source": src_hash,

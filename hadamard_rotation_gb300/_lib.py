@@ -14,6 +14,8 @@ HQ_ERR_ALIGN = 3
 HQ_ERR_DTYPE = 4
 HQ_ERR_GROUP = 5
 HQ_ERR_CUDA = 6
+HQ_ERR_TOO_LARGE = 7
+HQ_ERR_ALIAS = 8
 
 HQ_F32 = 0
 HQ_BF16 = 1
@@ -81,6 +83,8 @@ def load() -> ctypes.CDLL:
         lib.hq_host_pipeline_wait.restype = i32
         lib.hq_host_pipeline_destroy.argtypes = [p]
         lib.hq_host_pipeline_destroy.restype = i32
+        lib.hq_host_pipeline_inject_failure.argtypes = [p, i32]
+        lib.hq_host_pipeline_inject_failure.restype = i32
         lib.hq_read_fault.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         lib.hq_read_fault.restype = i32
         lib.hq_quantize_nvfp4_host_noalloc.argtypes = [p, i32, i64, i64, i32, p, p, p, p]

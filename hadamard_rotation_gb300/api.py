@@ -364,6 +364,13 @@ class HostQuantizer:
         self.wait()
         return self.q_host, self.s_host, float(self.sg_host[0])
 
+    def inject_failure(self, step: int) -> None:
+        """Test of the failure handling (hq_host_pipeline_inject_failure): the next submit()
+        behaves as if the CUDA runtime refused its step ``step`` (0 input copy, 1 pass 1, 2 pass 2,
+        3 output transfer); nothing on the device fails."""
+        check(_lib.load().hq_host_pipeline_inject_failure(self._handle, step),
+              "hq_host_pipeline_inject_failure")
+
     def close(self) -> None:
         if getattr(self, "_handle", None):
             check(_lib.load().hq_host_pipeline_destroy(self._handle), "hq_host_pipeline_destroy")

@@ -55,6 +55,50 @@ hq_status hq::cuda_fail(cudaError_t e) {
 
 namespace {
 
+// cuCtxGetCurrent and cuCtxGetId, reached through the runtime's driver entry points (so the
+// library needs no link against the driver library).  CUcontext is an opaque pointer and
+// CUresult an int enum whose success value is 0.
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+
+struct DriverCtxCalls {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverCtxCalls& driver_ctx_calls() {
+  static const DriverCtxCalls calls = [] {
+    DriverCtxCalls c;
+    auto lookup = [](const char* name) -> void* {
+      void* f = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess) {
+        cudaGetLastError();  // a failed lookup leaves no error behind for the caller's next call
+        return nullptr;
+      }
+      return q == cudaDriverEntryPointSuccess ? f : nullptr;
+    };
+    c.get_current = reinterpret_cast<CtxGetCurrentFn>(lookup("cuCtxGetCurrent"));
+    c.get_id = reinterpret_cast<CtxGetIdFn>(lookup("cuCtxGetId"));
+    return c;
+  }();
+  return calls;
+}
+
+}  // namespace
+
+unsigned long long hq::context_id() {
+  const DriverCtxCalls& c = driver_ctx_calls();
+  if (!c.get_current || !c.get_id) return 0;
+  void* ctx = nullptr;
+  if (c.get_current(&ctx) != 0 || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (c.get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+namespace {
+
 using hq::cuda_fail;
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -73,12 +117,15 @@ hq::FastDiv make_fast_div(uint32_t d) {
   return f;
 }
 
-// Resident CTAs per SM for a kernel, and the SM count, cached per device.
+// Resident CTAs per SM for a kernel, cached per device and context (the dynamic
+// shared-memory attribute set below belongs to the context: after cudaDeviceReset it is
+// set again), and the SM count, cached per device.
 struct GridCache {
   std::mutex mu;
   static constexpr int kSlots = 128;
   const void* fn[kSlots] = {};
   int dev[kSlots] = {};
+  unsigned long long ctx[kSlots] = {};
   int ctas[kSlots] = {};
   int n = 0;
   int sms[64] = {};
@@ -89,11 +136,13 @@ cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, size_t smem, unsig
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long ctx = hq::context_id();
   int per_sm = 0, sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_grid.mu);
     for (int i = 0; i < g_grid.n; ++i)
-      if (g_grid.fn[i] == fn && g_grid.dev[i] == dev) per_sm = g_grid.ctas[i];
+      if (g_grid.fn[i] == fn && g_grid.dev[i] == dev && ctx != 0 && g_grid.ctx[i] == ctx)
+        per_sm = g_grid.ctas[i];
     if (dev >= 0 && dev < 64) sms = g_grid.sms[dev];
   }
   if (sms == 0) {
@@ -111,12 +160,20 @@ cudaError_t persistent_grid(const void* fn, uint64_t n_tiles, size_t smem, unsig
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, hq::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    std::lock_guard<std::mutex> lock(g_grid.mu);
-    if (g_grid.n < GridCache::kSlots) {
-      g_grid.fn[g_grid.n] = fn;
-      g_grid.dev[g_grid.n] = dev;
-      g_grid.ctas[g_grid.n] = per_sm;
-      ++g_grid.n;
+    // The calls above made a context current if none was: key the entry on it.
+    const unsigned long long now = ctx != 0 ? ctx : hq::context_id();
+    if (now != 0) {
+      std::lock_guard<std::mutex> lock(g_grid.mu);
+      int slot = -1;
+      for (int i = 0; i < g_grid.n; ++i)
+        if (g_grid.fn[i] == fn && g_grid.dev[i] == dev) slot = i;  // an older context's entry
+      if (slot < 0 && g_grid.n < GridCache::kSlots) slot = g_grid.n++;
+      if (slot >= 0) {
+        g_grid.fn[slot] = fn;
+        g_grid.dev[slot] = dev;
+        g_grid.ctx[slot] = now;
+        g_grid.ctas[slot] = per_sm;
+      }
     }
   }
   const uint64_t want = (n_tiles + hq::kWarpsPerCta - 1) / hq::kWarpsPerCta;
@@ -431,7 +488,8 @@ hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M
   if (!amax_next) return HQ_ERR_NULL;
   if (!aligned(amax_next, 4)) return HQ_ERR_ALIGN;
   if (M > 0 && K > 0) {
-    if (!amax_prev || !q || !scales || amax_prev == amax_next) return HQ_ERR_NULL;
+    if (!amax_prev || !q || !scales) return HQ_ERR_NULL;
+    if (amax_prev == amax_next) return HQ_ERR_ALIAS;
     if (!aligned(amax_prev, 4) || !aligned(q, 16) || !aligned(scales, 4) ||
         (s_global && !aligned(s_global, 4)))
       return HQ_ERR_ALIGN;
@@ -552,6 +610,7 @@ const char* hq_status_string(hq_status status) {
     case HQ_ERR_CUDA: return "HQ_ERR_CUDA: CUDA runtime error";
     case HQ_ERR_TOO_LARGE:
       return "HQ_ERR_TOO_LARGE: tensor exceeds the fixed scratch of the allocation-free entry point";
+    case HQ_ERR_ALIAS: return "HQ_ERR_ALIAS: two buffers that must be distinct are the same";
   }
   return "unknown hq_status";
 }

@@ -47,6 +47,8 @@ struct hq_host_pipeline {
   uint64_t submitted = 0;
   bool pageable_writable = false;  // the device writes pageable host memory through the host page tables
   int copy_out_ctas = 0;
+  int broken_error = 0;  // the cudaError_t of a submission that failed after enqueueing work
+  int inject_step = -1;  // hq_host_pipeline_inject_failure: the step the next submission fails at
 };
 
 namespace {
@@ -202,56 +204,76 @@ hq_status hq_host_pipeline_create(int64_t M, int64_t K, hq_dtype dtype, int grou
 hq_status hq_host_pipeline_submit(hq_host_pipeline* p, const void* x_host, uint8_t* q_host,
                                   uint8_t* scales_host, float* s_global_host) {
   if (!p || !x_host || !q_host || !scales_host || !s_global_host) return HQ_ERR_NULL;
+  if (p->broken_error != 0) return fail(static_cast<cudaError_t>(p->broken_error));
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(e);
   if (dev != p->device && (e = cudaSetDevice(p->device)) != cudaSuccess) return fail(e);
   auto& s = p->slot[p->submitted & 1];
+  // A refused step (or the injected one) ends the submission.  Steps 0..3: input copy, pass 1,
+  // pass 2, output transfer.
+  const int inject = p->inject_step;
+  p->inject_step = -1;
   hq_status st = HQ_OK;
+  bool enqueued = false;  // some work of this submission is on a stream
+  auto injected = [&](int step) {
+    if (st == HQ_OK && step == inject) st = fail(cudaErrorNotPermitted);
+    return st != HQ_OK;
+  };
   // input copy: the slot's x must no longer be read by an earlier pass 2
-  if (s.used && (e = cudaStreamWaitEvent(p->in, s.compute_done, 0)) != cudaSuccess) st = fail(e);
-  if (st == HQ_OK &&
-      (e = cudaMemcpyAsync(s.x, x_host, p->x_bytes, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
-    st = fail(e);
-  if (st == HQ_OK && (e = cudaEventRecord(s.in_done, p->in)) != cudaSuccess) st = fail(e);
-  // both passes: after the input arrived and after the slot's last outputs left
-  if (st == HQ_OK && (e = cudaStreamWaitEvent(p->compute, s.in_done, 0)) != cudaSuccess)
-    st = fail(e);
-  if (st == HQ_OK && s.used && (e = cudaStreamWaitEvent(p->compute, s.out_done, 0)) != cudaSuccess)
-    st = fail(e);
-  if (st == HQ_OK)
-    st = hq_rot_amax(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, nullptr, p->compute);
-  if (st == HQ_OK)
-    st = hq_rotate_quant_nvfp4(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, s.q, s.s,
-                               s.sglobal, p->compute);
-  if (st == HQ_OK && (e = cudaEventRecord(s.compute_done, p->compute)) != cudaSuccess)
-    st = fail(e);
-  // outputs to the host: stored by a kernel where the device can write the buffers,
-  // otherwise copied
-  if (st == HQ_OK && (e = cudaStreamWaitEvent(p->out, s.compute_done, 0)) != cudaSuccess)
-    st = fail(e);
-  void* qv = device_view(q_host, p->pageable_writable);
-  void* sv = device_view(scales_host, p->pageable_writable);
-  void* gv = device_view(s_global_host, p->pageable_writable);
-  if (st == HQ_OK && qv && sv && gv) {
-    k_copy_out<<<p->copy_out_ctas, 512, 0, p->out>>>(s.q, static_cast<uint8_t*>(qv), p->q_bytes, s.s,
-                                                     static_cast<uint8_t*>(sv), p->s_bytes, s.sglobal,
-                                                     static_cast<float*>(gv));
-    if ((e = cudaGetLastError()) != cudaSuccess) st = fail(e);
-  } else if (st == HQ_OK) {
-    if ((e = cudaMemcpyAsync(q_host, s.q, p->q_bytes, cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+  if (!injected(0)) {
+    if (s.used && (e = cudaStreamWaitEvent(p->in, s.compute_done, 0)) != cudaSuccess) st = fail(e);
+    if (st == HQ_OK &&
+        (e = cudaMemcpyAsync(s.x, x_host, p->x_bytes, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
       st = fail(e);
-    if (st == HQ_OK && (e = cudaMemcpyAsync(scales_host, s.s, p->s_bytes, cudaMemcpyDeviceToHost,
-                                            p->out)) != cudaSuccess)
+    if (st == HQ_OK) enqueued = true;
+    if (st == HQ_OK && (e = cudaEventRecord(s.in_done, p->in)) != cudaSuccess) st = fail(e);
+    // both passes: after the input arrived and after the slot's last outputs left
+    if (st == HQ_OK && (e = cudaStreamWaitEvent(p->compute, s.in_done, 0)) != cudaSuccess)
       st = fail(e);
-    if (st == HQ_OK && (e = cudaMemcpyAsync(s_global_host, s.sglobal, sizeof(float),
-                                            cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+    if (st == HQ_OK && s.used && (e = cudaStreamWaitEvent(p->compute, s.out_done, 0)) != cudaSuccess)
       st = fail(e);
   }
-  if (st == HQ_OK && (e = cudaEventRecord(s.out_done, p->out)) != cudaSuccess) st = fail(e);
+  if (!injected(1))
+    st = hq_rot_amax(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, nullptr, p->compute);
+  if (!injected(2)) {
+    st = hq_rotate_quant_nvfp4(s.x, p->dtype, p->M, p->K, p->K, p->group, s.amax, s.q, s.s,
+                               s.sglobal, p->compute);
+    if (st == HQ_OK && (e = cudaEventRecord(s.compute_done, p->compute)) != cudaSuccess)
+      st = fail(e);
+  }
+  // outputs to the host: stored by a kernel where the device can write the buffers,
+  // otherwise copied
+  if (!injected(3)) {
+    if ((e = cudaStreamWaitEvent(p->out, s.compute_done, 0)) != cudaSuccess) st = fail(e);
+    void* qv = device_view(q_host, p->pageable_writable);
+    void* sv = device_view(scales_host, p->pageable_writable);
+    void* gv = device_view(s_global_host, p->pageable_writable);
+    if (st == HQ_OK && qv && sv && gv) {
+      k_copy_out<<<p->copy_out_ctas, 512, 0, p->out>>>(s.q, static_cast<uint8_t*>(qv), p->q_bytes,
+                                                       s.s, static_cast<uint8_t*>(sv), p->s_bytes,
+                                                       s.sglobal, static_cast<float*>(gv));
+      if ((e = cudaGetLastError()) != cudaSuccess) st = fail(e);
+    } else if (st == HQ_OK) {
+      if ((e = cudaMemcpyAsync(q_host, s.q, p->q_bytes, cudaMemcpyDeviceToHost, p->out)) !=
+          cudaSuccess)
+        st = fail(e);
+      if (st == HQ_OK && (e = cudaMemcpyAsync(scales_host, s.s, p->s_bytes,
+                                              cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+        st = fail(e);
+      if (st == HQ_OK && (e = cudaMemcpyAsync(s_global_host, s.sglobal, sizeof(float),
+                                              cudaMemcpyDeviceToHost, p->out)) != cudaSuccess)
+        st = fail(e);
+    }
+    if (st == HQ_OK && (e = cudaEventRecord(s.out_done, p->out)) != cudaSuccess) st = fail(e);
+  }
   if (st == HQ_OK) {
     s.used = true;
     ++p->submitted;
+  } else if (enqueued) {
+    // The slot's events may not cover what is in flight: no later submission may reuse it.
+    p->broken_error = hq_last_cuda_error();
+    if (p->broken_error == 0) p->broken_error = static_cast<int>(cudaErrorUnknown);
   }
   if (dev != p->device) cudaSetDevice(dev);
   return st;
@@ -265,6 +287,13 @@ hq_status hq_host_pipeline_wait(hq_host_pipeline* p) {
   if (e != cudaSuccess) return fail(e);
   e = cudaStreamSynchronize(p->in);
   if (e != cudaSuccess) return fail(e);
+  return HQ_OK;
+}
+
+hq_status hq_host_pipeline_inject_failure(hq_host_pipeline* p, int step) {
+  if (!p) return HQ_ERR_NULL;
+  if (step > 3) return HQ_ERR_SHAPE;
+  p->inject_step = step < 0 ? -1 : step;
   return HQ_OK;
 }
 

@@ -29,18 +29,23 @@ constexpr size_t kAlign = 256;
 
 std::mutex g_scratch_mu;
 uint8_t* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
 size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Device address of the scratch array on device `dev` (which must be current).
-// The first call for a device looks the address up; later calls reuse it.
+// The first call in a context looks the address up; later calls in the same context reuse
+// it.  After cudaDeviceReset the device's context is a new one, where the array has to be
+// looked up again: the cache is keyed on the context's unique ID (0 = unknown, never cached).
 cudaError_t scratch_on(int dev, uint8_t** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const unsigned long long ctx = hq::context_id();
+  if (ctx == 0 || g_scratch_ctx[dev] != ctx || g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_hq_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+    g_scratch_ctx[dev] = hq::context_id();  // the lookup made a context current if none was
   }
   *out = g_scratch_addr[dev];
   return cudaSuccess;

@@ -58,7 +58,7 @@ extern "C" {
 
 typedef enum {
   HQ_OK = 0,
-  HQ_ERR_NULL = 1,  /* a required pointer is NULL (or two that must differ are the same) */
+  HQ_ERR_NULL = 1,  /* a required pointer is NULL */
   HQ_ERR_SHAPE = 2, /* M < 0, K < 0, ldx < K, K not a multiple of max(16, G), M * K beyond
                        int64, or, in the calls that read x, K >= 2^36 (a row of 2^32 or
                        more 16-element blocks) */
@@ -66,8 +66,9 @@ typedef enum {
   HQ_ERR_DTYPE = 4, /* unknown element type */
   HQ_ERR_GROUP = 5, /* rotation group not in {0, 16, 256} */
   HQ_ERR_CUDA = 6,  /* the CUDA runtime refused a launch or an enqueue */
-  HQ_ERR_TOO_LARGE = 7 /* the tensor does not fit the fixed scratch of
-                          hq_quantize_nvfp4_host_noalloc */
+  HQ_ERR_TOO_LARGE = 7, /* the tensor does not fit the fixed scratch of
+                           hq_quantize_nvfp4_host_noalloc */
+  HQ_ERR_ALIAS = 8      /* two buffers that must be distinct are the same */
 } hq_status;
 
 typedef enum {
@@ -188,7 +189,7 @@ HQ_API int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K);
  *
  *   x, dtype, M, K, ldx, group, q, scales, s_global : as for hq_rotate_quant_nvfp4.
  *   amax_prev : 1 float on the device (read).      amax_next : 1 float on the device (written).
- *   The two must be different floats; passing the same pointer returns HQ_ERR_NULL.
+ *   The two must be different floats; passing the same pointer returns HQ_ERR_ALIAS.
  */
 HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M,
                                                int64_t K, int64_t ldx, int group,
@@ -320,7 +321,11 @@ HQ_API hq_status hq_host_pipeline_create(int64_t M, int64_t K, hq_dtype dtype, i
 
 /* Enqueue one quantization and return at once.  x_host: [M, K] of dtype; q_host: [M, K/2] bytes;
  * scales_host: [M, K/16] bytes; s_global_host: 1 float.  Results are complete after
- * hq_host_pipeline_wait(). */
+ * hq_host_pipeline_wait().
+ * If a step fails after part of the submission was enqueued (HQ_ERR_CUDA), the buffer set's
+ * ordering events may not cover the work in flight, so the pipeline refuses every later
+ * submission with HQ_ERR_CUDA (hq_last_cuda_error() gives the first failure); wait for it and
+ * destroy it.  A submission refused before anything was enqueued (HQ_ERR_NULL) leaves it usable. */
 HQ_API hq_status hq_host_pipeline_submit(hq_host_pipeline* p, const void* x_host, uint8_t* q_host,
                                          uint8_t* scales_host, float* s_global_host);
 
@@ -329,6 +334,14 @@ HQ_API hq_status hq_host_pipeline_wait(hq_host_pipeline* p);
 
 /* Wait for outstanding work, then release the streams, events and the object (NULL is a no-op). */
 HQ_API hq_status hq_host_pipeline_destroy(hq_host_pipeline* p);
+
+/* hq_host_pipeline_inject_failure -- a test of the failure handling above, not part of the
+ * quantization path (the pages have no counterpart).  The next submission to `p` behaves as if
+ * the CUDA runtime refused its step `step` (0 the input copy, 1 pass 1, 2 pass 2, 3 the output
+ * transfer): that step and the ones after it are not enqueued, the submission returns
+ * HQ_ERR_CUDA with cudaErrorNotPermitted recorded, and the steps before it stay enqueued.
+ * Nothing on the device fails.  step < 0 cancels a pending injection; step > 3: HQ_ERR_SHAPE. */
+HQ_API hq_status hq_host_pipeline_inject_failure(hq_host_pipeline* p, int step);
 
 /*
  * hq_quantize_nvfp4_host_noalloc -- the quantization of one host tensor with no device
@@ -350,7 +363,9 @@ HQ_API hq_status hq_host_pipeline_destroy(hq_host_pipeline* p);
  *   (about 13.1 million bf16 or 7.35 million fp32 elements).  Larger tensors return
  *   HQ_ERR_TOO_LARGE before anything is enqueued.
  *   Set-up: the first call on a device looks up the array's device address (once per device,
- *   with that device current), so make that first call before any stream capture.
+ *   with that device current), so make that first call before any stream capture.  The address
+ *   belongs to the device's context: after cudaDeviceReset the next call looks it up again (and
+ *   is then a first call again).
  *   Sharing: every call on a device uses the same array and leaves its contents there; calls
  *   whose work overlaps on the GPU (other streams, other host threads) race on it, so order
  *   them (one stream, or events).  The call clears what must start at zero (the amax).

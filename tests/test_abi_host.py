@@ -53,7 +53,7 @@ def test_header_compiles_as_c(tmp_path):
 
 def test_version_and_status_strings(lib):
     assert lib.hq_version() >= 100
-    for code in range(7):
+    for code in range(9):
         assert lib.hq_status_string(code).decode().startswith("HQ_")
     assert b"unknown" in lib.hq_status_string(99)
     assert lib.hq_last_cuda_error() == 0
@@ -189,6 +189,7 @@ def test_host_pipeline_argument_checks(lib):
     assert lib.hq_host_pipeline_submit(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE)) == 1
     assert lib.hq_host_pipeline_wait(None) == 1
     assert lib.hq_host_pipeline_destroy(None) == 0
+    assert lib.hq_host_pipeline_inject_failure(None, 1) == 1
 
 
 def test_delayed_argument_checks(lib):
@@ -199,7 +200,7 @@ def test_delayed_argument_checks(lib):
             P(sg) if sg else None, None)
     assert dl(nxt=0) == 1
     assert dl(prev=0) == 1 and dl(q=0) == 1 and dl(s=0) == 1
-    assert dl(prev=FAKE + 64) == 1        # the two amax pointers alias
+    assert dl(prev=FAKE + 64) == 8        # the two amax pointers alias: HQ_ERR_ALIAS
     assert dl(G=32) == 5 and dl(dt=3) == 4 and dl(K=24, ldx=24) == 2
     assert dl(nxt=FAKE + 66) == 3 and dl(q=FAKE + 8) == 3
 
@@ -266,7 +267,8 @@ def test_binding_has_every_abi_call_under_the_same_name():
     import hadamard_rotation_gb300 as hq
 
     wrapped_elsewhere = {"hq_host_pipeline_create", "hq_host_pipeline_destroy", "hq_host_pipeline_submit",
-                         "hq_host_pipeline_wait", "hq_host_pipeline_workspace_bytes", "hq_last_cuda_error"}
+                         "hq_host_pipeline_wait", "hq_host_pipeline_workspace_bytes",
+                         "hq_host_pipeline_inject_failure", "hq_last_cuda_error"}
     missing = [n for n in declared_functions() if n not in wrapped_elsewhere and not callable(getattr(hq, n, None))]
     assert not missing, missing
     assert hq.hq_version() == 100

@@ -76,15 +76,18 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_traffic_table_aliases_point_at_captures():
-    # A source listed as running the captured kernels must map to a source that has a capture,
-    # and never to itself; the profile summaries name the captured source.
+def test_traffic_table_keys_name_a_source_a_workload_and_a_group():
+    # Each captured traffic figure is keyed by the kernel source hash it was taken on (16 hex
+    # digits, the form kernel_source_hash() returns), a named workload and a rotation group, and
+    # is no larger than the bytes a launch could move if it read every input byte and wrote
+    # every output byte twice.
     sys.path.insert(0, ROOT)
     import bench
+    from hadamard_rotation_gb300 import synth
 
-    captured = {key[0] for key in bench.NCU_TRAFFIC}
-    for later, source in bench.SAME_KERNELS_AS.items():
-        assert source in captured and later not in captured and later != source
-    profiles = os.path.join(ROOT, "profiles")
-    text = "".join(open(os.path.join(profiles, f)).read() for f in os.listdir(profiles))
-    assert all(source in text for source in captured)
+    assert len(bench.kernel_source_hash()) == 16
+    for (source, name, group), traffic in bench.NCU_TRAFFIC.items():
+        assert len(source) == 16 and int(source, 16) >= 0
+        assert name in synth.WORKLOADS and group in synth.WORKLOADS[name].groups
+        w = synth.WORKLOADS[name]
+        assert 0 < traffic <= 2 * (w.bytes_in() + w.bytes_out())

@@ -1,7 +1,10 @@
-"""The paths bench.py times beside the metric's step, checked against the oracle on the bench
-tensor itself (bf16 [32768, 28672], the 1.88 GB LLM MLP-up-sized workload) in the launch
-configuration the bench uses.  The two-pass step on this tensor is test_workload_parity.
+"""The paths bench.py times, checked against the oracle on the bench tensor itself (bf16
+[32768, 28672], the 1.88 GB LLM MLP-up-sized workload) in the launch configuration the bench
+uses:
 
+  - the metric's step verbatim: hq_quantize_nvfp4 with a workspace, which on this tensor is the
+    streaming pass 1 reducing into the workspace (its last CTA writes amax) and pass 2, both
+    launched as programmatic dependents; twice in a row on one workspace;
   - delayed-amax single pass with the true amax: codes and scales equal pass 2's, the amax it
     reduces equals the tensor's;
   - pass 2 with swizzled scales: codes in full; the scales of sampled 128-row tiles (first,
@@ -41,6 +44,30 @@ def nvfp4_reference(bench_tensor):
 
 def f32_bits(a):
     return np.asarray(a, np.float32).view(np.uint32)
+
+
+def test_bench_step_twice_on_one_workspace(bench_tensor, nvfp4_reference):
+    _, x, _ = bench_tensor
+    oq, os_, oamax, osg = nvfp4_reference
+    M, K = x.shape
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    amax = torch.empty(1, dtype=torch.float32, device="cuda")
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M, K // 16), dtype=torch.uint8, device="cuda")
+    sg = torch.empty(1, dtype=torch.float32, device="cuda")
+    assert x.numel() * x.element_size() > hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES  # two launches
+    for call in range(2):
+        q.fill_(0xEE)
+        s.fill_(0xEE)
+        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, fused=True,
+                             workspace=ws)
+        torch.cuda.synchronize()
+        assert f32_bits(amax.cpu().numpy())[0] == f32_bits([oamax])[0], call
+        assert f32_bits(sg.cpu().numpy())[0] == f32_bits([osg])[0], call
+        assert np.array_equal(s.cpu().numpy(), os_), call
+        assert np.array_equal(q.cpu().numpy(), oq), call
+        assert not ws.any().item(), call         # the workspace is 0 again after every call
+    assert hq.hq_read_fault() == 0
 
 
 def test_delayed_single_pass(bench_tensor, nvfp4_reference):

@@ -289,6 +289,42 @@ def test_host_pipeline_output_buffers_of_any_kind(pinned_outputs):
     hqz.close()
 
 
+@pytest.mark.parametrize("step", [0, 1, 2, 3])
+def test_host_pipeline_refuses_submissions_after_a_partial_failure(step):
+    """A submission whose step `step` is refused (injected on the host: the device sees no
+    failure) returns HQ_ERR_CUDA.  Once part of it was enqueued (a refused pass 1, pass 2 or
+    output transfer), the pipeline refuses every later submission, since the buffer set's
+    events may not cover the work in flight; a refused input copy enqueued nothing and leaves it
+    usable.  The submissions before the failure still complete and equal the oracle."""
+    from hadamard_rotation_gb300._lib import HQ_ERR_CUDA, HQError
+
+    M, K = 256, 1024
+    hqz = hq.HostQuantizer(M, K, torch.bfloat16, 16)
+    x = rand_input(M, K, torch.bfloat16, seed=31).pin_memory()
+    first = [torch.empty((M, K // 2), dtype=torch.uint8, pin_memory=True),
+             torch.empty((M, K // 16), dtype=torch.uint8, pin_memory=True),
+             torch.empty(1, dtype=torch.float32, pin_memory=True)]
+    hqz.submit(x, *first)                       # a good submission before the failure
+    hqz.inject_failure(step)
+    with pytest.raises(HQError) as err:
+        hqz.submit(x)
+    assert err.value.status == HQ_ERR_CUDA
+    if step == 0:
+        hqz.submit(x)                           # nothing was enqueued: still usable
+    else:
+        with pytest.raises(HQError) as again:
+            hqz.submit(x)
+        assert again.value.status == HQ_ERR_CUDA
+    hqz.wait()
+    oq, os_, oamax, osg = oracle.quantize(synth.as_oracle_array(x), 16)
+    assert_bytes_equal("codes before the failure", first[0].numpy(), oq)
+    assert_bytes_equal("scales before the failure", first[1].numpy(), os_)
+    if step == 0:
+        assert_bytes_equal("codes after a refused copy", hqz.q_host.numpy(), oq)
+    hqz.close()
+    assert torch.cuda.synchronize() is None     # the context is still usable
+
+
 def test_host_quantizer_matches_oracle_on_a_workload():
     w = synth.WORKLOADS["bf16_4096x4096"]
     x_host = synth.generate(w).pin_memory()

@@ -46,3 +46,49 @@ def test_tiles_are_contiguous():
     buf = swizzle_scales(tile_of)
     for t in range(4):
         assert np.all(buf[t * 512:(t + 1) * 512] == t + 1)
+
+
+def torch_blocked_helpers():
+    """PyTorch's own statement of the layout, as Python source: ``to_blocked`` and
+    ``from_blocked`` in torch/testing/_internal/common_quantized.py, the helpers PyTorch's tests
+    use to feed block scales to ``torch._scaled_mm`` (their comments cite cuBLAS's "1D block
+    scaling factors layout").  ``to_blocked`` builds the layout with reshapes and a transpose;
+    ``from_blocked`` reads it back with the per-element offset formula.  The module itself
+    imports test-only packages, so the two functions (and their ``ceil_div``) are taken from its
+    source with ``ast`` and run on their own."""
+    import ast
+    import importlib.util
+
+    import torch
+
+    spec = importlib.util.find_spec("torch.testing._internal.common_quantized")
+    if spec is None or spec.origin is None:
+        pytest.skip("this torch has no common_quantized.py")
+    tree = ast.parse(open(spec.origin).read())
+    wanted = {"ceil_div", "to_blocked", "from_blocked"}
+    funcs = [n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name in wanted]
+    if {f.name for f in funcs} != wanted:
+        pytest.skip("this torch's common_quantized.py lacks to_blocked / from_blocked")
+    ns = {"torch": torch}
+    exec(compile(ast.Module(body=funcs, type_ignores=[]), spec.origin, "exec"), ns)
+    return ns["to_blocked"], ns["from_blocked"]
+
+
+@pytest.mark.parametrize("M,C0", [(1, 1), (31, 3), (128, 4), (129, 5), (200, 6), (256, 8), (300, 17)])
+def test_layout_equals_pytorchs_blocked_scale_helpers(M, C0):
+    """The oracle's swizzle against an independent statement of the same layout.  Distinct byte
+    labels catch a transposed pair of in-tile terms ((r % 32) * 16 + (r / 32) * 4 swapped), a
+    wrong tile order or wrong padding, which the bijection test above cannot."""
+    import torch
+
+    to_blocked, from_blocked = torch_blocked_helpers()
+    rng = np.random.default_rng(M * 7 + C0)
+    s = rng.integers(0, 256, (M, C0), dtype=np.uint8)
+    ours = swizzle_scales(s)
+    theirs = to_blocked(torch.from_numpy(s)).numpy()
+    assert theirs.dtype == np.uint8 and theirs.size == ours.size
+    assert np.array_equal(ours, theirs)
+    # from_blocked takes the [M, K] data tensor only for its shape (K = 16 * C0 for NVFP4)
+    data = torch.empty((M, 16 * C0), dtype=torch.uint8)
+    back = from_blocked(data, torch.from_numpy(ours), 16).numpy()
+    assert np.array_equal(back, s)

@@ -6,8 +6,9 @@ at start-up.  Instead of a workspace, it stages the tensor in a fixed array insi
 These tests call it through the C ABI on two calls in a row, with different tensors, rotation
 groups and sizes, so that a second call cannot lean on what the first left in the shared array.
 Each result must equal, byte for byte, what the existing entry points (hq_rot_amax and
-hq_rotate_quant_nvfp4 on device buffers) produce for the same input.  A tensor larger than the
-array must be refused before anything runs.
+hq_rotate_quant_nvfp4 on device buffers) produce for the same input, and what the CPU oracle
+computes from the definition.  A tensor larger than the array must be refused before anything
+runs.
 
 This file is collected last on purpose; it needs no state from the other tests.
 """
@@ -18,6 +19,8 @@ import pytest
 import torch
 
 import hadamard_rotation_gb300 as hq
+import oracle
+from hadamard_rotation_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +34,7 @@ def lib():
     from hadamard_rotation_gb300 import build
 
     build.build()
+    oracle.build()
     lib = hq.load()
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.hq_quantize_nvfp4_host_noalloc.argtypes = [p, i32, i64, i64, i32, p, p, p, p]
@@ -78,8 +82,11 @@ def test_noalloc_matches_existing_entry_points_on_two_calls_in_a_row(lib):
         x_host = host_input(M, K, dtype, seed)
         got = noalloc(lib, x_host, group)
         ref = existing(x_host, group)
-        for name, g, r in zip(("codes", "scales", "s_global"), got, ref):
+        oq, os_, _, osg = oracle.quantize(synth.as_oracle_array(x_host), group)
+        defined = (oq, os_, np.array([osg], np.float32))
+        for name, g, r, o in zip(("codes", "scales", "s_global"), got, ref, defined):
             assert np.array_equal(g.view(np.uint8), r.view(np.uint8)), (name, M, K, group)
+            assert np.array_equal(g.view(np.uint8), o.view(np.uint8)), (name, M, K, group, "oracle")
 
 
 def test_noalloc_refuses_a_tensor_larger_than_its_scratch(lib):
