@@ -52,6 +52,8 @@ def load() -> ctypes.CDLL:
         lib.hq_rot_amax.restype = i32
         lib.hq_rotate_quant_nvfp4.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p]
         lib.hq_rotate_quant_nvfp4.restype = i32
+        lib.hq_rotate_quant_nvfp4_ws.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]
+        lib.hq_rotate_quant_nvfp4_ws.restype = i32
         lib.hq_quantize_nvfp4.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]
         lib.hq_quantize_nvfp4.restype = i32
         lib.hq_rotate_quant_nvfp4_delayed.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]

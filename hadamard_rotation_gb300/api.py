@@ -91,9 +91,10 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     return q, scales, s_global
 
 
-# hq_quantize_nvfp4's workspaces kept by this binding, one per (device, stream).
+# The workspaces of hq_quantize_nvfp4 and hq_rotate_quant_nvfp4_ws kept by this binding, one
+# per (device, stream).
 _WORKSPACES: dict[tuple[int, int], torch.Tensor] = {}
-HQ_QUANTIZE_WORKSPACE_WORDS = 4
+HQ_QUANTIZE_WORKSPACE_WORDS = 288
 HQ_QUANTIZE_FUSED_MAX_BYTES = 64 * 1024 * 1024
 
 
@@ -105,6 +106,26 @@ def _workspace(device: torch.device, stream: torch.cuda.Stream | None) -> torch.
         w = torch.zeros(HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=device)
         _WORKSPACES[key] = w
     return w
+
+
+def hq_rotate_quant_nvfp4_ws(x: torch.Tensor, group: int, amax: torch.Tensor,
+                             q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                             s_global: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None,
+                             stream: torch.cuda.Stream | None = None):
+    """Pass 2 as hq_rotate_quant_nvfp4, with the tiles handed to the warps at run time from the
+    counters in ``workspace`` (int32 [HQ_QUANTIZE_WORKSPACE_WORDS], zero before first use;
+    default: the one this binding keeps per device and stream)."""
+    dt, M, K, ldx = _x_args(x)
+    amax = _need(amax, (1,), torch.float32, x.device, "amax")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    workspace = _workspace(x.device, stream) if workspace is None else _need(
+        workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
+    _call(x.device, "hq_rotate_quant_nvfp4_ws", _ptr(x), dt, M, K, ldx, group, _ptr(amax),
+          _ptr(q), _ptr(scales), _ptr(s_global), _ptr(workspace), stream=stream)
+    return q, scales, s_global
 
 
 def hq_quantize_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor | None = None,

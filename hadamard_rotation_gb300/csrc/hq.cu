@@ -236,6 +236,22 @@ hq_status check_x(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx,
   return HQ_OK;
 }
 
+// Workspace words (HQ_QUANTIZE_WORKSPACE_WORDS in all): [0] grid-barrier arrivals of the
+// one-launch kernel, [1] amax bits, [2] CTAs done with [0] and [1], [3] warps done with the
+// tile counters; then the tile counters of the run-time split from word kSchedWord on, each on
+// its own 128-byte line.  A call that records no fault leaves every word 0.
+constexpr int kSchedWord = hq::kSchedStrideWords;
+static_assert(kSchedWord + hq::kSchedClasses * hq::kSchedStrideWords <= HQ_QUANTIZE_WORKSPACE_WORDS,
+              "workspace too small for the tile counters");
+
+// The run-time split: contiguous rows only (it reads through the TMA ring), from 16384 warp
+// tiles (32 M elements) on: below that a warp has a few tiles, there is little to balance,
+// and the fixed split measured faster (bf16 [4096, 4096]: 10.5 against 11.8 us per pass 2);
+// up to 2^34 tiles (a tile's class index is a 32-bit counter value).
+bool schedulable(const hq::Params& p, const uint32_t* workspace, bool strided) {
+  return workspace != nullptr && !strided && p.n_tiles >= 16384 && p.n_tiles < (uint64_t{1} << 34);
+}
+
 hq::Params base_params(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx) {
   hq::Params p = {};
   p.x = static_cast<const uint8_t*>(x);
@@ -298,6 +314,13 @@ template <int G, bool NEXT>
 hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream s) {
   using hq::k_rotate_quant_nvfp4;
   constexpr int kMode = HQ_PASS2_MODE;
+  if constexpr (!NEXT && kMode == hq::kLoadTma) {
+    if (p.sched != nullptr && !strided)  // tiles handed out at run time
+      return bf16 ? launch(k_rotate_quant_nvfp4<G, true, kMode, false, false, true>, p, s,
+                           ring_bytes<HQ_PASS2_STAGES>(kMode, true), true)
+                  : launch(k_rotate_quant_nvfp4<G, false, kMode, false, false, true>, p, s,
+                           ring_bytes<HQ_PASS2_STAGES>(kMode, false), true);
+  }
   if (bf16)
     return strided ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadStrided, NEXT>, p, s, 0, true)
                    : launch(k_rotate_quant_nvfp4<G, true, kMode, NEXT>, p, s,
@@ -305,6 +328,14 @@ hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream
   return strided ? launch(k_rotate_quant_nvfp4<G, false, hq::kLoadStrided, NEXT>, p, s, 0, true)
                  : launch(k_rotate_quant_nvfp4<G, false, kMode, NEXT>, p, s,
                           ring_bytes<HQ_PASS2_STAGES>(kMode, false), true);
+}
+
+hq_status dispatch_quant_group(const hq::Params& p, int group, bool bf16, bool strided, hq_stream s) {
+  switch (group) {
+    case 0: return dispatch_quant<0, false>(p, bf16, strided, s);
+    case 16: return dispatch_quant<16, false>(p, bf16, strided, s);
+    default: return dispatch_quant<256, false>(p, bf16, strided, s);
+  }
 }
 
 // Pass 2 with swizzled scales: row-group tiles through the TMA ring, one bulk copy
@@ -362,11 +393,13 @@ hq_status hq_rot_amax(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64
   }
 }
 
-hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
-                                int64_t ldx, int group, const float* amax, uint8_t* q,
-                                uint8_t* scales, float* s_global, hq_stream stream) {
+hq_status hq_rotate_quant_nvfp4_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                   int64_t ldx, int group, const float* amax, uint8_t* q,
+                                   uint8_t* scales, float* s_global, uint32_t* workspace,
+                                   hq_stream stream) {
   hq_status st = check_x(x, dtype, M, K, ldx, group);
   if (st != HQ_OK) return st;
+  if (workspace && !aligned(workspace, 4)) return HQ_ERR_ALIGN;
   if (M == 0 || K == 0) return HQ_OK;
   if (!amax || !q || !scales) return HQ_ERR_NULL;
   if (!aligned(amax, 4) || !aligned(q, 16) || !aligned(scales, 4) ||
@@ -377,6 +410,10 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
   p.q = q;
   p.s = scales;
   p.sglobal_out = s_global;
+  if (schedulable(p, workspace, is_strided(M, K, ldx))) {
+    p.sched = workspace + kSchedWord;
+    p.sched_done = workspace + 3;
+  }
   const bool bf16 = dtype == HQ_BF16;
   const bool strided = is_strided(M, K, ldx);
   switch (group) {
@@ -384,6 +421,13 @@ hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_
     case 16: return dispatch_quant<16, false>(p, bf16, strided, stream);
     default: return dispatch_quant<256, false>(p, bf16, strided, stream);
   }
+}
+
+hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                int64_t ldx, int group, const float* amax, uint8_t* q,
+                                uint8_t* scales, float* s_global, hq_stream stream) {
+  return hq_rotate_quant_nvfp4_ws(x, dtype, M, K, ldx, group, amax, q, scales, s_global, nullptr,
+                                  stream);
 }
 
 hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
@@ -421,7 +465,21 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
       st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
     }
     if (st != HQ_OK) return st;
-    return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
+    if (!workspace)
+      return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
+    // Pass 2 as hq_rotate_quant_nvfp4_ws; since the pass 1 above released it only after
+    // waiting for x's producer, it fetches its first tiles of x before it waits for pass 1.
+    hq::Params p = base_params(x, dtype, M, K, ldx);
+    p.amax_in = amax;
+    p.q = q;
+    p.s = scales;
+    p.sglobal_out = s_global;
+    if (schedulable(p, workspace, is_strided(M, K, ldx))) {
+      p.sched = workspace + kSchedWord;
+      p.sched_done = workspace + 3;
+    }
+    p.x_ready = 1;
+    return dispatch_quant_group(p, group, dtype == HQ_BF16, is_strided(M, K, ldx), stream);
   }
   hq::Params p = base_params(x, dtype, M, K, ldx);
   p.q = q;

@@ -63,6 +63,13 @@ constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kBlocksPerLane = 4;
 constexpr int kTileBlocks = 32 * kBlocksPerLane;  // 128 NVFP4 blocks per warp tile
 
+// Dynamic tile schedule: tile t belongs to class t % kSchedClasses, and warp w of every CTA
+// takes the tiles of class w from that class's counter.  The counters sit a 128-byte line
+// apart so that the atomic traffic of different classes does not meet at one address.
+constexpr int kSchedClasses = kWarpsPerCta;
+constexpr int kSchedStrideWords = 32;
+static_assert(kSchedClasses == kThreads / 32, "one class per warp of a CTA");
+
 // Fault bits recorded by the kernels (read back with hq_read_fault()).
 constexpr unsigned kFaultWaitTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
@@ -115,6 +122,13 @@ struct Params {
   unsigned* sync;          // [0] CTAs past pass 1, [1] amax bits, [2] CTAs done; 0 on entry and exit
                            // (pass 1 with a workspace: [1] amax bits, [2] CTAs done)
   float* amax_copy;        // the tensor's amax, written once it is known
+  // run-time tile split (for_each_tile, DYN): kSchedClasses counters kSchedStrideWords apart
+  // and the count of warps done with them, all 0 on entry and put back to 0 by the last warp
+  unsigned* sched;
+  unsigned* sched_done;
+  int x_ready;             // pass 2: x is complete at launch (the pass 1 before it waited for
+                           // x's producer before releasing it), so tiles may be fetched before
+                           // griddepcontrol.wait
   // dequant
   const uint8_t* dq_q;
   const uint8_t* dq_s;
@@ -583,22 +597,77 @@ struct RgTile {      // 32-bit fields: the host keeps units below 2^29, so rows 
 };
 
 
-// Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's
-// values in registers.  Warp w of W takes the tiles w, w + W, w + 2W, ...
+// A prologue that does nothing (for_each_tile's default).
+struct NoPrologue {
+  __device__ __forceinline__ void operator()() const {}
+};
+
+constexpr uint64_t kNoTile = ~uint64_t{0};
+
+// 64-bit broadcast from lane 0.
+__device__ __forceinline__ uint64_t bcast0(uint64_t v) {
+  const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), 0);
+  const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), 0);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// A warp of the run-time split whose class has no tile left for it (its last counter fetch
+// came back past the end, or it never had a tile) counts itself out; the last warp of the grid
+// to do so puts the counters and the count back to 0 for the next call.  Called by lane 0,
+// once per warp, as soon as that is known: usually a tile or two before the warp's end, so
+// the reset overlaps the work still in flight.  Every counter atomic of a warp has returned
+// its value before the warp counts itself out, and all warps have counted themselves out
+// before the reset, so no fetch of this launch can follow it.
+__device__ __forceinline__ void sched_retire(const Params& p) {
+  if (atomicAdd(p.sched_done, 1u) == gridDim.x * static_cast<unsigned>(kWarpsPerCta) - 1u) {
+    __threadfence();
+#pragma unroll
+    for (int c = 0; c < kSchedClasses; ++c) atomicExch(p.sched + c * kSchedStrideWords, 0u);
+    atomicExch(p.sched_done, 0u);
+  }
+}
+
+// Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's values in
+// registers.
+//
+// Which tiles.  Fixed split (DYN false): warp w of W takes the tiles w, w + W, w + 2W, ...
+// Run-time split (DYN, contiguous rows only): tile t belongs to class t % C (C =
+// kSchedClasses) and warp c of every CTA serves class c, tiles c + C j.  Its first R class
+// indices are fixed, j = blockIdx.x + s gridDim.x (s < R, the ring depth), so the first
+// copies need no atomic; every later j is R gridDim.x + the value of an atomicAdd on the
+// class counter p.sched[c * kSchedStrideWords].  Only lane 0 keeps this schedule: it reads
+// the counter one tile ahead (the atomic's latency hides behind the tile in between), issues
+// the copies, and the other lanes learn each tile's index from it when they read that slot,
+// long after it was chosen.  Warps that run ahead take more tiles, and all warps run out of
+// work within about one tile of each other.  The counters are 0 on entry, and the last warp
+// to run out of tiles puts them back to 0 (sched_retire).
+//
+// GDC: the kernel was launched as a programmatic dependent and has not yet executed
+// griddepcontrol.wait; the loop does, before its first access to global memory, or, when
+// p.x_ready declares x complete, right after issuing its first tile copies.
+// `pre()` runs once in every warp before the first tile is read: in the TMA form after the
+// warp's first copies have been issued, so that work the tiles need (reading the amax,
+// building the divisor table) overlaps their flight instead of delaying it.  Every warp of
+// the CTA calls it, so it may hold a __syncthreads().
 // KEEP_L2: read x with an L2 evict-last hint (it is read again soon) instead of
-// evict-first.  REVERSE: the k-th tile of the sequence is tile n_tiles - 1 - k, so
-// the pass walks x from its end (pass 1 of the two-launch path: pass 2 walks it
-// from the start, and each pass then begins where the previous one ended, with
+// evict-first.  REVERSE (fixed split only): the k-th tile of the sequence is tile
+// n_tiles - 1 - k, so the pass walks x from its end (pass 1 of the two-launch path: pass 2
+// walks it from the start, and each pass then begins where the previous one ended, with
 // that part of x still in L2).
 template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool KEEP_L2 = false, bool S1 = false,
-          bool REVERSE = false, typename Body>
-__device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
+          bool REVERSE = false, bool GDC = false, bool DYN = false, typename Body,
+          typename Pre = NoPrologue>
+__device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
+  static_assert(!(DYN && (REVERSE || MODE != kLoadTma)), "run-time split: TMA ring, forward walk");
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + wid;
   const uint64_t nw = static_cast<uint64_t>(gridDim.x) * kWarpsPerCta;
   auto tile_of = [&](uint64_t seq) { return REVERSE ? p.n_tiles - 1 - seq : seq; };
+  auto gdc_wait = []() { asm volatile("griddepcontrol.wait;" ::: "memory"); };
   if constexpr (MODE != kLoadTma) {
+    if constexpr (GDC) gdc_wait();
+    pre();
     for (uint64_t seq = gw; seq < p.n_tiles; seq += nw) {
       const uint64_t base = tile_of(seq) * kTileBlocks;
       bool valid[4];
@@ -620,46 +689,121 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
       tma_load(ring_s + slot * R::kTileBytes, p.x + first * 16u * R::kElemBytes,
                static_cast<uint32_t>(nblk * 16u * R::kElemBytes), bar0 + slot * 8, policy);
     };
+    auto timed_out = [&](uint64_t k, uint64_t issued) {
+      if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+      for (uint64_t m = k; m < issued; ++m)
+        mbar_wait(bar0 + static_cast<int>(m % R::kStages) * 8, static_cast<uint32_t>((m / R::kStages) & 1));
+    };
 
     if (lane == 0) {
       for (int s = 0; s < R::kStages; ++s) mbar_init(bar0 + s * 8, 1);
       fence_mbar_init();
     }
     __syncwarp();
-    uint64_t issued = 0;  // tiles of this warp handed to TMA so far
-    if (lane == 0) {
-      for (int s = 0; s < R::kStages; ++s)
-        if (gw + s * nw < p.n_tiles) issue(gw + s * nw, s);
-    }
-    for (int s = 0; s < R::kStages; ++s)
-      if (gw + s * nw < p.n_tiles) ++issued;
+    const bool early = GDC && p.x_ready;
+    if (GDC && !early) gdc_wait();
 
-    uint64_t k = 0;
-    for (uint64_t seq = gw; seq < p.n_tiles; seq += nw, ++k) {
-      const int slot = static_cast<int>(k % R::kStages);
-      const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
-      const bool ok = mbar_wait(bar0 + slot * 8, parity);
-      if (!__all_sync(0xFFFFFFFFu, ok)) {
-        if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
-        for (uint64_t m = k; m < issued; ++m)
-          mbar_wait(bar0 + static_cast<int>(m % R::kStages) * 8,
-                    static_cast<uint32_t>((m / R::kStages) & 1));
-        return;
+    if constexpr (!DYN) {
+      uint64_t issued = 0;  // tiles of this warp handed to TMA so far
+      if (lane == 0) {
+        for (int s = 0; s < R::kStages; ++s)
+          if (gw + s * nw < p.n_tiles) issue(gw + s * nw, s);
       }
-      const uint64_t base = tile_of(seq) * kTileBlocks;
-      bool valid[4];
-      Lane4 t;
-      load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
-      __syncwarp();  // every lane has read the slot
-      const uint64_t next = seq + R::kStages * nw;
-      if (next < p.n_tiles) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue(next, slot);
+      for (int s = 0; s < R::kStages; ++s)
+        if (gw + s * nw < p.n_tiles) ++issued;
+      if (early) gdc_wait();
+      pre();
+
+      uint64_t k = 0;
+      for (uint64_t seq = gw; seq < p.n_tiles; seq += nw, ++k) {
+        const int slot = static_cast<int>(k % R::kStages);
+        const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
+        const bool ok = mbar_wait(bar0 + slot * 8, parity);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          timed_out(k, issued);
+          return;
         }
-        ++issued;
+        const uint64_t base = tile_of(seq) * kTileBlocks;
+        bool valid[4];
+        Lane4 t;
+        load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        __syncwarp();  // every lane has read the slot
+        const uint64_t next = seq + R::kStages * nw;
+        if (next < p.n_tiles) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            issue(next, slot);
+          }
+          ++issued;
+        }
+        body(base, lane, valid, t);
       }
-      body(base, lane, valid, t);
+    } else {
+      // Lane 0's schedule: queue[s] is the tile held by the s-th slot to be read (kNoTile:
+      // none, and none after it).
+      const uint64_t cls = static_cast<uint64_t>(wid);
+      unsigned* const counter = p.sched + wid * kSchedStrideWords;
+      uint64_t queue[R::kStages];
+      uint64_t issued = 0;
+      unsigned pend = 0;
+      bool more = true;  // lane 0: this warp's class may still have tiles for it
+      if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < R::kStages; ++s) {
+          const uint64_t tile = cls + kSchedClasses * (blockIdx.x + static_cast<uint64_t>(s) * gridDim.x);
+          queue[s] = more && tile < p.n_tiles ? tile : kNoTile;
+          more = queue[s] != kNoTile;
+          if (more) {
+            issue(queue[s], s);
+            ++issued;
+          }
+        }
+      }
+      if (early) gdc_wait();
+      if (lane == 0) {  // the counters are ready once the kernel before has completed
+        if (more)
+          pend = atomicAdd(counter, 1u);
+        else
+          sched_retire(p);
+      }
+      pre();
+
+      for (uint64_t k = 0;; ++k) {
+        const uint64_t cur = bcast0(lane == 0 ? queue[0] : 0);
+        if (cur == kNoTile) break;
+        const int slot = static_cast<int>(k % R::kStages);
+        const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
+        const bool ok = mbar_wait(bar0 + slot * 8, parity);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          timed_out(k, bcast0(issued));
+          return;
+        }
+        const uint64_t base = cur * kTileBlocks;
+        bool valid[4];
+        Lane4 t;
+        load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0) {
+          uint64_t nt = kNoTile;
+          if (more) {
+            nt = cls + kSchedClasses * (static_cast<uint64_t>(R::kStages) * gridDim.x + pend);
+            if (nt < p.n_tiles) {
+              pend = atomicAdd(counter, 1u);  // the one after, read ahead
+              fence_proxy_async_smem();
+              issue(nt, slot);
+              ++issued;
+            } else {
+              nt = kNoTile;
+              more = false;
+              sched_retire(p);
+            }
+          }
+#pragma unroll
+          for (int s = 0; s + 1 < R::kStages; ++s) queue[s] = queue[s + 1];
+          queue[R::kStages - 1] = nt;
+        }
+        body(base, lane, valid, t);
+      }
     }
   }
 }
@@ -668,8 +812,8 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body) {
 // each as its 8 tiles in order, and calls body(tile, lane, valid, t) with the
 // RgTile.  The unit positions (row group, column chunk) of the tile being read
 // and of the tile being fetched advance by W units with one carry, no division.
-template <int G, bool BF16, int STAGES, typename Body>
-__device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
+template <int G, bool BF16, int STAGES, typename Body, typename Pre = NoPrologue>
+__device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
   using R = Ring<BF16, STAGES>;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -740,6 +884,7 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body) {
       step(ip);
     }
   }
+  pre();
   Pos cp = start();  // the tile to read: unit cp, tile crs
   int crs = 0;
   for (uint64_t k = 0; cp.u < n_units; ++k) {
@@ -1033,11 +1178,11 @@ __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
 
 template <int G, bool BF16, int MODE, bool WRITE_Y>
 __global__ void __launch_bounds__(kThreads, HQ_PASS1_MIN_CTAS) k_rot_amax(Params p) {
-  // As k_rot_amax_stream: the next kernel may be launched now.
+  // As k_rot_amax_stream: wait for the kernel before, then let the next one be launched.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   // |y| = RN(|z| / sqrt(G)) is monotone in |z|, so max |y| = RN(max |z| / sqrt(G))
   // exactly; the scaling commutes with the max over the CTA.
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // as k_rot_amax_stream
   cta_amax_to_global(__fmul_rn(rot_amax_tiles<G, BF16, MODE, WRITE_Y>(p), inv_sqrt_g<G>()), p.amax_out,
                      p.sync ? p.sync + 2 : nullptr, p.amax_copy);
 }
@@ -1063,12 +1208,13 @@ __device__ __forceinline__ void ld_v8_stream(const uint8_t* src, uint32_t* w) {
 
 template <int G, bool BF16>
 __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_amax_stream(Params p) {
-  // Let the next kernel on the stream (pass 2) be launched now; it waits for this grid's
-  // completion before it reads anything.  When this grid was itself launched as a
-  // programmatic dependent (hq_quantize_nvfp4 with a workspace), wait for the kernel before
-  // it to complete before reading x.
-  asm volatile("griddepcontrol.launch_dependents;");
+  // When this grid was launched as a programmatic dependent (hq_quantize_nvfp4 with a
+  // workspace), wait for the kernel before it to complete before reading x.  Then let the
+  // next kernel on the stream (pass 2) be launched: it waits for this grid's completion
+  // before it reads the amax, and since the launch comes after this wait, whatever wrote x
+  // has completed by then (pass 2 of hq_quantize_nvfp4 reads its first tiles of x early).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kWords = BF16 ? 8 : 16;  // 32-bit words per 16-element block
   const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;
   uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -1182,17 +1328,16 @@ __device__ __forceinline__ bool grid_barrier(unsigned* count, unsigned target) {
 // tiles row-major; inside a tile, row r and column c at (r % 32) * 16 + (r / 32) *
 // 4 + c.  The tiles of this mode are row groups (RgTile), so that every scale
 // store fills whole 32-byte pieces of that layout, padding included.
-template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
-__device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float amax) {
-  // s_global = amax / (448 * 6), or 1 if that is 0.
-  float s_global = __fdiv_rn(amax, 2688.0f);
-  if (s_global == 0.0f) s_global = 1.0f;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.sglobal_out) *p.sglobal_out = s_global;
-  // Reciprocals for the block-scale divisions (Markstein fast path).
+// amax: where the global amax is read, once the first tile copies are in flight (global
+// memory for pass 2, shared memory in the one-launch kernel).
+// GDC: the kernel was launched as a programmatic dependent and has not yet executed
+// griddepcontrol.wait; the tile loop does.
+template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false, bool GDC = false,
+          bool DYN = false>
+__device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float* amax) {
   const float r6 = __frcp_rn(6.0f);
-  const float rg = __frcp_rn(s_global);
-  const bool sg_ok = s_global >= 0x1p-60f && s_global <= 0x1p60f;
-  const bool q_fast = s_global >= 0x1p-87f && s_global <= 0x1p91f;
+  float s_global, rg;  // s_global and its reciprocal (Markstein fast path of the block scales)
+  bool sg_ok, q_fast;
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
@@ -1213,15 +1358,24 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
   // computed once per CTA instead of once per block.
   __shared__ float tab_d[128];
   __shared__ float tab_nr[128];
-  if (q_fast) {  // the same for every thread of the grid
-    for (int e = threadIdx.x; e < 128; e += kThreads) {
-      const float sfe = __fmul_rn(e4m3x2_to_f32(static_cast<uint32_t>(e)).x, s_global);
-      const float d = (sfe == 0.0f) ? 1.0f : __fmul_rn(sfe, sq);
-      tab_d[e] = d;
-      tab_nr[e] = -__frcp_rn(d);
+  auto prologue = [&]() {
+    // s_global = amax / (448 * 6), or 1 if that is 0.
+    s_global = __fdiv_rn(*amax, 2688.0f);
+    if (s_global == 0.0f) s_global = 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.sglobal_out) *p.sglobal_out = s_global;
+    rg = __frcp_rn(s_global);
+    sg_ok = s_global >= 0x1p-60f && s_global <= 0x1p60f;
+    q_fast = s_global >= 0x1p-87f && s_global <= 0x1p91f;
+    if (q_fast) {  // the same for every thread of the grid
+      for (int e = threadIdx.x; e < 128; e += kThreads) {
+        const float sfe = __fmul_rn(e4m3x2_to_f32(static_cast<uint32_t>(e)).x, s_global);
+        const float d = (sfe == 0.0f) ? 1.0f : __fmul_rn(sfe, sq);
+        tab_d[e] = d;
+        tab_nr[e] = -__frcp_rn(d);
+      }
+      __syncthreads();
     }
-    __syncthreads();
-  }
+  };
   float next_amax = 0.0f;  // max of the block amaxes this thread saw (REDUCE_NEXT)
   uint32_t swz_acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // SWZ: scale words of the unit's rows
 
@@ -1382,19 +1536,25 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float 
     }
   };
   if constexpr (SWZ)
-    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body);
+    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body, prologue);
   else
-    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, false, kS1>(p, tile_body);
+    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, false, kS1, false, GDC, DYN>(p, tile_body, prologue);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
 }
 
-template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false>
+template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   // Launched with programmatic dependent launch: wait for the kernel before this one on
   // the stream (normally pass 1, which writes *amax_in) to complete before any access to
-  // global memory.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ>(p, *p.amax_in);
+  // global memory other than the first tiles of an x that p.x_ready declares complete.
+  // The plain tile loop waits itself, after its first tile copies when x is known to be
+  // complete (p.x_ready); the row-group loop waits here.
+  if constexpr (SWZ) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ>(p, p.amax_in);
+  } else {
+    rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ, true, DYN>(p, p.amax_in);
+  }
 }
 
 // Both passes in one cooperative launch, for an x that L2 holds: pass 1 reads x
@@ -1426,7 +1586,7 @@ __global__ void __launch_bounds__(kThreads, BF16 ? 2 : 1) k_quant_nvfp4_fused(Pa
   }
   __syncthreads();
   if (!ok) return;
-  rotate_quant_tiles<G, BF16, kLoadTma, false>(p, amax_s);
+  rotate_quant_tiles<G, BF16, kLoadTma, false>(p, &amax_s);
 }
 
 // ---------------------------------------------------------------------------

@@ -114,8 +114,10 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
 
 /* Tensors of x of at most this many bytes take hq_quantize_nvfp4's one-launch path. */
 #define HQ_QUANTIZE_FUSED_MAX_BYTES (64ll * 1024 * 1024)
-/* Size of hq_quantize_nvfp4's workspace, in 32-bit words. */
-#define HQ_QUANTIZE_WORKSPACE_WORDS 4
+/* Size of the workspace of hq_quantize_nvfp4 and hq_rotate_quant_nvfp4_ws, in 32-bit words
+ * (control words and the counters of the run-time tile schedule, each on its own 128-byte
+ * line). */
+#define HQ_QUANTIZE_WORKSPACE_WORDS 288
 
 /*
  * hq_quantize_nvfp4 -- both passes in one call: *amax, then codes, scales and s_global exactly as
@@ -128,18 +130,18 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
  *   evict-last hint, all CTAs meet at a grid-wide barrier once the amax is reduced, and the
  *   second reads x back from L2.  Otherwise the call is two launches, pass 1 then pass 2 as
  *   hq_rotate_quant_nvfp4.  With `workspace`, pass 1 reduces the amax into the workspace and
- *   its last CTA writes *amax (no memset before it), and both launches are programmatic
- *   dependents of the kernel before them on the stream (each waits for that kernel to complete
- *   before it reads memory); without, pass 1 is hq_rot_amax.
+ *   its last CTA writes *amax (no memset before it), pass 2 is hq_rotate_quant_nvfp4_ws (tiles
+ *   handed out at run time), and both launches are programmatic dependents of the kernel
+ *   before them on the stream (each waits for that kernel to complete before it reads
+ *   memory); without, pass 1 is hq_rot_amax and pass 2 hq_rotate_quant_nvfp4.
  *
  *   x, dtype, M, K, ldx, group : as for hq_rot_amax.
  *   amax      : 1 float on the device (written; 0 for an empty tensor).
  *   q, scales, s_global : as for hq_rotate_quant_nvfp4.
  *   workspace : NULL (hq_rot_amax then hq_rotate_quant_nvfp4), or HQ_QUANTIZE_WORKSPACE_WORDS
- *               uint32 on the device, 4-byte
- *               aligned, all 0 before its first use (e.g. cudaMemset).  Each call that records
- *               no fault leaves it 0 again.  Calls that may run at the same time (different
- *               streams) need different workspaces.
+ *               uint32 on the device, 4-byte aligned, all 0 before its first use (e.g.
+ *               cudaMemset).  Each call that records no fault leaves it 0 again.  Calls that may
+ *               run at the same time (different streams) need different workspaces.
  *   A grid barrier that waits about a second without all CTAs arriving records bit 0 of the
  *   fault word (hq_read_fault); those CTAs skip the second pass and the outputs are undefined.
  */
@@ -147,6 +149,25 @@ HQ_API hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int
                                    int64_t ldx, int group, float* amax, uint8_t* q,
                                    uint8_t* scales, float* s_global, uint32_t* workspace,
                                    hq_stream stream);
+
+/*
+ * hq_rotate_quant_nvfp4_ws -- pass 2 exactly as hq_rotate_quant_nvfp4 (same arguments, same
+ *   outputs), with the tiles of x handed to the warps at run time instead of by a fixed split.
+ *   (Not a step of the pages' method: a schedule.  With a fixed split the warps of an SM
+ *   advance at different speeds, and the last ones still run while the others have left,
+ *   with the memory system part idle.  Here each warp takes its next tile from a counter in
+ *   `workspace`, so all warps run out of work at about the same time.)
+ *
+ *   workspace : HQ_QUANTIZE_WORKSPACE_WORDS uint32 on the device, 4-byte aligned, all 0 before
+ *               its first use (e.g. cudaMemset); each call that records no fault leaves it 0
+ *               again.  Calls that may run at the same time (different streams) need different
+ *               workspaces; hq_quantize_nvfp4's may be shared with it on one stream.
+ *               NULL: the fixed split of hq_rotate_quant_nvfp4.
+ */
+HQ_API hq_status hq_rotate_quant_nvfp4_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                          int64_t ldx, int group, const float* amax, uint8_t* q,
+                                          uint8_t* scales, float* s_global, uint32_t* workspace,
+                                          hq_stream stream);
 
 /*
  * hq_rotate_quant_nvfp4_swizzled -- pass 2 exactly as hq_rotate_quant_nvfp4, with the E4M3 block

@@ -42,6 +42,11 @@ def nvfp4_reference(bench_tensor):
     return oracle.quantize(xo, 16)
 
 
+# A finished call leaves every workspace word 0 (the next call relies on it).
+def settled(ws) -> bool:
+    return not ws.any().item()
+
+
 def f32_bits(a):
     return np.asarray(a, np.float32).view(np.uint32)
 
@@ -66,7 +71,7 @@ def test_bench_step_twice_on_one_workspace(bench_tensor, nvfp4_reference):
         assert f32_bits(sg.cpu().numpy())[0] == f32_bits([osg])[0], call
         assert np.array_equal(s.cpu().numpy(), os_), call
         assert np.array_equal(q.cpu().numpy(), oq), call
-        assert not ws.any().item(), call         # the workspace is 0 again after every call
+        assert settled(ws), call         # the workspace is ready for the next call
     assert hq.hq_read_fault() == 0
 
 

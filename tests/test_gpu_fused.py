@@ -27,6 +27,11 @@ def built():
     hq.load()
 
 
+# A finished call leaves every workspace word 0 (the next call relies on it).
+def settled(ws) -> bool:
+    return not ws.any().item()
+
+
 def f32_bits(a) -> np.ndarray:
     return np.asarray(a, np.float32).view(np.uint32)
 
@@ -81,7 +86,7 @@ def test_fused_matches_oracle(M, K, group, dtype):
     got = hq.hq_quantize_nvfp4(x_host.cuda(), group, workspace=ws)
     torch.cuda.synchronize()
     check(x_host, group, got, f"{M}x{K} {dtype}")
-    assert not ws.any().item(), ws
+    assert settled(ws), ws
 
 
 @pytest.mark.parametrize("group", [0, 16, 256])
@@ -110,7 +115,7 @@ def test_repeated_calls_reuse_the_workspace():
             got = hq.hq_quantize_nvfp4(x_host.cuda(), group, workspace=ws)
             torch.cuda.synchronize()
             check(x_host, group, got, f"call {i} group {group}")
-            assert not ws.any().item()
+            assert settled(ws)
 
 
 @pytest.mark.parametrize("rows", [8192, 8193])
@@ -147,7 +152,7 @@ def test_two_launches_with_a_workspace_leave_it_zero():
                 got = hq.hq_quantize_nvfp4(padded[:, :2048], group, workspace=ws)
                 torch.cuda.synchronize()
                 check(x_host, group, got, f"strided {dtype} call {i} group {group}")
-                assert not ws.any().item()
+                assert settled(ws)
 
 
 def test_streaming_pass_1_with_a_workspace_in_a_row():
@@ -159,7 +164,7 @@ def test_streaming_pass_1_with_a_workspace_in_a_row():
         got = hq.hq_quantize_nvfp4(x_host.cuda(), 16, workspace=ws)
         torch.cuda.synchronize()
         check(x_host, 16, got, f"bf16 [8200, 4096] seed {seed}")
-        assert not ws.any().item()
+        assert settled(ws)
 
 
 def test_two_launch_modes_agree():
@@ -242,4 +247,63 @@ def test_cuda_graph_capture_and_replay(fused):
         g.replay()
         torch.cuda.synchronize()
         check(x_host, 16, (q, s, sg, amax), f"replay {i} fused={fused}")
-        assert not ws.any().item()
+        assert settled(ws)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (999, 4352), (4099, 8192), (16385, 2048), (2053, 17408)])
+def test_pass_2_with_run_time_tile_schedule(M, K):
+    """hq_rotate_quant_nvfp4_ws hands the tiles out from counters in the workspace from 16384
+    warp tiles on (below, and for strided rows, it is the fixed split).  Small sizes (one
+    block; fewer tiles than warps) and sizes past the threshold with a ragged last tile (16385
+    x 2048: 16385 tiles, 2053 x 17408: 17449 tiles, classes of unequal length); contiguous and
+    strided rows, both input types, every group it can take; each call twice in a row on one
+    workspace.  Codes, scales and s_global equal the oracle's, and the workspace is 0 after
+    every call."""
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    for dtype in (torch.bfloat16, torch.float32):
+        x_host = rand_input(M, K, dtype, seed=M + K)
+        xo = synth.as_oracle_array(x_host)
+        for strided in (False, True):
+            if strided:
+                xd = torch.zeros(M, K + 64, dtype=dtype, device="cuda")
+                xd[:, :K] = x_host.cuda()
+                x = xd[:, :K]
+            else:
+                x = x_host.cuda()
+            for group in (0, 16, 256):
+                if K % max(group, 16):
+                    continue
+                oq, os_, oamax, osg = oracle.quantize(xo, group)
+                amax = torch.tensor([oamax], dtype=torch.float32, device="cuda")
+                label = f"{dtype} [{M}, {K}] strided={strided} group={group}"
+                for call in range(2):
+                    q, s, sg = hq.hq_rotate_quant_nvfp4_ws(x, group, amax, workspace=ws)
+                    torch.cuda.synchronize()
+                    assert f32_bits(sg.cpu().numpy())[0] == f32_bits([osg])[0], label
+                    assert np.array_equal(s.cpu().numpy(), os_), (label, call)
+                    assert np.array_equal(q.cpu().numpy(), oq), (label, call)
+                    assert settled(ws), (label, call)
+    assert hq.hq_read_fault() == 0
+
+
+def test_run_time_schedule_on_two_streams_with_their_own_workspaces():
+    """Two streams quantize two tensors at the same time, each with its own workspace (the
+    documented rule for calls that may overlap): both results exact, both workspaces 0."""
+    xs = [rand_input(4096, 8192, torch.bfloat16, seed=61 + i) for i in range(2)]  # 16384 tiles
+    streams = [torch.cuda.Stream() for _ in xs]
+    wss = [torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+           for _ in xs]
+    xd = [x.cuda() for x in xs]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):
+        outs = []
+        for x, st, ws in zip(xd, streams, wss):
+            with torch.cuda.stream(st):
+                amax = hq.hq_rot_amax(x, 16, stream=st)
+                outs.append(hq.hq_rotate_quant_nvfp4_ws(x, 16, amax, workspace=ws, stream=st))
+    torch.cuda.synchronize()
+    for x_host, (q, s, sg), ws in zip(xs, outs, wss):
+        oq, os_, _, osg = oracle.quantize(synth.as_oracle_array(x_host), 16)
+        assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), os_)
+        assert settled(ws)
