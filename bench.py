@@ -333,10 +333,10 @@ def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: i
                 i[0] += 1
                 return k
 
-            def p2():
+            def p2():  # pass 2 as the step runs it (run-time tile split from 16384 tiles on)
                 k = nxt()
-                hq.hq_rotate_quant_nvfp4(xs[k], group, amax, q=qs[k], scales=ss[k], s_global=sg,
-                                         stream=stream)
+                hq.hq_rotate_quant_nvfp4_ws(xs[k], group, amax, q=qs[k], scales=ss[k], s_global=sg,
+                                            workspace=ws, stream=stream)
 
             def p1():
                 hq.hq_rot_amax(xs[nxt()], group, amax=a1, stream=stream)
@@ -414,12 +414,14 @@ def run_ours(args, w):
     # launches, pass 1 reducing into the workspace (no memset before it).
     fused = bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
+    ws2 = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
 
     def pass1():
         hq.hq_rot_amax(x, group, amax=amax, stream=stream)
 
-    def pass2():
-        hq.hq_rotate_quant_nvfp4(x, group, amax, q=q, scales=s, s_global=sg, stream=stream)
+    def pass2():  # pass 2 as the step runs it (run-time tile split from 16384 tiles on)
+        hq.hq_rotate_quant_nvfp4_ws(x, group, amax, q=q, scales=s, s_global=sg, workspace=ws2,
+                                    stream=stream)
 
     def step():
         hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, fused=True,

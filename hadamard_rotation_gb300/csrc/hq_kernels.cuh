@@ -141,9 +141,14 @@ struct Params {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
-// a - b with one rounding: b * (-1) is exact, so fma(b, -1, a) = RN(a - b).
+// a - b with one rounding per lane (the packed subtract: two register pairs read, where the
+// fma form RN(b * -1 + a) read three; bf16 [32768, 28672] pass 2: 351.4 -> 348.4 us).
 __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+  const unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
+  const unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long rd;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2*>(&rd);
 }
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
@@ -211,15 +216,6 @@ __device__ __forceinline__ float div_markstein(float a, float b, float r) {
   const float q0 = __fmul_rn(a, r);
   const float e = __fmaf_rn(-q0, b, a);
   return __fmaf_rn(e, r, q0);
-}
-
-// div_markstein on two dividends at once (packed fp32x2): the same three roundings per
-// value, so the same results.  -q0 * b = q0 * (-b) exactly.
-__device__ __forceinline__ float2 div2_markstein(float2 a, float b, float r) {
-  const float2 r2 = make_float2(r, r);
-  const float2 q0 = mul2(a, r2);
-  const float2 e = fma2(q0, make_float2(-b, -b), a);
-  return fma2(e, r2, q0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1406,21 +1402,8 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
     for (int j = 0; j < 4; ++j) v_fast &= am[j] <= 0x1p90f;
     float v[4];
     if (v_fast) {
-      if constexpr (G == 256) {
-        // The 256-group pass is bound by instruction issue: two packed pairs instead of
-        // four scalar chains (502 against 512 us on bf16 [32768, 28672]; for G <= 16 the
-        // scalar form is as fast).
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float2 w2 = div2_markstein(
-              div2_markstein(make_float2(am[2 * k], am[2 * k + 1]), 6.0f, r6), s_global, rg);
-          v[2 * k] = w2.x;
-          v[2 * k + 1] = w2.y;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = div_markstein(div_markstein(am[j], 6.0f, r6), s_global, rg);
-      }
+      for (int j = 0; j < 4; ++j) v[j] = div_markstein(div_markstein(am[j], 6.0f, r6), s_global, rg);
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = __fdiv_rn(__fdiv_rn(am[j], 6.0f), s_global);
@@ -1455,9 +1438,17 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 z = t.P[k][i];
-          const float2 q0n = mul2(z, nr);
-          const float2 e = fma2(q0n, d, z);
-          qv[i] = fma2(e, nr, q0n);
+          if constexpr (G == 256) {
+            // Scalar here: bf16 [8192, 16384] 73.4 -> 71.7 us (the packed form keeps the
+            // FMA pipe's heavy half busy two cycles per instruction; G = 16 is faster packed)
+            const float q0x = __fmul_rn(z.x, nr.x), q0y = __fmul_rn(z.y, nr.y);
+            const float ex = __fmaf_rn(q0x, d.x, z.x), ey = __fmaf_rn(q0y, d.y, z.y);
+            qv[i] = make_float2(__fmaf_rn(ex, nr.x, q0x), __fmaf_rn(ey, nr.y, q0y));
+          } else {
+            const float2 q0n = mul2(z, nr);
+            const float2 e = fma2(q0n, d, z);
+            qv[i] = fma2(e, nr, q0n);
+          }
         }
         constexpr uint32_t kFlip = 0x88888888u;  // sign bit of every nibble
         w[2 * k][0] = kFlip ^ e2m1x8(qv[0].x, qv[1].x, qv[2].x, qv[3].x, qv[4].x, qv[5].x, qv[6].x, qv[7].x);
