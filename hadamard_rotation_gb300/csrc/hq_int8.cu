@@ -17,7 +17,7 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // INT8 per-token rotate-quant: one CTA of kI8Threads per SM, looping over row groups.
 template <int G, bool BF16, int MODE, bool FULL>
 hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
-  // G = 16 is bound by memory: fixed warp places (L = 1); G = 64, 256: round robin.
+  // G <= 16 is bound by memory: fixed warp places (L = 1); G >= 64: round robin.
   auto kernel = hq::k_rotate_quant_int8<G, BF16, MODE, FULL, (G > 16)>;
   const size_t smem = (MODE == hq::kLoadTma) ? static_cast<size_t>(hq::kI8RingBytes) : 0;
   int dev = 0, sms = 0;
@@ -37,8 +37,25 @@ hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
   return HQ_OK;
 }
 
+// Rows longer than tensor memory can park: one CTA of kI8Threads per SM, each row read twice.
+template <int G, bool BF16>
+hq_status launch_int8_long(const hq::I8Params& p, hq_stream stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  const unsigned grid = static_cast<unsigned>(p.M < sms ? p.M : sms);
+  hq::k_rotate_quant_int8_long<G, BF16><<<grid, hq::kI8Threads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HQ_OK;
+}
+
 template <int G>
 hq_status dispatch_int8(const hq::I8Params& p, bool bf16, hq_stream s) {
+  if (p.K > hq::kI8MaxK)
+    return bf16 ? launch_int8_long<G, true>(p, s) : launch_int8_long<G, false>(p, s);
   const bool full = p.K % hq::kI8TileElems == 0;
   if (bf16)
     return full ? launch_int8<G, true, hq::kLoadTma, true>(p, s)
@@ -83,8 +100,9 @@ extern "C" {
 hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
                                int group, int8_t* q, float* scales, hq_stream stream) {
   if (dtype != HQ_F32 && dtype != HQ_BF16) return HQ_ERR_DTYPE;
-  if (group != 16 && group != 64 && group != 256) return HQ_ERR_GROUP;
-  if (M < 0 || K < 0 || ldx < K || K % group != 0 || K > hq::kI8MaxK) return HQ_ERR_SHAPE;
+  if (group != 4 && group != 16 && group != 64 && group != 256 && group != 1024) return HQ_ERR_GROUP;
+  if (M < 0 || K < 0 || ldx < K || K % group != 0 || K % 16 != 0) return HQ_ERR_SHAPE;
+  if (K / hq::kI8TileElems >= (int64_t{1} << 30)) return HQ_ERR_SHAPE;  // tiles per row in an int
   const int64_t es = dtype == HQ_BF16 ? 2 : 4;
   if ((K > 0 && M > INT64_MAX / K) || ldx > INT64_MAX / es) return HQ_ERR_SHAPE;
   if (M == 0 || K == 0) return HQ_OK;
@@ -104,7 +122,10 @@ hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t
     b = t;
   }
   const int lcm = p.tiles_per_row / a * hq::kI8Warps;
-  if (group == 16) {  // memory-bound: whole rows, one tile per warp (see hq_int8.cuh)
+  if (p.tiles_per_row > hq::kI8Warps) {  // the long-row kernel: one row at a time
+    p.rows_per_block = 1;
+    p.tiles_per_warp = 0;
+  } else if (group <= 16) {  // memory-bound: whole rows, one tile per warp (see hq_int8.cuh)
     p.rows_per_block = hq::kI8Warps / p.tiles_per_row;
     p.tiles_per_warp = 1;
   } else {
@@ -115,9 +136,11 @@ hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t
   p.scales = scales;
   const bool bf16 = dtype == HQ_BF16;
   switch (group) {
+    case 4: return dispatch_int8<4>(p, bf16, stream);
     case 16: return dispatch_int8<16>(p, bf16, stream);
     case 64: return dispatch_int8<64>(p, bf16, stream);
-    default: return dispatch_int8<256>(p, bf16, stream);
+    case 256: return dispatch_int8<256>(p, bf16, stream);
+    default: return dispatch_int8<1024>(p, bf16, stream);
   }
 }
 

@@ -79,77 +79,103 @@ __device__ __forceinline__ void h4_step(float2& a0, float2& a1, float2& a2, floa
 // its quad so that the cross-lane step below runs the same instructions on all
 // four lanes: lane bit 0 swaps the two float2 arrays, lane bit 1 swaps .x and .y.
 // In every lane add2(P[0][i], P[1][i]) pairs digit-3 values {0, 1} and {2, 3}.
+// G = 1024 has a second cross-lane step, on digit 4 (the quad within the 1024-group,
+// lane bits 2 and 3); lane bits 2 and 3 then enter the map as well (xor-ed onto bits
+// 0 and 1), so that the lanes l, l ^ 4, l ^ 8 and l ^ 12 stand to one another as the
+// lanes of a quad do.
+template <int G>
 __device__ __forceinline__ uint32_t i8_d3(int lane, int j) {
   const int k = j >> 1, c = j & 1;
-  return static_cast<uint32_t>(((c ^ ((lane >> 1) & 1)) << 1) | (k ^ (lane & 1)));
+  const int lb = (G == 1024) ? (lane ^ (lane >> 2)) : lane;
+  return static_cast<uint32_t>(((c ^ ((lb >> 1) & 1)) << 1) | (k ^ (lb & 1)));
 }
 
 // Block (of 16 channels, within the warp tile) that slot j of the lane loads.
+//   G <= 16: block 32 j + lane.
+//   G >= 64: the quad q = lane / 4 holds blocks 16 q .. 16 q + 15, lane % 4 being the
+//   block's digit 2 and the slot's digit-3 value (i8_d3) its digit 3; for G = 1024, q % 4
+//   is digit 4 and q / 4 the 1024-group of the tile.
 template <int G>
 __device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
-  if constexpr (G == 16)
+  if constexpr (G <= 16)
     return static_cast<uint32_t>(32 * j + lane);
   else
-    return static_cast<uint32_t>((lane >> 2) * 16 + (lane & 3) + 4 * i8_d3(lane, j));
+    return static_cast<uint32_t>((lane >> 2) * 16 + (lane & 3) + 4 * i8_d3<G>(lane, j));
 }
 
 // Block that slot j holds after the rotation: each 4-point step leaves, in the
 // register that held input digit value d, the output of digit value 3 - d.
 template <int G>
 __device__ __forceinline__ uint32_t i8_out_block(int lane, int j) {
-  if constexpr (G == 16)
+  if constexpr (G <= 16)
     return static_cast<uint32_t>(32 * j + lane);
   else if constexpr (G == 64)
-    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * i8_d3(lane, j));
+    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * i8_d3<G>(lane, j));
+  else if constexpr (G == 256)
+    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * (3 - i8_d3<G>(lane, j)));
   else
-    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * (3 - i8_d3(lane, j)));
+    return static_cast<uint32_t>((lane >> 4) * 64 + (3 - ((lane >> 2) & 3)) * 16 + (3 - (lane & 3)) +
+                                 4 * (3 - i8_d3<G>(lane, j)));
+}
+
+// A 4-point step whose four values sit in the lanes l, l ^ M1, l ^ M2, l ^ (M1 | M2) (digit
+// value = the lane's bits at M1 and M2), in the same register slots: the sum
+// S = (v0 + v1) + (v2 + v3) of every position is reduced and scattered in two exchanges
+// (the lanes with digit values {0, 1} form v0 + v1 and those with {2, 3} form v2 + v3, on
+// half of the positions each, then every lane adds the other pair's sum on a quarter: the
+// slot map i8_d3 gives those halves and quarters their own registers in each lane), and
+// gathered back in two more.  Each lane then keeps its own input v_c and produces the
+// negated output of digit value 3 - c.  1.5 shuffles per value.
+template <int M1, int M2>
+__device__ __forceinline__ void i8_cross_step(Lane4& t) {
+  const float2 nh = make_float2(-0.5f, -0.5f);
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float2 r;
+    r.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, M1);
+    r.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, M1);
+    const float2 u = add2(t.P[0][i], r);  // the pair sum on this lane's P[0] positions
+    s[i] = __fadd_rn(u.x, __shfl_xor_sync(0xFFFFFFFFu, u.y, M2));
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 s0 = make_float2(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], M2));  // S on P[0]
+    float2 s1;                                                                    // S on P[1]
+    s1.x = __shfl_xor_sync(0xFFFFFFFFu, s0.x, M1);
+    s1.y = __shfl_xor_sync(0xFFFFFFFFu, s0.y, M1);
+    t.P[0][i] = fma2(s0, nh, t.P[0][i]);
+    t.P[1][i] = fma2(s1, nh, t.P[1][i]);
+  }
 }
 
 // The regular-Hadamard rotation of the lane's 4 blocks, digit by digit.
-// Returns +1 if the registers hold y, -1 if they hold -y.
+// Returns +1 if the registers hold y, -1 if they hold -y (an odd number of steps).
 template <int G>
 __device__ __forceinline__ float rotate_regular(Lane4& t) {
+  static_assert(G == 4 || G == 16 || G == 64 || G == 256 || G == 1024, "group");
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     // digit 0: channels 4b .. 4b+3 of a block
 #pragma unroll
     for (int b = 0; b < 4; ++b) h4_step(t.P[k][4 * b], t.P[k][4 * b + 1], t.P[k][4 * b + 2], t.P[k][4 * b + 3]);
-    // digit 1: channels b, b+4, b+8, b+12
+    if constexpr (G >= 16) {
+      // digit 1: channels b, b+4, b+8, b+12
 #pragma unroll
-    for (int b = 0; b < 4; ++b) h4_step(t.P[k][b], t.P[k][b + 4], t.P[k][b + 8], t.P[k][b + 12]);
+      for (int b = 0; b < 4; ++b) h4_step(t.P[k][b], t.P[k][b + 4], t.P[k][b + 8], t.P[k][b + 12]);
+    }
   }
-  if constexpr (G == 16) {
+  if constexpr (G == 4) {
+    return -1.0f;
+  } else if constexpr (G == 16) {
     return 1.0f;
   } else {
-    // digit 2: the four lanes of a quad hold its four values (lane % 4).  The sum
-    // S = (v0 + v1) + (v2 + v3) of every position is reduced and scattered in two
-    // exchanges (lanes 0,1 form v0 + v1 and lanes 2,3 form v2 + v3 on half of the
-    // positions each, then every lane adds the other pair's sum on a quarter), and
-    // gathered back in two more.  Each lane then keeps its own input v_c and
-    // produces the negated output of digit value 3 - c.
-    const float2 nh = make_float2(-0.5f, -0.5f);
-    float s[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float2 r;
-      r.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 1);
-      r.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 1);
-      const float2 u = add2(t.P[0][i], r);  // the pair sum on this lane's P[0] positions
-      s[i] = __fadd_rn(u.x, __shfl_xor_sync(0xFFFFFFFFu, u.y, 2));
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 s0 = make_float2(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], 2));  // S on P[0]
-      float2 s1;                                                                   // S on P[1]
-      s1.x = __shfl_xor_sync(0xFFFFFFFFu, s0.x, 1);
-      s1.y = __shfl_xor_sync(0xFFFFFFFFu, s0.y, 1);
-      t.P[0][i] = fma2(s0, nh, t.P[0][i]);
-      t.P[1][i] = fma2(s1, nh, t.P[1][i]);
-    }
+    i8_cross_step<1, 2>(t);  // digit 2: the four lanes of a quad (lane % 4)
     if constexpr (G == 64) {
       return -1.0f;
     } else {
       // digit 3: the lane's four slots; add2 pairs digit values {0,1} and {2,3}.
+      const float2 nh = make_float2(-0.5f, -0.5f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 u = add2(t.P[0][i], t.P[1][i]);
@@ -158,7 +184,12 @@ __device__ __forceinline__ float rotate_regular(Lane4& t) {
         t.P[0][i] = fma2(s2, nh, t.P[0][i]);
         t.P[1][i] = fma2(s2, nh, t.P[1][i]);
       }
-      return 1.0f;
+      if constexpr (G == 256) {
+        return 1.0f;
+      } else {
+        i8_cross_step<4, 8>(t);  // digit 4: the four quads of a 1024-group ((lane / 4) % 4)
+        return -1.0f;
+      }
     }
   }
 }
@@ -389,7 +420,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   };
 
   int64_t drained_from = 0;  // first tile whose copy may still be in flight
-  constexpr float kSign = (G == 64) ? -1.0f : 1.0f;  // the registers hold kSign * y
+  constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;  // registers hold kSign * y
   Cursor ca = {0, 0, 0};  // tile it (rotate)
   Cursor cb = {0, 0, 0};  // tile it - 1 (quantize)
   for (int64_t it = 0; it <= n_it; ++it) {
@@ -529,6 +560,99 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   if (wid == 0) {
     tmem_fence_after_sync();
     tmem_dealloc_all(tmem_base_slot);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rows longer than tensor memory can park (K > kI8MaxK).  A CTA of 16 warps takes
+// rows blockIdx.x, blockIdx.x + gridDim.x, ...; warp w takes the warp tiles w, w + 16,
+// ... of a row (at least one each, since T > 16).  Each row is read twice: the first
+// walk rotates the tiles and keeps only their amax; the CTA meets at a barrier (the
+// row's amax, one word per warp, double-buffered by row parity, so a warp can be at
+// most one row ahead of a reader); the second walk reads the tiles again, rotates and
+// quantizes them.  The second read mostly hits L2 (a row's x is K * 2 or 4 bytes per
+// CTA).  Loads are 16-byte vector loads straight into registers (contiguous or
+// strided rows alike); nothing waits except the CTA barrier, so no bound is needed.
+// ---------------------------------------------------------------------------
+template <int G, bool BF16>
+__global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Params p) {
+  constexpr int es = BF16 ? 2 : 4;
+  constexpr int n16 = BF16 ? 2 : 4;  // 16-byte words per block of 16 channels
+  constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int T = p.tiles_per_row;
+  __shared__ float row_max[2][kI8Warps];
+
+  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0).
+  auto load = [&](int64_t row, int chunk, Lane4& t) {
+    const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
+    const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
+    const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t bl = i8_in_block<G>(lane, j);
+      uint4 w4[n16];
+      const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+#pragma unroll
+      for (int k = 0; k < n16; ++k)
+        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + k) : make_uint4(0u, 0u, 0u, 0u);
+      float f[16];
+      widen<BF16>(w4, f);
+      put_block(t, j, f);
+    }
+    return nvalid;
+  };
+
+  int64_t n = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++n) {
+    // walk 1: the row's amax
+    float amax = 0.0f;
+    for (int chunk = wid; chunk < T; chunk += kI8Warps) {
+      Lane4 t;
+      load(row, chunk, t);
+      rotate_regular<G>(t);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
+    }
+    amax = warp_max_nonneg(amax);
+    if (lane == 0) row_max[n & 1][wid] = amax;
+    __syncthreads();
+    const float row_amax = warp_max_nonneg(lane < kI8Warps ? row_max[n & 1][lane] : 0.0f);
+    const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
+    const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
+    if (threadIdx.x == 0) p.scales[row] = scale;
+    // walk 2: the codes (rint by the magic constant, as in k_rotate_quant_int8)
+    const float2 inv2 = make_float2(inv, inv);
+    const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+    const float2 one2 = make_float2(1.0f, 1.0f);
+    for (int chunk = wid; chunk < T; chunk += kI8Warps) {
+      Lane4 t;
+      const int64_t nvalid = load(row, chunk, t);
+      rotate_regular<G>(t);
+      int8_t* qrow = p.q + row * p.K + static_cast<int64_t>(chunk) * kI8TileElems;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t bx[16], by[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+          bx[i] = __float_as_uint(w.x);
+          by[i] = __float_as_uint(w.y);
+        }
+        const uint32_t box = i8_out_block<G>(lane, 2 * k);
+        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
+        if (static_cast<int64_t>(box) * 16 < nvalid)
+          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
+                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
+                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
+        if (static_cast<int64_t>(boy) * 16 < nvalid)
+          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
+                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
+                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
+      }
+    }
   }
 }
 

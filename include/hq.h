@@ -247,16 +247,21 @@ HQ_API hq_status hq_dequant_mxfp4(const uint8_t* q, const uint8_t* scales, int64
  *   ("hyperflow_h3_flash_int8.py", HyperFlow: regular_hadamard, rotate_quant_kernel; the
  *    activation side of a W8A8 linear whose weight was rotated offline.)
  *
- *   y      = x . R_G on every run of G consecutive channels of a row, R_G = kron(H4/2, ...),
- *            H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]] (orthonormal, symmetric, rows
- *            summing to one).  Fixed fp32 order: the base-4 digits of the channel index from the
- *            least significant, each 4-point step out_k = RN(S/2 - v_(3-k)),
- *            S = (v0 + v1) + (v2 + v3).
+ *   y      = x . R_G on every run of G consecutive channels of a row, R_G = kron(H4/2, ...)
+ *            (log4 G factors), H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]] (orthonormal,
+ *            symmetric, rows summing to one).  Fixed fp32 order: the base-4 digits of the
+ *            channel index from the least significant, each 4-point step out_k = RN(S/2 -
+ *            v_(3-k)), S = (v0 + v1) + (v2 + v3).  (The page's group of 1024 is computed from
+ *            its 16 x 64 factors; the Kronecker power is the same matrix, and the digit order
+ *            fixes the rounding.)
  *   scales : fp32 [M], scale = max(amax_row |y|, 1e-12) / 127.
  *   q      : int8 [M, K] row-major, q = clamp(rint(y * (1/scale)), -127, 127) (half to even).
- *   x is read once; the rotated row stays on chip.
+ *   For K <= 32768, x is read once and the rotated row stays on chip (tensor memory); a longer
+ *   row is read twice, first for its amax and then to quantize it (the second read mostly
+ *   from L2).
  *
- *   group  : 16, 64 or 256; K a multiple of group and at most 32768.
+ *   group  : 4, 16, 64, 256 or 1024; K a multiple of the group and of 16 (the kernels move
+ *            whole 16-channel blocks), K / 2048 below 2^30.
  *   x      : [M, K] of dtype, row stride ldx (16-byte aligned; ldx * sizeof(dtype) % 16 == 0).
  *   q      : 16-byte aligned.   scales : 4-byte aligned.
  */

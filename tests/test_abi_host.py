@@ -210,9 +210,11 @@ def test_int8_argument_checks(lib):
         return lib.hq_rotate_quant_int8(P(x) if x else None, dt, M, K, ldx, G, P(q) if q else None,
                                         P(s) if s else None, None)
     assert i8(x=0) == 1 and i8(q=0) == 1 and i8(s=0) == 1
-    assert i8(G=32) == 5 and i8(G=0) == 5 and i8(G=4) == 5
+    assert i8(G=32) == 5 and i8(G=0) == 5 and i8(G=8) == 5 and i8(G=2048) == 5
     assert i8(dt=2) == 4
-    assert i8(K=48, ldx=48, G=64) == 2 and i8(K=32768 + 256, ldx=32768 + 256, G=256) == 2
+    assert i8(K=48, ldx=48, G=64) == 2 and i8(K=1536, ldx=1536, G=1024) == 2
+    assert i8(K=36, ldx=36, G=4) == 2          # a multiple of 4 but not of 16
+    assert i8(K=2 ** 41, ldx=2 ** 41, M=1, G=1024) == 2   # 2^30 warp tiles per row
     assert i8(ldx=32) == 2 and i8(M=-1) == 2
     assert i8(x=FAKE + 8) == 3 and i8(q=FAKE + 4) == 3 and i8(s=FAKE + 2) == 3
     assert i8(ldx=68) == 3                     # 136-byte bf16 row stride

@@ -1,8 +1,11 @@
 """INT8 per-token rotate-quant (hq_rotate_quant_int8) against the oracle, bit-exact.
 
-"hyperflow_h3_flash_int8.py" (HyperFlow): regular_hadamard, rotate_quant_kernel.  Shapes cover
-one and several warp tiles per row (2048 channels each), ragged last tiles, 1 to 16 rows per CTA
-step, both input types, strided rows, zero rows (the 1e-12 floor) and extreme magnitudes.
+"hyperflow_h3_flash_int8.py" (HyperFlow): regular_hadamard, hadamard_factors,
+rotate_quant_kernel, rotate_quant.  Groups 4, 16, 64, 256 and 1024 (the page's group sizes:
+powers of 4).  Shapes cover one and several warp tiles per row (2048 channels each), ragged last
+tiles, 1 to 16 rows per CTA step, rows longer than tensor memory parks (K > 32768: each row
+read twice), both input types, strided rows, zero rows (the 1e-12 floor) and extreme
+magnitudes.
 """
 import numpy as np
 import pytest
@@ -50,7 +53,12 @@ def check(x_host, group, x_dev=None):
 
 SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16), (9, 2304, 256),
           (100, 4096, 64), (7, 32768, 256), (1000, 1024, 16), (301, 3072, 64), (64, 6144, 256),
-          (40, 30720, 16)]
+          (40, 30720, 16),
+          # group 4 (one digit), group 1024 (five digits, two of them across lanes)
+          (2, 16, 4), (37, 2064, 4), (5, 1024, 1024), (13, 3072, 1024), (8, 32768, 1024),
+          # rows longer than tensor memory parks: 17 warp tiles, a ragged 18th, 32 and 48
+          (3, 34816, 16), (5, 36864 + 1024, 1024), (4, 65536, 256), (2, 98304 + 16, 4),
+          (3, 65536, 64)]
 
 
 @pytest.mark.parametrize("M,K,group", SHAPES)
@@ -59,16 +67,24 @@ def test_int8_parity(M, K, group, dtype):
     check(rand_input(M, K, dtype, seed=M + K + group), group)
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 def test_int8_strided_rows(group):
     big = rand_input(300, 4096 + 512, torch.bfloat16, seed=4)
     check(big[:, :4096].contiguous(), group, x_dev=big.cuda()[:, :4096])
 
 
+@pytest.mark.parametrize("group", [16, 1024])
+def test_int8_long_rows_strided_and_many(group):
+    """Rows of 65536 channels (each read twice), strided, more rows than SMs."""
+    big = rand_input(400, 65536 + 1024, torch.bfloat16, seed=7)
+    check(big[:, :65536].contiguous(), group, x_dev=big.cuda()[:, :65536])
+
+
 @pytest.mark.parametrize("scale", [1e-30, 1e-14, 1e30])
 def test_int8_extreme_magnitudes(scale):
-    for group in (16, 64, 256):
+    for group in (4, 16, 64, 256, 1024):
         check(rand_input(50, 1024, torch.float32, seed=9, scale=scale), group)
+    check(rand_input(3, 40960, torch.float32, seed=10, scale=scale), 256)   # a long row
 
 
 def test_int8_llm_sized_workload():
@@ -84,7 +100,7 @@ def test_int8_empty_and_limits():
     q, s = hq.hq_rotate_quant_int8(x, 256)
     assert q.numel() == 0
     with pytest.raises(hq.HQError):
-        hq.hq_rotate_quant_int8(torch.zeros(2, 32768 + 256, device="cuda", dtype=torch.bfloat16), 256)
+        hq.hq_rotate_quant_int8(torch.zeros(2, 1536, device="cuda", dtype=torch.bfloat16), 1024)
 
 
 def _tie_row(group):
@@ -114,9 +130,10 @@ def _tie_row(group):
     raise AssertionError("no tie case found")
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 def test_int8_rint_of_rounded_product(group):
     """q = rint(RN(y * (1/scale))): the product is rounded before rint."""
     row = _tie_row(group)
+    row = np.concatenate([row, np.zeros(-row.size % 16, np.float32)])  # whole 16-channel blocks
     x = torch.from_numpy(np.tile(row, (4, 1)))
     check(x, group)

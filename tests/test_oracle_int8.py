@@ -24,18 +24,27 @@ def kron_power(n):
     return r
 
 
-@pytest.mark.parametrize("group", [4, 16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 def test_rotation_is_the_pages_kronecker_power(oracle_lib, group):
     R = int8_rotate(np.eye(group, dtype=np.float32), group).astype(np.float64)
     assert np.array_equal(R, kron_power(group))
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 def test_rotation_properties_from_the_docstring(oracle_lib, group):
     R = int8_rotate(np.eye(group, dtype=np.float32), group).astype(np.float64)
     assert np.array_equal(R @ R.T, np.eye(group))       # orthonormal
     assert np.array_equal(R, R.T)                       # symmetric
     assert np.array_equal(R.sum(axis=1), np.ones(group))  # rows sum to one
+
+
+def test_factoring_of_1024_as_16_by_64(oracle_lib):
+    # HyperFlow's hadamard_factors computes a group of 1024 as factors 16 and 64: the
+    # Kronecker product of the two smaller rotations is the group-1024 rotation.
+    R = int8_rotate(np.eye(1024, dtype=np.float32), 1024).astype(np.float64)
+    R16 = int8_rotate(np.eye(16, dtype=np.float32), 16).astype(np.float64)
+    R64 = int8_rotate(np.eye(64, dtype=np.float32), 64).astype(np.float64)
+    assert np.array_equal(R, np.kron(R16, R64)) and np.array_equal(R, np.kron(R64, R16))
 
 
 def test_factoring_of_256(oracle_lib):
@@ -46,7 +55,7 @@ def test_factoring_of_256(oracle_lib):
     assert np.array_equal(R, np.kron(Ra, Rb))
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 def test_fp32_evaluation_matches_dense_product(oracle_lib, group):
     rng = np.random.default_rng(group)
     x = rng.standard_normal((32, 4 * group)).astype(np.float32)
@@ -57,7 +66,7 @@ def test_fp32_evaluation_matches_dense_product(oracle_lib, group):
     assert np.max(np.abs(y - ref) / norms) < 1e-6
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 @pytest.mark.parametrize("c", [1.0, -7.5, 3e-8, 2e30])
 def test_single_channel_closed_form(oracle_lib, group, c):
     K = 2 * group
@@ -79,7 +88,7 @@ def test_zero_row_uses_the_floor(oracle_lib):
     assert s[1] == floor       # amax 1e-20 / 2 is below 1e-12
 
 
-@pytest.mark.parametrize("group", [16, 64, 256])
+@pytest.mark.parametrize("group", [4, 16, 64, 256, 1024])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_codes_are_nearest_integers_within_the_bound(oracle_lib, group, dtype):
     import torch
