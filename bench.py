@@ -1,18 +1,18 @@
 """Benchmark: fused Hadamard rotation + NVFP4 quantization on GB300.
 
 One step = the whole hot path over one activation tensor already resident in HBM, as
-hq_quantize_nvfp4 runs it: pass 1 (rotate, global amax) then pass 2 (rotate, block scales,
-codes).  For an x of more than 64 MiB these are two launches, hq_rot_amax then
-hq_rotate_quant_nvfp4; a smaller x runs both as one cooperative kernel.  The metric is GB/s
-of algorithmic bytes in + out per step:
+hq_quantize_nvfp4 runs it with a workspace: pass 1 (rotate, global amax, reduced into the
+workspace) then pass 2 (rotate, block scales, codes; tiles handed out at run time), two
+launches chained by programmatic dependent launch.  The metric is GB/s of algorithmic bytes
+in + out per step:
     bytes = M*K*sizeof(x)  (x read)  +  M*K/2 (codes)  +  M*K/16 (E4M3 scales).
 Default workload: x bf16 [32768, 28672] (1.88 GB, larger than L2, so no flush is needed
 between steps), N(0,1) with 0.5% outlier channels x100, seed 3, rotation group 16.
 
 Also reported on the same JSON line:
-  roofline      the dominant kernel (pass 2, or the one kernel of a one-launch step): its
-                algorithmic bytes / its average launch time (CUDA events around every launch
-                in the timed region), against the measured HBM copy bandwidth;
+  roofline      the dominant kernel (pass 2): its algorithmic bytes / its average launch time
+                (CUDA events around every launch in an instrumented run of the step), against
+                the measured HBM copy bandwidth;
   e2e           the same metric through the public API with host buffers: pinned host x ->
                 device, both passes, codes + scales + s_global -> pinned host, every step;
   cpu_baseline  the CPU oracle on a bounded sample of the workload, on this host's cores;
@@ -278,21 +278,50 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------------- GPU arm -----
 
-def _median_ms(fn_batch, reps: int) -> float:
-    """Median over `reps` runs of fn_batch(), which returns milliseconds per launch."""
-    return statistics.median(fn_batch() for _ in range(reps))
+def graph_ms_per_call(fn, calls: int, reps: int, dev) -> float:
+    """Median milliseconds per call of fn, from `reps` replays of a CUDA graph that holds
+    `calls` calls in a row (captured once; the replays have no host work between launches, so
+    short kernels are not starved by the Python binding's per-call cost)."""
+    import torch
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):  # warm-up outside the capture (grid sizes, attributes)
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) / calls)
+    del g
+    return statistics.median(times)
 
 
-def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: int = 200,
+def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: int = 100,
                     reps: int = 5) -> dict:
-    """Every named workload and rotation mode, timed the same way: pass 2 alone, pass 1 alone and
-    the whole step (hq_quantize_nvfp4 with a workspace), each as `launches` launches back to
-    back between two CUDA events on the launching stream, median of `reps` such runs.
+    """Every named workload and rotation mode, timed the same way: pass 2 alone (as the step
+    runs it, hq_rotate_quant_nvfp4_ws), pass 1 alone (hq_rot_amax) and the whole step
+    (hq_quantize_nvfp4 with a workspace), each as `launches` calls back to back in one CUDA
+    graph, median of `reps` replays timed by CUDA events.
 
     Inputs larger than L2 are read from HBM by construction.  For an input that L2 holds, the
-    launches cycle through enough copies of x and of the outputs that each launch reads an x
-    last touched at least three L2 capacities earlier; the same kernels are also timed cold, one
-    launch per event pair after an L2 flush (the flush outside the pair), which adds the launch
+    calls cycle through enough copies of x and of the outputs that each call reads an x last
+    touched at least three L2 capacities earlier; the same calls are also timed cold, one call
+    per event pair after an L2 flush (the flush outside the pair), which adds the launch
     latency to every figure.  `have` maps workload names to device tensors already made."""
     import torch
 
@@ -316,13 +345,14 @@ def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: i
         a1 = torch.empty(1, dtype=torch.float32, device=dev)
         sg = torch.empty(1, dtype=torch.float32, device=dev)
         ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
+        ws2 = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
         entry = {"workload": w.describe(), "M": w.M, "K": w.K, "input_dtype": w.dtype,
                  "bytes_per_step": nb,
-                 "timing": ("inputs larger than L2, back to back" if not small else
-                            (f"back to back over {copies} copies of x and the outputs "
-                             f"({copies * nb / 1e6:.0f} MB), no flush; cold: L2 flushed before "
-                             "each launch, one event pair per launch" if copies > 1 else
-                             "cold only: L2 flushed before each launch, one event pair per launch")),
+                 "timing": ("inputs larger than L2; calls back to back in a CUDA graph" if not small else
+                            (f"calls back to back in a CUDA graph over {copies} copies of x and the "
+                             f"outputs ({copies * nb / 1e6:.0f} MB), no flush; cold: L2 flushed "
+                             "before each call, one event pair per call" if copies > 1 else
+                             "cold only: L2 flushed before each call, one event pair per call")),
                  "groups": {}}
         for group in w.groups:
             hq.hq_rot_amax(x0, group, amax=amax, stream=stream)
@@ -333,25 +363,27 @@ def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: i
                 i[0] += 1
                 return k
 
+            # the calls take the current stream, so that a graph capture records them
             def p2():  # pass 2 as the step runs it (run-time tile split from 16384 tiles on)
                 k = nxt()
                 hq.hq_rotate_quant_nvfp4_ws(xs[k], group, amax, q=qs[k], scales=ss[k], s_global=sg,
-                                            workspace=ws, stream=stream)
+                                            workspace=ws2)
 
             def p1():
-                hq.hq_rot_amax(xs[nxt()], group, amax=a1, stream=stream)
+                hq.hq_rot_amax(xs[nxt()], group, amax=a1)
 
             def st():
                 k = nxt()
                 hq.hq_quantize_nvfp4(xs[k], group, amax=a1, q=qs[k], scales=ss[k], s_global=sg,
-                                     fused=True, workspace=ws, stream=stream)
+                                     workspace=ws)
 
             g = {}
             for key, fn in (("pass2", p2), ("pass1", p1), ("step", st)):
                 if copies > 1 or not small:
-                    g[f"{key}_ms"] = _median_ms(lambda: time_launches(fn, launches, stream, dev, None), reps)
+                    i[0] = 0
+                    g[f"{key}_ms"] = graph_ms_per_call(fn, launches, reps, dev)
                 if small:
-                    g[f"{key}_cold_ms"] = time_launches(fn, 50, stream, dev, flush)
+                    g[f"{key}_cold_ms"] = time_launches(fn, 50, torch.cuda.current_stream(dev), dev, flush)
             for suffix in ("", "_cold"):
                 if f"pass2{suffix}_ms" not in g:
                     continue
@@ -362,14 +394,12 @@ def measure_configs(hq, synth, dev, stream, peak: float, have: dict, launches: i
                 g[f"pass1{suffix}_gbs_read"] = bin_ / (p1ms / 1e3) / 1e9
                 g[f"step{suffix}_gbs"] = nb / (stms / 1e3) / 1e9
                 g[f"step{suffix}_gbs_both_reads"] = (2 * bin_ + bout) / (stms / 1e3) / 1e9
-            g["step_path"] = ("one cooperative kernel" if bin_ <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
-                              else "pass 1 then pass 2, two launches")
+            g["step_path"] = "pass 1 then pass 2, two launches"
             entry["groups"]["off" if group == 0 else str(group)] = g
         out[name] = entry
         del xs, qs, ss, x0
         torch.cuda.empty_cache()
     return out
-
 
 
 def run_ours(args, w):
@@ -409,10 +439,8 @@ def run_ours(args, w):
     if bytes_in + bytes_out < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # The step is one hq_quantize_nvfp4 call with a workspace: for an x of at most 64 MiB one
-    # cooperative kernel (both passes, x re-read from L2), otherwise pass 1 then pass 2 as two
+    # The step is one hq_quantize_nvfp4 call with a workspace: pass 1 then pass 2 as two
     # launches, pass 1 reducing into the workspace (no memset before it).
-    fused = bytes_in <= hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
     ws2 = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
 
@@ -424,8 +452,8 @@ def run_ours(args, w):
                                     stream=stream)
 
     def step():
-        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, fused=True,
-                             workspace=ws, stream=stream)
+        hq.hq_quantize_nvfp4(x, group, amax=amax, q=q, scales=s, s_global=sg, workspace=ws,
+                             stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -471,24 +499,19 @@ def run_ours(args, w):
     value = throughput_gbs(step_bytes, K, world, region_ms)
 
     # ---- the passes, from a second run of the same step with an event between them ----
-    if fused:
-        # the passes on their own, beside the step (the step runs them as one kernel)
-        pass1_ms = [time_launches(pass1, K, stream, dev, flush)]
-        pass2_ms = [time_launches(pass2, K, stream, dev, flush)]
-    else:
-        evp = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-        for i in range(K):
-            evp[i][0].record(stream)
-            pass1()
-            evp[i][1].record(stream)
-            pass2()
-            evp[i][2].record(stream)
-            if flush is not None:
-                flush.fill_(1.0)
-        torch.cuda.synchronize(dev)
-        pass1_ms = [evp[i][0].elapsed_time(evp[i][1]) for i in range(K)]
-        pass2_ms = [evp[i][1].elapsed_time(evp[i][2]) for i in range(K)]
-        instrumented_step_ms = sum(evp[i][0].elapsed_time(evp[i][2]) for i in range(K)) / K
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        evp[i][0].record(stream)
+        pass1()
+        evp[i][1].record(stream)
+        pass2()
+        evp[i][2].record(stream)
+        if flush is not None:
+            flush.fill_(1.0)
+    torch.cuda.synchronize(dev)
+    pass1_ms = [evp[i][0].elapsed_time(evp[i][1]) for i in range(K)]
+    pass2_ms = [evp[i][1].elapsed_time(evp[i][2]) for i in range(K)]
+    instrumented_step_ms = sum(evp[i][0].elapsed_time(evp[i][2]) for i in range(K)) / K
 
     # ---- single-pass mode (delayed amax): one kernel per step, reported beside the step ----
     # each call quantizes with the amax the previous call reduced (two buffers alternate)
@@ -576,15 +599,15 @@ def run_ours(args, w):
     swz["frac_of_peak"] = swz["gbs"] / peak
     p2 = sum(pass2_ms) / len(pass2_ms)
     p1 = sum(pass1_ms) / len(pass1_ms)
-    # the dominant kernel: pass 2, or the one kernel of the step
-    dom_ms = step_ms if fused else p2
+    # the dominant kernel: pass 2
+    dom_ms = p2
     achieved = step_bytes / (dom_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((src_hash, w.name, group))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "traffic_kernel_source": src_hash if traffic is not None else None,
-                "kernel": "k_quant_nvfp4_fused" if fused else "k_rotate_quant_nvfp4",
+                "kernel": "k_rotate_quant_nvfp4",
                 "peak_source": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
@@ -598,18 +621,15 @@ def run_ours(args, w):
                           else "L2 flushed between steps (256 MB write, outside the step time)"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
-        "step_path": ("hq_quantize_nvfp4: one cooperative kernel (x at most 64 MiB)" if fused
-                      else "hq_quantize_nvfp4: pass 1 then pass 2, two launches"),
+        "step_path": "hq_quantize_nvfp4: pass 1 then pass 2, two launches",
         "passes": {"pass1_ms": p1, "pass2_ms": p2,
                    "pass1_gbs_read": bytes_in / (p1 / 1e3) / 1e9,
                    "pass2_gbs": step_bytes / (p2 / 1e3) / 1e9,
                    "pass2_frac_of_nominal_8000": step_bytes / (p2 / 1e3) / 1e9 / 8000.0,
                    "step_gbs_both_reads": (2 * bytes_in + bytes_out) / (step_ms / 1e3) / 1e9,
-                   "timed": ("beside the step, as separate launches" if fused else
-                             "a second run of the step, CUDA events before, between and after "
+                   "timed": ("a second run of the step, CUDA events before, between and after "
                              "the passes (each event adds about 2 us)"),
-                   "two_launch_step_ms": p1 + p2 if fused else None,
-                   "instrumented_step_ms": None if fused else instrumented_step_ms},
+                   "instrumented_step_ms": instrumented_step_ms},
         "single_pass_delayed": {
             "ms_per_step": single_ms, "gbs": step_bytes / (single_ms / 1e3) / 1e9,
             "frac_of_peak": step_bytes / (single_ms / 1e3) / 1e9 / peak,
@@ -623,7 +643,7 @@ def run_ours(args, w):
                 "ms_per_step": e2e_ms / e2e_steps, "api": "HostQuantizer (hq_host_pipeline_*)",
                 "timer": "host clock, wait() at the end"},
         "configs": configs,
-        "gpu_launches": K if fused else 2 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
         "kernel_source": src_hash,
     }

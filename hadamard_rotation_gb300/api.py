@@ -95,7 +95,6 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
 # per (device, stream).
 _WORKSPACES: dict[tuple[int, int], torch.Tensor] = {}
 HQ_QUANTIZE_WORKSPACE_WORDS = 288
-HQ_QUANTIZE_FUSED_MAX_BYTES = 64 * 1024 * 1024
 
 
 def _workspace(device: torch.device, stream: torch.cuda.Stream | None) -> torch.Tensor:
@@ -130,20 +129,20 @@ def hq_rotate_quant_nvfp4_ws(x: torch.Tensor, group: int, amax: torch.Tensor,
 
 def hq_quantize_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor | None = None,
                       q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
-                      s_global: torch.Tensor | None = None, fused: bool = True,
+                      s_global: torch.Tensor | None = None, use_workspace: bool = True,
                       workspace: torch.Tensor | None = None,
                       stream: torch.cuda.Stream | None = None):
     """Both passes in one call: (q, scales, s_global, amax), as hq_rot_amax then
-    hq_rotate_quant_nvfp4.  With ``fused`` (default), an x of contiguous rows and at most
-    HQ_QUANTIZE_FUSED_MAX_BYTES runs as one cooperative kernel; its workspace (int32
-    [HQ_QUANTIZE_WORKSPACE_WORDS], zero before first use) defaults to one this binding keeps
-    per device and stream."""
+    hq_rotate_quant_nvfp4.  With ``use_workspace`` (default) the call passes a workspace (int32
+    [HQ_QUANTIZE_WORKSPACE_WORDS], zero before first use; default: one this binding keeps per
+    device and stream): pass 1 reduces the amax into it without a memset and pass 2 takes its
+    tiles at run time; without, the plain hq_rot_amax then hq_rotate_quant_nvfp4."""
     dt, M, K, ldx = _x_args(x)
     amax = _need(amax, (1,), torch.float32, x.device, "amax")
     q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
     scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
     s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
-    if fused:
+    if use_workspace:
         workspace = _workspace(x.device, stream) if workspace is None else _need(
             workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
     else:
@@ -291,9 +290,8 @@ def hq_quantize_nvfp4_host_noalloc(x_host: torch.Tensor, group: int,
 
 def hq_read_fault(clear: bool = False) -> int:
     """The device fault word (waits for the device to be idle); bit 0: a kernel's bounded wait
-    (for one of its own tile copies, or at hq_quantize_nvfp4's grid barrier) ran out.  ``clear``
-    resets it after reading, and zeroes the hq_quantize_nvfp4 workspaces this binding keeps on
-    the current device (a fault can leave one non-zero)."""
+    for one of its own tile copies ran out.  ``clear`` resets it after reading, and zeroes the
+    workspaces this binding keeps on the current device (a fault can leave one non-zero)."""
     v = ctypes.c_uint(0)
     check(_lib.load().hq_read_fault(ctypes.byref(v), 1 if clear else 0), "hq_read_fault")
     if clear:
@@ -308,7 +306,7 @@ def hq_read_fault(clear: bool = False) -> int:
 def hq_selftest_bounded_wait(unit: int = 0, stream: torch.cuda.Stream | None = None) -> None:
     """Enqueue the bounded-wait self-test (one warp waits on a barrier nothing completes, gives
     up after about a second and records bit 0 of the fault word).  unit 0: the NVFP4 / MXFP4
-    kernels' translation unit, 1: the INT8 kernel's, 2: hq_quantize_nvfp4's grid barrier."""
+    kernels' translation unit, 1: the INT8 kernel's."""
     check(_lib.load().hq_selftest_bounded_wait(unit, _stream_handle(stream)), "hq_selftest_bounded_wait")
 
 

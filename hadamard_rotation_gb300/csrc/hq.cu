@@ -33,15 +33,6 @@ __global__ void k_selftest_bounded_wait() {
   if (!__all_sync(0xFFFFFFFFu, ok) && threadIdx.x == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
 }
 
-// The grid barrier of k_quant_nvfp4_fused with one arrival more than the grid
-// can give: the wait runs out.
-__device__ unsigned g_selftest_count;
-
-__global__ void k_selftest_grid_barrier() {
-  if (threadIdx.x == 0) atomicExch(&g_selftest_count, 0u);
-  grid_barrier(&g_selftest_count, gridDim.x + 1);
-}
-
 }  // namespace hq
 
 namespace {
@@ -236,9 +227,8 @@ hq_status check_x(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx,
   return HQ_OK;
 }
 
-// Workspace words (HQ_QUANTIZE_WORKSPACE_WORDS in all): [0] grid-barrier arrivals of the
-// one-launch kernel, [1] amax bits, [2] CTAs done with [0] and [1], [3] warps done with the
-// tile counters; then the tile counters of the run-time split from word kSchedWord on, each on
+// Workspace words (HQ_QUANTIZE_WORKSPACE_WORDS in all): [0] unused, [1] pass 1's amax bits,
+// [2] CTAs of pass 1 done, [3] warps done with the tile counters; then the tile counters of the run-time split from word kSchedWord on, each on
 // its own 128-byte line.  A call that records no fault leaves every word 0.
 constexpr int kSchedWord = hq::kSchedStrideWords;
 static_assert(kSchedWord + hq::kSchedClasses * hq::kSchedStrideWords <= HQ_QUANTIZE_WORKSPACE_WORDS,
@@ -350,24 +340,6 @@ hq_status dispatch_quant_swizzled(const hq::Params& p, bool bf16, hq_stream s) {
                 ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, false));
 }
 
-// Both passes in one cooperative launch (k_quant_nvfp4_fused): the dynamic shared
-// memory holds the larger of the two TMA rings.
-template <int G>
-hq_status launch_fused(hq::Params p, bool bf16, hq_stream s) {
-  void (*fn)(hq::Params) = bf16 ? hq::k_quant_nvfp4_fused<G, true> : hq::k_quant_nvfp4_fused<G, false>;
-  const size_t r1 = ring_bytes<HQ_PASS1_STAGES>(hq::kLoadTma, bf16);
-  const size_t r2 = ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, bf16);
-  const size_t smem = r1 > r2 ? r1 : r2;
-  unsigned grid = 0;
-  cudaError_t e = persistent_grid(reinterpret_cast<const void*>(fn), p.n_tiles, smem, &grid);
-  if (e != cudaSuccess) return cuda_fail(e);
-  void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(hq::kThreads),
-                                  args, smem, static_cast<cudaStream_t>(s));
-  if (e != cudaSuccess) return cuda_fail(e);
-  return HQ_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -443,57 +415,39 @@ hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
     if (!aligned(q, 16) || !aligned(scales, 4) || (s_global && !aligned(s_global, 4)))
       return HQ_ERR_ALIGN;
   }
-  const bool fused = workspace && M > 0 && K > 0 && !is_strided(M, K, ldx) &&
-                     M * K <= HQ_QUANTIZE_FUSED_MAX_BYTES / elem_size(dtype);
-  if (!fused) {
-    if (workspace && M > 0 && K > 0) {
-      // Pass 1 reduces into the workspace (0 on entry) and its last CTA writes *amax, so no
-      // memset separates it from the kernel before it: it is launched as a programmatic
-      // dependent and waits for that kernel's completion before it reads x.
-      hq::Params p = base_params(x, dtype, M, K, ldx);
-      p.amax_out = reinterpret_cast<float*>(workspace + 1);
-      p.sync = workspace;
-      p.amax_copy = amax;
-      const bool bf16 = dtype == HQ_BF16;
-      const bool strided = is_strided(M, K, ldx);
-      switch (group) {
-        case 0: st = dispatch_rot_amax<0>(p, bf16, strided, false, stream); break;
-        case 16: st = dispatch_rot_amax<16>(p, bf16, strided, false, stream); break;
-        default: st = dispatch_rot_amax<256>(p, bf16, strided, false, stream); break;
-      }
-    } else {
-      st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
-    }
+  if (!workspace || M == 0 || K == 0) {
+    st = hq_rot_amax(x, dtype, M, K, ldx, group, amax, nullptr, stream);
     if (st != HQ_OK) return st;
-    if (!workspace)
-      return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
-    // Pass 2 as hq_rotate_quant_nvfp4_ws; since the pass 1 above released it only after
-    // waiting for x's producer, it fetches its first tiles of x before it waits for pass 1.
-    hq::Params p = base_params(x, dtype, M, K, ldx);
-    p.amax_in = amax;
-    p.q = q;
-    p.s = scales;
-    p.sglobal_out = s_global;
-    if (schedulable(p, workspace, is_strided(M, K, ldx))) {
-      p.sched = workspace + kSchedWord;
-      p.sched_done = workspace + 3;
-    }
-    p.x_ready = 1;
-    return dispatch_quant_group(p, group, dtype == HQ_BF16, is_strided(M, K, ldx), stream);
+    return hq_rotate_quant_nvfp4(x, dtype, M, K, ldx, group, amax, q, scales, s_global, stream);
   }
+  const bool bf16 = dtype == HQ_BF16;
+  const bool strided = is_strided(M, K, ldx);
+  // Pass 1 reduces into the workspace (0 on entry) and its last CTA writes *amax, so no
+  // memset separates it from the kernel before it: it is launched as a programmatic
+  // dependent and waits for that kernel's completion before it reads x.
+  hq::Params p1 = base_params(x, dtype, M, K, ldx);
+  p1.amax_out = reinterpret_cast<float*>(workspace + 1);
+  p1.sync = workspace;
+  p1.amax_copy = amax;
+  switch (group) {
+    case 0: st = dispatch_rot_amax<0>(p1, bf16, strided, false, stream); break;
+    case 16: st = dispatch_rot_amax<16>(p1, bf16, strided, false, stream); break;
+    default: st = dispatch_rot_amax<256>(p1, bf16, strided, false, stream); break;
+  }
+  if (st != HQ_OK) return st;
+  // Pass 2 as hq_rotate_quant_nvfp4_ws; since pass 1 released it only after waiting for x's
+  // producer, it fetches its first tiles of x before it waits for pass 1.
   hq::Params p = base_params(x, dtype, M, K, ldx);
+  p.amax_in = amax;
   p.q = q;
   p.s = scales;
   p.sglobal_out = s_global;
-  p.sync = workspace;
-  p.amax_out = reinterpret_cast<float*>(workspace + 1);
-  p.amax_copy = amax;
-  const bool bf16 = dtype == HQ_BF16;
-  switch (group) {
-    case 0: return launch_fused<0>(p, bf16, stream);
-    case 16: return launch_fused<16>(p, bf16, stream);
-    default: return launch_fused<256>(p, bf16, stream);
+  if (schedulable(p, workspace, strided)) {
+    p.sched = workspace + kSchedWord;
+    p.sched_done = workspace + 3;
   }
+  p.x_ready = 1;
+  return dispatch_quant_group(p, group, bf16, strided, stream);
 }
 
 int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K) {
@@ -694,15 +648,12 @@ hq_status hq_read_fault(unsigned int* fault, int clear) {
 }
 
 hq_status hq_selftest_bounded_wait(int unit, hq_stream stream) {
-  if (unit < 0 || unit > 2) return HQ_ERR_SHAPE;
+  if (unit < 0 || unit > 1) return HQ_ERR_SHAPE;
   if (unit == 1) {
     const cudaError_t e = hq::int8_selftest_bounded_wait(static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? HQ_OK : cuda_fail(e);
   }
-  if (unit == 2)
-    hq::k_selftest_grid_barrier<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
-  else
-    hq::k_selftest_bounded_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  hq::k_selftest_bounded_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? HQ_OK : cuda_fail(e);
 }

@@ -9,7 +9,6 @@
 //   k_rot_amax            pass 1 in tiles (G = 256, strided rows, or a rotated output).
 //   k_rotate_quant_nvfp4  pass 2: stream x once, rotate in registers, block amax,
 //                         E4M3 block scale, E2M1 codes, write codes + scales once.
-//   k_quant_nvfp4_fused   both passes in one cooperative launch, for an x L2 holds.
 //   k_rotate_quant_mxfp4  MXFP4 (E8M0 scale per 32 values), one pass.
 //   k_dequant_nvfp4       round trip: codes * scales, optional inverse rotation.
 //
@@ -118,10 +117,9 @@ struct Params {
   uint64_t rows;           // M (row-group tiles)
   uint32_t n_cc;           // row-group tiles: column chunks of 16 blocks per row, ceil(K/256)
   FastDiv div_ncc;         // divider for n_cc
-  // both passes in one launch (k_quant_nvfp4_fused)
-  unsigned* sync;          // [0] CTAs past pass 1, [1] amax bits, [2] CTAs done; 0 on entry and exit
-                           // (pass 1 with a workspace: [1] amax bits, [2] CTAs done)
-  float* amax_copy;        // the tensor's amax, written once it is known
+  // pass 1 with a workspace (hq_quantize_nvfp4)
+  unsigned* sync;          // [1] amax bits, [2] CTAs done; 0 on entry and exit
+  float* amax_copy;        // the tensor's amax, written by the last CTA
   // run-time tile split (for_each_tile, DYN): kSchedClasses counters kSchedStrideWords apart
   // and the count of warps done with them, all 0 on entry and put back to 0 by the last warp
   unsigned* sched;
@@ -289,12 +287,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // x is streamed once: its lines are the first to leave L2.
-__device__ __forceinline__ uint64_t l2_keep_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 __device__ __forceinline__ uint64_t l2_stream_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -645,14 +637,13 @@ __device__ __forceinline__ void sched_retire(const Params& p) {
 // warp's first copies have been issued, so that work the tiles need (reading the amax,
 // building the divisor table) overlaps their flight instead of delaying it.  Every warp of
 // the CTA calls it, so it may hold a __syncthreads().
-// KEEP_L2: read x with an L2 evict-last hint (it is read again soon) instead of
-// evict-first.  REVERSE (fixed split only): the k-th tile of the sequence is tile
+// x is read with an L2 evict-first hint (it is streamed once).  REVERSE (fixed split only):
+// the k-th tile of the sequence is tile
 // n_tiles - 1 - k, so the pass walks x from its end (pass 1 of the two-launch path: pass 2
 // walks it from the start, and each pass then begins where the previous one ended, with
 // that part of x still in L2).
-template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool KEEP_L2 = false, bool S1 = false,
-          bool REVERSE = false, bool GDC = false, bool DYN = false, typename Body,
-          typename Pre = NoPrologue>
+template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool S1 = false, bool REVERSE = false,
+          bool GDC = false, bool DYN = false, typename Body, typename Pre = NoPrologue>
 __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
   static_assert(!(DYN && (REVERSE || MODE != kLoadTma)), "run-time split: TMA ring, forward walk");
   const int lane = threadIdx.x & 31;
@@ -677,7 +668,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
     uint8_t* ring = hq_smem + wid * R::kStages * R::kTileBytes;
     const uint32_t ring_s = smem_addr(ring);
     const uint32_t bar0 = smem_addr(hq_smem + R::kDataBytes) + wid * R::kStages * 8;
-    const uint64_t policy = KEEP_L2 ? l2_keep_policy() : l2_stream_policy();
+    const uint64_t policy = l2_stream_policy();
 
     auto issue = [&](uint64_t seq, int slot) {
       const uint64_t first = tile_of(seq) * kTileBlocks;
@@ -1126,7 +1117,7 @@ __device__ __forceinline__ float absmax256_x(Lane4& t, int lane) {
 
 // This thread's max |z| (unscaled butterfly output) over its tiles of x; y is
 // written too when WRITE_Y.
-template <int G, bool BF16, int MODE, bool WRITE_Y, bool KEEP_L2 = false>
+template <int G, bool BF16, int MODE, bool WRITE_Y>
 __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
   // Without a rotated output, the 256-group takes slot order 1 and skips the
   // last stage's outputs (absmax256_x).
@@ -1135,9 +1126,8 @@ __device__ __forceinline__ float rot_amax_tiles(const Params& p) {
   // (widen_stage1_bf16), with or without a rotated output.
   constexpr bool kS1 = BF16 && G == 256;
   float zmax = 0.0f;
-  // Two launches: walk x from its end (for_each_tile, REVERSE).  One launch (KEEP_L2):
-  // x stays in L2 either way.
-  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, KEEP_L2, kS1, !KEEP_L2>(
+  // Walk x from its end (for_each_tile, REVERSE): pass 2 walks it from the start.
+  for_each_tile<G, BF16, MODE, HQ_PASS1_STAGES, kAbsTrick ? 1 : 0, kS1, true>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kAbsTrick) {
       zmax = max_nan(zmax, absmax256_x<kS1>(t, lane));
@@ -1281,41 +1271,6 @@ __global__ void __launch_bounds__(kThreads, HQ_STREAM_DEPTH == 1 ? 4 : 3) k_rot_
 }
 
 // ---------------------------------------------------------------------------
-// Grid barrier for a cooperative launch (every CTA resident).  Thread 0 of each
-// CTA adds 1 to *count after its earlier global writes and waits, about one
-// second at most, until *count reaches `target` (gridDim.x: all CTAs arrived).
-// Returns false to every thread of the CTA when the wait ran out
-// (kFaultWaitTimeout is recorded).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ bool grid_barrier(unsigned* count, unsigned target) {
-  __shared__ int ok_s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(count, 1u);
-    int ok = 1;
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire_gpu(count) < target) {
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(&g_hq_fault, kFaultWaitTimeout);
-        ok = 0;
-        break;
-      }
-      __nanosleep(64);
-    }
-    ok_s = ok;
-  }
-  __syncthreads();
-  return ok_s != 0;
-}
-
-// ---------------------------------------------------------------------------
 // Pass 2: rotate + quantize + pack.
 // ---------------------------------------------------------------------------
 // SWZ: write the scales in the swizzled tile layout of block-scaled NVFP4 GEMMs
@@ -1324,8 +1279,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned* count, unsigned target) {
 // tiles row-major; inside a tile, row r and column c at (r % 32) * 16 + (r / 32) *
 // 4 + c.  The tiles of this mode are row groups (RgTile), so that every scale
 // store fills whole 32-byte pieces of that layout, padding included.
-// amax: where the global amax is read, once the first tile copies are in flight (global
-// memory for pass 2, shared memory in the one-launch kernel).
+// amax: where the global amax is read, once the first tile copies are in flight.
 // GDC: the kernel was launched as a programmatic dependent and has not yet executed
 // griddepcontrol.wait; the tile loop does.
 template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false, bool GDC = false,
@@ -1529,7 +1483,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
   if constexpr (SWZ)
     for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body, prologue);
   else
-    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, false, kS1, false, GDC, DYN>(p, tile_body, prologue);
+    for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1, false, GDC, DYN>(p, tile_body, prologue);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
 }
 
@@ -1546,38 +1500,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   } else {
     rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ, true, DYN>(p, p.amax_in);
   }
-}
-
-// Both passes in one cooperative launch, for an x that L2 holds: pass 1 reads x
-// through the TMA ring with an evict-last hint and reduces the amax into
-// p.sync[1]; the CTAs meet at a grid barrier; pass 2 reads x again (from L2, now
-// evict-first) with that amax.  The last CTA to finish zeroes p.sync[0..2] for the
-// next call.  Results are those of k_rot_amax followed by k_rotate_quant_nvfp4.
-template <int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, BF16 ? 2 : 1) k_quant_nvfp4_fused(Params p) {
-  __shared__ float amax_s;
-  unsigned* const arrived = p.sync;
-  unsigned* const amax_bits = p.sync + 1;
-  unsigned* const done = p.sync + 2;
-  const float zmax = rot_amax_tiles<G, BF16, kLoadTma, false, true>(p);
-  cta_amax_to_global(__fmul_rn(zmax, inv_sqrt_g<G>()), reinterpret_cast<float*>(amax_bits));
-  const bool ok = grid_barrier(arrived, gridDim.x);
-  if (threadIdx.x == 0) {
-    const float a = __uint_as_float(ld_acquire_gpu(amax_bits));
-    amax_s = a;
-    if (ok && blockIdx.x == 0) *p.amax_copy = a;
-    // Every read of p.sync by this CTA is done: count it out.
-    __threadfence();
-    if (atomicAdd(done, 1u) == gridDim.x - 1) {
-      __threadfence();
-      atomicExch(arrived, 0u);
-      atomicExch(amax_bits, 0u);
-      atomicExch(done, 0u);
-    }
-  }
-  __syncthreads();
-  if (!ok) return;
-  rotate_quant_tiles<G, BF16, kLoadTma, false>(p, &amax_s);
 }
 
 // ---------------------------------------------------------------------------
@@ -1604,7 +1526,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
   constexpr float c = inv_sqrt_g<G>();
   constexpr int kOrder = G == 256 ? 2 : 0;
   constexpr bool kS1 = BF16 && G == 256;
-  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, false, kS1>(
+  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kOrder == 2)
       rotate_tile_x256<kS1>(t, lane);

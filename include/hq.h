@@ -112,8 +112,6 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
-/* Tensors of x of at most this many bytes take hq_quantize_nvfp4's one-launch path. */
-#define HQ_QUANTIZE_FUSED_MAX_BYTES (64ll * 1024 * 1024)
 /* Size of the workspace of hq_quantize_nvfp4 and hq_rotate_quant_nvfp4_ws, in 32-bit words
  * (control words and the counters of the run-time tile schedule, each on its own 128-byte
  * line). */
@@ -125,15 +123,12 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
  *   ("A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2: the global scale needs the
  *    amax of the whole rotated tensor before any block is quantized, hence two passes over x.)
  *
- *   When x's rows are back to back, x takes at most HQ_QUANTIZE_FUSED_MAX_BYTES and `workspace`
- *   is given, the two passes run as one cooperative kernel: the first reads x with an L2
- *   evict-last hint, all CTAs meet at a grid-wide barrier once the amax is reduced, and the
- *   second reads x back from L2.  Otherwise the call is two launches, pass 1 then pass 2 as
- *   hq_rotate_quant_nvfp4.  With `workspace`, pass 1 reduces the amax into the workspace and
- *   its last CTA writes *amax (no memset before it), pass 2 is hq_rotate_quant_nvfp4_ws (tiles
- *   handed out at run time), and both launches are programmatic dependents of the kernel
- *   before them on the stream (each waits for that kernel to complete before it reads
- *   memory); without, pass 1 is hq_rot_amax and pass 2 hq_rotate_quant_nvfp4.
+ *   Two launches, pass 1 then pass 2.  With `workspace`, pass 1 reduces the amax into the
+ *   workspace and its last CTA writes *amax (no memset before it); pass 2 is
+ *   hq_rotate_quant_nvfp4_ws (tiles handed out at run time) and fetches its first tiles of x
+ *   while pass 1 ends; both launches are programmatic dependents of the kernel before them on
+ *   the stream (each waits for that kernel to complete before it reads what the kernel
+ *   wrote).  Without, pass 1 is hq_rot_amax and pass 2 hq_rotate_quant_nvfp4.
  *
  *   x, dtype, M, K, ldx, group : as for hq_rot_amax.
  *   amax      : 1 float on the device (written; 0 for an empty tensor).
@@ -142,8 +137,6 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
  *               uint32 on the device, 4-byte aligned, all 0 before its first use (e.g.
  *               cudaMemset).  Each call that records no fault leaves it 0 again.  Calls that may
  *               run at the same time (different streams) need different workspaces.
- *   A grid barrier that waits about a second without all CTAs arriving records bit 0 of the
- *   fault word (hq_read_fault); those CTAs skip the second pass and the outputs are undefined.
  */
 HQ_API hq_status hq_quantize_nvfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
                                    int64_t ldx, int group, float* amax, uint8_t* q,
@@ -309,9 +302,8 @@ HQ_API hq_status hq_read_fault(unsigned int* fault, int clear);
  * word and returns; no memory is touched and the context stays usable.  Returns once the launch
  * is enqueued (read the result with hq_read_fault).
  *   unit : 0 runs the wait in the translation unit of the NVFP4 / MXFP4 kernels, 1 in that of
- *          the INT8 kernel (each has its own copy of the fault word; hq_read_fault reads both),
- *          2 is hq_quantize_nvfp4's grid-barrier wait, in one CTA waiting for one arrival more
- *          than the grid holds.  Anything else: HQ_ERR_SHAPE.
+ *          the INT8 kernel (each has its own copy of the fault word; hq_read_fault reads both).
+ *          Anything else: HQ_ERR_SHAPE.
  */
 HQ_API hq_status hq_selftest_bounded_wait(int unit, hq_stream stream);
 

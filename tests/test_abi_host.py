@@ -259,7 +259,7 @@ def test_swizzled_argument_checks_and_size(lib):
 
 
 def test_selftest_argument_check(lib):
-    assert lib.hq_selftest_bounded_wait(3, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
+    assert lib.hq_selftest_bounded_wait(2, None) == 2 and lib.hq_selftest_bounded_wait(-1, None) == 2
 
 
 def test_binding_has_every_abi_call_under_the_same_name():
@@ -301,9 +301,7 @@ def test_binding_constants_match_the_header():
 
     text = open(HEADER).read()
     words = re.search(r"#define HQ_QUANTIZE_WORKSPACE_WORDS (\d+)", text)
-    limit = re.search(r"#define HQ_QUANTIZE_FUSED_MAX_BYTES \((\d+)ll \* 1024 \* 1024\)", text)
     assert words and int(words.group(1)) == api.HQ_QUANTIZE_WORKSPACE_WORDS
-    assert limit and int(limit.group(1)) * 1024 * 1024 == api.HQ_QUANTIZE_FUSED_MAX_BYTES
 
 
 def test_noalloc_argument_checks_and_size_limit(lib):

@@ -1,9 +1,11 @@
-"""hq_quantize_nvfp4, both passes in one call, against the CPU oracle.
+"""hq_quantize_nvfp4, both passes in one call (two launches), against the CPU oracle.
 
-For an x of contiguous rows that fits in L2 the call runs both passes as one cooperative kernel
-with a grid barrier between them; otherwise it is the two launches.  Either way amax, s_global,
-codes and scales must be bit-exact with the oracle, and the workspace must be back to zero after
-every call (the next call relies on it).
+With a workspace, pass 1 reduces the amax into it (no memset) and pass 2 takes its tiles from the
+workspace's counters (from 16384 warp tiles on) and fetches its first tiles while pass 1 ends;
+without, the plain hq_rot_amax then hq_rotate_quant_nvfp4.  Either way amax, s_global, codes and
+scales must be bit-exact with the oracle, and the workspace must be back to zero after every call
+(the next call relies on it).  hq_rotate_quant_nvfp4_ws, pass 2 with the run-time split, is
+tested here too.
 """
 import numpy as np
 import pytest
@@ -14,8 +16,6 @@ import oracle
 from hadamard_rotation_gb300 import synth
 
 pytestmark = pytest.mark.gpu
-
-LIMIT = hq.api.HQ_QUANTIZE_FUSED_MAX_BYTES
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -80,7 +80,7 @@ SHAPES = [(1, 256), (2, 16 * 16), (129, 256), (77, 4096), (1000, 1024), (4099, 5
 @pytest.mark.parametrize("M,K", SHAPES)
 @pytest.mark.parametrize("group", [0, 16, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_fused_matches_oracle(M, K, group, dtype):
+def test_quantize_matches_oracle(M, K, group, dtype):
     x_host = rand_input(M, K, dtype, seed=M * 3 + K + group)
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     got = hq.hq_quantize_nvfp4(x_host.cuda(), group, workspace=ws)
@@ -100,12 +100,12 @@ def test_named_4096x4096_workload(group):
     names = kernels_launched(lambda: hq.quantize_nvfp4(x, group))
     if names is None:
         pytest.skip("the profiler sees no CUDA kernels here")
-    assert any("k_quant_nvfp4_fused" in n for n in names), names
+    assert len(names) == 2 and "k_rot_amax" in names[0] and "k_rotate_quant_nvfp4" in names[1], names
 
 
 def test_repeated_calls_reuse_the_workspace():
     """A large-amax tensor, then a small-amax one, then the first again, with one workspace:
-    each amax is exact, so the accumulator and the barrier count were reset in between."""
+    each amax is exact, so the accumulator and the CTA count were reset in between."""
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     xs = [rand_input(300, 2048, torch.bfloat16, seed=5, scale=100.0),
           rand_input(300, 2048, torch.bfloat16, seed=6, scale=0.01),
@@ -118,30 +118,12 @@ def test_repeated_calls_reuse_the_workspace():
             assert settled(ws)
 
 
-@pytest.mark.parametrize("rows", [8192, 8193])
-def test_size_limit_both_sides(rows):
-    """bf16 [8192, 4096] is exactly the one-launch limit; one row more takes two launches.
-    Both are exact."""
-    K = 4096
-    x_host = rand_input(rows, K, torch.bfloat16, seed=rows)
-    x = x_host.cuda()
-    assert (rows * K * 2 <= LIMIT) == (rows == 8192)
-    got = hq.quantize_nvfp4(x, 16)
-    torch.cuda.synchronize()
-    check(x_host, 16, got, f"bf16 [{rows}, {K}]")
-    names = kernels_launched(lambda: hq.quantize_nvfp4(x, 16))
-    if names is None:
-        pytest.skip("the profiler sees no CUDA kernels here")
-    fused = any("k_quant_nvfp4_fused" in n for n in names)
-    assert fused == (rows == 8192), names
-
-
 def test_two_launches_with_a_workspace_leave_it_zero():
     """Strided rows always take the two launches; with a workspace, pass 1 reduces the amax
     into it (no memset before the launch) and its last CTA writes amax.  A large, a small and
     a large amax in turn, every group and both input types (the streaming pass 1 needs
-    contiguous rows, so the tiled one runs here; the 8193-row case above covers the streaming
-    one): every result exact and the workspace back to 0 after each call."""
+    contiguous rows, so the tiled one runs here; the next test covers the streaming one): every
+    result exact and the workspace back to 0 after each call."""
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     for dtype in (torch.bfloat16, torch.float32):
         for i, scale in enumerate((100.0, 0.01, 100.0)):
@@ -156,8 +138,9 @@ def test_two_launches_with_a_workspace_leave_it_zero():
 
 
 def test_streaming_pass_1_with_a_workspace_in_a_row():
-    """Contiguous bf16 rows above the one-launch limit: the streaming pass 1 reduces into the
-    workspace.  Two different tensors in a row on one workspace, both exact, workspace 0."""
+    """Contiguous bf16 rows: the streaming pass 1 reduces into the workspace, and pass 2 (16400
+    warp tiles) takes the run-time split.  Two different tensors in a row on one workspace, both
+    exact, workspace 0."""
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     for seed, scale in ((51, 7.0), (52, 0.003)):
         x_host = rand_input(8200, 4096, torch.bfloat16, seed=seed, scale=scale)
@@ -168,12 +151,12 @@ def test_streaming_pass_1_with_a_workspace_in_a_row():
 
 
 def test_two_launch_modes_agree():
-    """fused=False (no workspace: the two launches) and strided rows (always two launches) give
-    the same bytes as the one-launch path."""
+    """Without a workspace (hq_rot_amax then hq_rotate_quant_nvfp4) and on strided rows (the
+    fixed split) the bytes are those of the workspace path."""
     x_host = rand_input(640, 3072, torch.bfloat16, seed=17)
     x = x_host.cuda()
     a = hq.hq_quantize_nvfp4(x, 16)
-    b = hq.hq_quantize_nvfp4(x, 16, fused=False)
+    b = hq.hq_quantize_nvfp4(x, 16, use_workspace=False)
     big = torch.zeros(640, 3072 + 256, dtype=torch.bfloat16, device="cuda")
     big[:, :3072] = x
     c = hq.hq_quantize_nvfp4(big[:, :3072], 16)
@@ -220,33 +203,34 @@ def test_two_streams_at_once():
         check(xs[i], 16, outs[i], f"stream {i}")
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_cuda_graph_capture_and_replay(fused):
+@pytest.mark.parametrize("use_ws", [True, False])
+def test_cuda_graph_capture_and_replay(use_ws):
     """Both paths captured in a CUDA graph and replayed on new contents of the same input
-    buffer: every replay is exact (the one-launch workspace is zero again after each)."""
-    xs = [rand_input(1024, 2048, torch.bfloat16, seed=70 + i, scale=10.0 ** (i - 1)) for i in range(3)]
+    buffer: every replay is exact (the workspace, whose pass 2 takes the run-time split on this
+    tensor of 16384 warp tiles, is zero again after each)."""
+    xs = [rand_input(4096, 8192, torch.bfloat16, seed=70 + i, scale=10.0 ** (i - 1)) for i in range(3)]
     x = xs[0].cuda()
     amax = torch.empty(1, device="cuda")
-    q = torch.empty((1024, 1024), dtype=torch.uint8, device="cuda")
-    s = torch.empty((1024, 128), dtype=torch.uint8, device="cuda")
+    q = torch.empty((4096, 4096), dtype=torch.uint8, device="cuda")
+    s = torch.empty((4096, 512), dtype=torch.uint8, device="cuda")
     sg = torch.empty(1, device="cuda")
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):  # warm-up outside the capture (grid sizes, attributes)
-        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
-                             workspace=ws if fused else None, stream=side)
+        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, use_workspace=use_ws,
+                             workspace=ws if use_ws else None, stream=side)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, fused=fused,
-                             workspace=ws if fused else None)
+        hq.hq_quantize_nvfp4(x, 16, amax=amax, q=q, scales=s, s_global=sg, use_workspace=use_ws,
+                             workspace=ws if use_ws else None)
     for i, x_host in enumerate(xs):
         x.copy_(x_host.cuda())
         g.replay()
         torch.cuda.synchronize()
-        check(x_host, 16, (q, s, sg, amax), f"replay {i} fused={fused}")
+        check(x_host, 16, (q, s, sg, amax), f"replay {i} workspace={use_ws}")
         assert settled(ws)
 
 
