@@ -512,7 +512,8 @@ __device__ __forceinline__ void load_tile_global(const Params& p, uint64_t tile_
 }
 
 // Loads from a tile staged in shared memory (block b of the tile at b*16*es).
-template <int G, bool BF16, int ORDER = 0, bool S1 = false>
+// FULL: the caller knows that all kTileBlocks blocks of the tile lie inside the tensor.
+template <int G, bool BF16, int ORDER = 0, bool S1 = false, bool FULL = false>
 __device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t tile_base, uint64_t nb,
                                                int lane, bool (&valid)[4], Lane4& t) {
   constexpr int es = BF16 ? 2 : 4;
@@ -521,7 +522,7 @@ __device__ __forceinline__ void load_tile_smem(const uint8_t* slot, uint64_t til
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const uint32_t bl = slot_block<G, ORDER>(lane, s);
-    valid[s] = tile_base + bl < nb;
+    valid[s] = FULL || tile_base + bl < nb;
     uint4 w4[n16];
     if (valid[s]) {
       const uint4* src = reinterpret_cast<const uint4*>(slot + bl * 16u * es);
@@ -615,6 +616,20 @@ __device__ __forceinline__ void sched_retire(const Params& p) {
   }
 }
 
+// body(tile_base, lane, valid, t), compiled twice: for a tile whose blocks all lie inside the
+// tensor (every tile but the last) `valid` is a constant, so the body's per-block checks and
+// branches drop out of the path that runs for all other tiles.
+template <typename Tile, typename Body>
+__device__ __forceinline__ void call_body(bool full, const Tile& tile, int lane, bool (&valid)[4], Lane4& t,
+                                          Body& body) {
+  if (full) {
+    bool all[4] = {true, true, true, true};
+    body(tile, lane, all, t);
+  } else {
+    body(tile, lane, valid, t);
+  }
+}
+
 // Run `body(tile_base, lane, valid, t)` over this warp's tiles with the tile's values in
 // registers.
 //
@@ -646,6 +661,9 @@ template <int G, bool BF16, int MODE, int STAGES, int ORDER = 0, bool S1 = false
           bool GDC = false, bool DYN = false, typename Body, typename Pre = NoPrologue>
 __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
   static_assert(!(DYN && (REVERSE || MODE != kLoadTma)), "run-time split: TMA ring, forward walk");
+  // The 256-group's quantizing tile bodies (layout ORDER 2) are compiled a second time for
+  // whole tiles (call_body); elsewhere the single form measured as fast or faster.
+  constexpr bool kSplitFull = G == 256 && ORDER == 2;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const uint64_t gw = static_cast<uint64_t>(blockIdx.x) * kWarpsPerCta + wid;
@@ -711,9 +729,13 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
           return;
         }
         const uint64_t base = tile_of(seq) * kTileBlocks;
+        const bool full = kSplitFull && p.nb - base >= kTileBlocks;  // the same in every lane
         bool valid[4];
         Lane4 t;
-        load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        if (full)
+          load_tile_smem<G, BF16, ORDER, S1, true>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        else
+          load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
         __syncwarp();  // every lane has read the slot
         const uint64_t next = seq + R::kStages * nw;
         if (next < p.n_tiles) {
@@ -723,7 +745,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
           }
           ++issued;
         }
-        body(base, lane, valid, t);
+        call_body(full, base, lane, valid, t, body);
       }
     } else {
       // Lane 0's schedule: queue[s] is the tile held by the s-th slot to be read (kNoTile:
@@ -766,9 +788,13 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
           return;
         }
         const uint64_t base = cur * kTileBlocks;
+        const bool full = kSplitFull && p.nb - base >= kTileBlocks;  // the same in every lane
         bool valid[4];
         Lane4 t;
-        load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        if (full)
+          load_tile_smem<G, BF16, ORDER, S1, true>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
+        else
+          load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, base, p.nb, lane, valid, t);
         __syncwarp();  // every lane has read the slot
         if (lane == 0) {
           uint64_t nt = kNoTile;
@@ -789,7 +815,7 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
           for (int s = 0; s + 1 < R::kStages; ++s) queue[s] = queue[s + 1];
           queue[R::kStages - 1] = nt;
         }
-        body(base, lane, valid, t);
+        call_body(full, base, lane, valid, t, body);
       }
     }
   }
