@@ -539,13 +539,16 @@ def run_ours(args, w):
     mx = None
     if w.K % 32 == 0:
         s_mx = torch.empty((w.M, w.K // 32), dtype=torch.uint8, device=dev)
-        mx_ms = time_launches(lambda: hq.hq_rotate_quant_mxfp4(x, group, q=q, scales=s_mx, stream=stream),
+        ws_mx = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
+        mx_ms = time_launches(lambda: hq.hq_rotate_quant_mxfp4_ws(x, group, q=q, scales=s_mx,
+                                                                  workspace=ws_mx, stream=stream),
                               K, stream, dev, flush)
         mx_bytes = bytes_in + w.numel // 2 + w.numel // 32
         mx = {"group": group, "ms_per_launch": mx_ms, "bytes_per_launch": mx_bytes,
               "gbs": mx_bytes / (mx_ms / 1e3) / 1e9,
-              "note": "hq_rotate_quant_mxfp4 (one pass: no global scale)"}
-        del s_mx
+              "note": "hq_rotate_quant_mxfp4_ws (one pass: no global scale; tiles handed out at "
+                      "run time)"}
+        del s_mx, ws_mx
 
     # ---- INT8 per-token rotate-quant (regular Hadamard, G = 256) on the same tensor ----
     int8 = None

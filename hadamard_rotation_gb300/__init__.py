@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     hq_rot_amax,
     hq_rotate_quant_int8,
     hq_rotate_quant_mxfp4,
+    hq_rotate_quant_mxfp4_ws,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
     hq_rotate_quant_nvfp4_swizzled,
@@ -36,6 +37,7 @@ __all__ = [
     "hq_rot_amax",
     "hq_rotate_quant_int8",
     "hq_rotate_quant_mxfp4",
+    "hq_rotate_quant_mxfp4_ws",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
     "hq_rotate_quant_nvfp4_swizzled",

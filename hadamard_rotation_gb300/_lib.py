@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
         lib.hq_swizzled_scales_bytes.restype = i64
         lib.hq_rotate_quant_mxfp4.argtypes = [p, i32, i64, i64, i64, i32, p, p, p]
         lib.hq_rotate_quant_mxfp4.restype = i32
+        lib.hq_rotate_quant_mxfp4_ws.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p]
+        lib.hq_rotate_quant_mxfp4_ws.restype = i32
         lib.hq_dequant_mxfp4.argtypes = [p, p, i64, i64, i32, i32, p, p]
         lib.hq_dequant_mxfp4.restype = i32
         lib.hq_rotate_quant_int8.argtypes = [p, i32, i64, i64, i64, i32, p, p, p]

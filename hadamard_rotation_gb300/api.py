@@ -91,7 +91,7 @@ def hq_rotate_quant_nvfp4(x: torch.Tensor, group: int, amax: torch.Tensor,
     return q, scales, s_global
 
 
-# The workspaces of hq_quantize_nvfp4 and hq_rotate_quant_nvfp4_ws kept by this binding, one
+# The workspaces of hq_quantize_nvfp4 and the _ws entry points kept by this binding, one
 # per (device, stream).
 _WORKSPACES: dict[tuple[int, int], torch.Tensor] = {}
 HQ_QUANTIZE_WORKSPACE_WORDS = 288
@@ -207,6 +207,23 @@ def hq_rotate_quant_mxfp4(x: torch.Tensor, group: int, q: torch.Tensor | None = 
     scales = _need(scales, (M, K // 32), torch.uint8, x.device, "scales")
     _call(x.device, "hq_rotate_quant_mxfp4", _ptr(x), dt, M, K, ldx, group, _ptr(q), _ptr(scales),
           stream=stream)
+    return q, scales
+
+
+def hq_rotate_quant_mxfp4_ws(x: torch.Tensor, group: int, q: torch.Tensor | None = None,
+                             scales: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None,
+                             stream: torch.cuda.Stream | None = None):
+    """MXFP4 as hq_rotate_quant_mxfp4, with the tiles handed to the warps at run time from the
+    counters in ``workspace`` (as hq_rotate_quant_nvfp4_ws; default: the one this binding keeps
+    per device and stream)."""
+    dt, M, K, ldx = _x_args(x)
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 32), torch.uint8, x.device, "scales")
+    workspace = _workspace(x.device, stream) if workspace is None else _need(
+        workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
+    _call(x.device, "hq_rotate_quant_mxfp4_ws", _ptr(x), dt, M, K, ldx, group, _ptr(q),
+          _ptr(scales), _ptr(workspace), stream=stream)
     return q, scales
 
 

@@ -551,11 +551,13 @@ hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float*
   }
 }
 
-hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
-                                int group, uint8_t* q, uint8_t* scales, hq_stream stream) {
+hq_status hq_rotate_quant_mxfp4_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                                   int group, uint8_t* q, uint8_t* scales, uint32_t* workspace,
+                                   hq_stream stream) {
   hq_status st = check_x(x, dtype, M, K, ldx, group);
   if (st != HQ_OK) return st;
   if (K % 32 != 0) return HQ_ERR_SHAPE;
+  if (workspace && !aligned(workspace, 4)) return HQ_ERR_ALIGN;
   if (M == 0 || K == 0) return HQ_OK;
   if (!q || !scales) return HQ_ERR_NULL;
   if (!aligned(q, 16)) return HQ_ERR_ALIGN;
@@ -564,28 +566,42 @@ hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_
   p.s = scales;
   const bool bf16 = dtype == HQ_BF16;
   const bool strided = is_strided(M, K, ldx);
+  if (schedulable(p, workspace, strided)) {
+    p.sched = workspace + kSchedWord;
+    p.sched_done = workspace + 3;
+  }
   using hq::k_rotate_quant_mxfp4;
   constexpr int kMode = HQ_PASS2_MODE;
-  auto go = [&](auto k_strided, auto k_flat, size_t smem) {  // programmatic dependent launch
-    return strided ? launch(k_strided, p, stream, 0, true) : launch(k_flat, p, stream, smem, true);
+  // programmatic dependent launch; contiguous rows through the TMA ring take the run-time
+  // split when the workspace allows it
+  auto go = [&](auto k_strided, auto k_flat, auto k_dyn, size_t smem) {
+    if (strided) return launch(k_strided, p, stream, 0, true);
+    if (kMode == hq::kLoadTma && p.sched != nullptr) return launch(k_dyn, p, stream, smem, true);
+    return launch(k_flat, p, stream, smem, true);
   };
+  const size_t smem = bf16 ? ring_bytes<HQ_PASS2_STAGES>(kMode, true) : ring_bytes<HQ_PASS2_STAGES>(kMode, false);
   switch (group) {
     case 0:
       return bf16 ? go(k_rotate_quant_mxfp4<0, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<0, true, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                       k_rotate_quant_mxfp4<0, true, hq::kLoadTma, true>, smem)
                   : go(k_rotate_quant_mxfp4<0, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<0, false, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+                       k_rotate_quant_mxfp4<0, false, hq::kLoadTma, true>, smem);
     case 16:
       return bf16 ? go(k_rotate_quant_mxfp4<16, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<16, true, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                       k_rotate_quant_mxfp4<16, true, hq::kLoadTma, true>, smem)
                   : go(k_rotate_quant_mxfp4<16, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<16, false, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+                       k_rotate_quant_mxfp4<16, false, hq::kLoadTma, true>, smem);
     default:
       return bf16 ? go(k_rotate_quant_mxfp4<256, true, hq::kLoadStrided>, k_rotate_quant_mxfp4<256, true, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, true))
+                       k_rotate_quant_mxfp4<256, true, hq::kLoadTma, true>, smem)
                   : go(k_rotate_quant_mxfp4<256, false, hq::kLoadStrided>, k_rotate_quant_mxfp4<256, false, kMode>,
-                       ring_bytes<HQ_PASS2_STAGES>(kMode, false));
+                       k_rotate_quant_mxfp4<256, false, hq::kLoadTma, true>, smem);
   }
+}
+
+hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K, int64_t ldx,
+                                int group, uint8_t* q, uint8_t* scales, hq_stream stream) {
+  return hq_rotate_quant_mxfp4_ws(x, dtype, M, K, ldx, group, q, scales, nullptr, stream);
 }
 
 hq_status hq_dequant_mxfp4(const uint8_t* q, const uint8_t* scales, int64_t M, int64_t K,

@@ -1544,7 +1544,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
 // other half of a 32-block sits in lane ^ 3, in the other register of the P[0] / P[1]
 // pair (block bit 0 is lane bit 0 and block bits 1 and 3 are unchanged), and bf16
 // tiles arrive with the first butterfly stage applied.
-template <int G, bool BF16, int MODE>
+// DYN: the run-time tile split of for_each_tile (tile counters in p.sched).
+template <int G, bool BF16, int MODE, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
   // Launched with programmatic dependent launch, as pass 2: wait for the kernel before this
   // one on the stream to complete before any access to global memory.
@@ -1552,7 +1553,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_mxfp4(Params p) {
   constexpr float c = inv_sqrt_g<G>();
   constexpr int kOrder = G == 256 ? 2 : 0;
   constexpr bool kS1 = BF16 && G == 256;
-  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1>(
+  for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1, false, false, DYN>(
       p, [&](uint64_t base, int lane, bool (&valid)[4], Lane4& t) {
     if constexpr (kOrder == 2)
       rotate_tile_x256<kS1>(t, lane);

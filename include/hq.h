@@ -112,7 +112,8 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
-/* Size of the workspace of hq_quantize_nvfp4 and hq_rotate_quant_nvfp4_ws, in 32-bit words
+/* Size of the workspace of hq_quantize_nvfp4, hq_rotate_quant_nvfp4_ws and
+ * hq_rotate_quant_mxfp4_ws, in 32-bit words
  * (control words and the counters of the run-time tile schedule, each on its own 128-byte
  * line). */
 #define HQ_QUANTIZE_WORKSPACE_WORDS 288
@@ -229,6 +230,18 @@ HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, in
 HQ_API hq_status hq_rotate_quant_mxfp4(const void* x, hq_dtype dtype, int64_t M, int64_t K,
                                        int64_t ldx, int group, uint8_t* q, uint8_t* scales,
                                        hq_stream stream);
+
+/*
+ * hq_rotate_quant_mxfp4_ws -- hq_rotate_quant_mxfp4 exactly (same arguments, same outputs), with
+ *   the tiles of x handed to the warps at run time as in hq_rotate_quant_nvfp4_ws (a schedule,
+ *   not a step of the method).
+ *   workspace : as for hq_rotate_quant_nvfp4_ws (HQ_QUANTIZE_WORKSPACE_WORDS uint32, all 0
+ *               before its first use and left 0 by each call that records no fault; one per
+ *               stream that may run at the same time).  NULL: hq_rotate_quant_mxfp4.
+ */
+HQ_API hq_status hq_rotate_quant_mxfp4_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                          int64_t ldx, int group, uint8_t* q, uint8_t* scales,
+                                          uint32_t* workspace, hq_stream stream);
 
 /* hq_dequant_mxfp4 -- value = (+-grid[code & 7]) * 2^(byte - 127), then the rotation again when
  * `unrotate` (group 16 or 256).  out: fp32 [M, K], 16-byte aligned; q 8-byte aligned. */

@@ -230,6 +230,14 @@ def test_mxfp4_argument_checks(lib):
     assert mx(K=48, ldx=48) == 2             # not a multiple of 32
     assert mx(G=64) == 5 and mx(dt=5) == 4
     assert mx(q=FAKE + 8) == 3 and mx(x=FAKE + 4) == 3
+
+    def mxw(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, q=FAKE, s=FAKE, ws=FAKE + 256):
+        return lib.hq_rotate_quant_mxfp4_ws(P(x) if x else None, dt, M, K, ldx, G, P(q) if q else None,
+                                            P(s) if s else None, P(ws) if ws else None, None)
+    assert mxw(x=0) == 1 and mxw(q=0) == 1 and mxw(s=0) == 1
+    assert mxw(K=48, ldx=48) == 2 and mxw(G=64) == 5 and mxw(dt=5) == 4
+    assert mxw(ws=FAKE + 2) == 3 and mxw(q=FAKE + 8) == 3
+    assert mxw(M=0) == 0 and mxw(M=0, ws=0) == 0
     assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 48, 0, 0, P(FAKE), None) == 2
     assert lib.hq_dequant_mxfp4(None, P(FAKE), 4, 64, 0, 0, P(FAKE), None) == 1
     assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 64, 0, 1, P(FAKE), None) == 5

@@ -1,4 +1,5 @@
-"""MXFP4 (hq_rotate_quant_mxfp4 / hq_dequant_mxfp4) against the oracle, bit-exact.
+"""MXFP4 (hq_rotate_quant_mxfp4, hq_rotate_quant_mxfp4_ws / hq_dequant_mxfp4) against the oracle,
+bit-exact.
 
 "A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §1 (MXFP4: 32-element blocks, E8M0
 power-of-two scales) and "Try this" (the error study with MXFP4 semantics); scale rule as the
@@ -35,10 +36,15 @@ def rand_input(M, K, dtype, seed, scale=1.0):
     return t if dtype == torch.float32 else t.to(dtype)
 
 
-def check(x_host, group, x_dev=None, roundtrip=False):
+def check(x_host, group, x_dev=None, roundtrip=False, ws=None):
     x = x_dev if x_dev is not None else x_host.cuda()
-    q, s = hq.hq_rotate_quant_mxfp4(x, group)
+    if ws is None:
+        q, s = hq.hq_rotate_quant_mxfp4(x, group)
+    else:
+        q, s = hq.hq_rotate_quant_mxfp4_ws(x, group, workspace=ws)
     torch.cuda.synchronize()
+    if ws is not None:
+        assert not ws.any().item(), "the workspace is not back to 0"
     xo = synth.as_oracle_array(x_host)
     oq, os_ = oracle.quantize_mxfp4(xo, group)
     assert np.array_equal(s.cpu().numpy(), os_), "scales differ"
@@ -82,3 +88,28 @@ def test_mxfp4_on_named_workloads(name):
     w = synth.WORKLOADS[name]
     x = synth.generate(w)
     check(x, w.groups[0])
+
+
+def new_workspace():
+    return torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+
+
+# hq_rotate_quant_mxfp4_ws: the tiles are handed out at run time from 16384 warp tiles on
+# (2^21 16-blocks); below that, and for strided rows, it is the fixed split.
+@pytest.mark.parametrize("M,K,group", [(1, 32, 16), (999, 4352, 16), (4099, 8192, 16), (16385, 2048, 256),
+                                       (2053, 17408, 0), (4099, 8192, 256)])
+def test_mxfp4_with_a_workspace(M, K, group):
+    x = rand_input(M, K, torch.bfloat16, seed=M + 3 * K + group)
+    ws = new_workspace()
+    for _ in range(2):  # twice on one workspace: the first call leaves it ready for the next
+        check(x, group, ws=ws)
+
+
+def test_mxfp4_with_a_workspace_strided():
+    big = rand_input(300, 1280, torch.bfloat16, seed=9)
+    check(big[:, :1024].contiguous(), 16, x_dev=big.cuda()[:, :1024], ws=new_workspace())
+
+
+def test_mxfp4_with_a_workspace_on_the_named_workload():
+    w = synth.WORKLOADS["bf16_16384x8192_t3"]
+    check(synth.generate(w), 16, ws=new_workspace())
