@@ -527,13 +527,15 @@ def run_ours(args, w):
 
     # ---- pass 2 with the block scales in the swizzled GEMM layout, same tensor ----
     s_sw = torch.empty(hq.hq_swizzled_scales_bytes(w.M, w.K), dtype=torch.uint8, device=dev)
-    sw_ms = time_launches(lambda: hq.hq_rotate_quant_nvfp4_swizzled(
-        x, group, amax, q=q, scales=s_sw, s_global=sg, stream=stream), K, stream, dev, flush)
+    ws_sw = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device=dev)
+    sw_ms = time_launches(lambda: hq.hq_rotate_quant_nvfp4_swizzled_ws(
+        x, group, amax, q=q, scales=s_sw, s_global=sg, workspace=ws_sw, stream=stream), K, stream, dev,
+        flush)
     swz = {"group": group, "ms_per_launch": sw_ms, "bytes_per_launch": step_bytes,
            "gbs": step_bytes / (sw_ms / 1e3) / 1e9,
-           "note": "hq_rotate_quant_nvfp4_swizzled: pass 2 writing the scales in the 128x4-tile "
-                   "layout of block-scaled NVFP4 GEMMs"}
-    del s_sw
+           "note": "hq_rotate_quant_nvfp4_swizzled_ws: pass 2 writing the scales in the 128x4-tile "
+                   "layout of block-scaled NVFP4 GEMMs (units handed out at run time)"}
+    del s_sw, ws_sw
 
     # ---- MXFP4 (E8M0 per 32, single pass) on the same tensor and group ----
     mx = None

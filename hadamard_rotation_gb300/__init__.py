@@ -18,6 +18,7 @@ from .api import (  # noqa: F401
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
     hq_rotate_quant_nvfp4_swizzled,
+    hq_rotate_quant_nvfp4_swizzled_ws,
     hq_rotate_quant_nvfp4_ws,
     hq_selftest_bounded_wait,
     hq_status_string,
@@ -41,6 +42,7 @@ __all__ = [
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
     "hq_rotate_quant_nvfp4_swizzled",
+    "hq_rotate_quant_nvfp4_swizzled_ws",
     "hq_rotate_quant_nvfp4_ws",
     "hq_selftest_bounded_wait",
     "hq_status_string",

@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
         lib.hq_rotate_quant_nvfp4_delayed.restype = i32
         lib.hq_rotate_quant_nvfp4_swizzled.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p]
         lib.hq_rotate_quant_nvfp4_swizzled.restype = i32
+        lib.hq_rotate_quant_nvfp4_swizzled_ws.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]
+        lib.hq_rotate_quant_nvfp4_swizzled_ws.restype = i32
         lib.hq_swizzled_scales_bytes.argtypes = [i64, i64]
         lib.hq_swizzled_scales_bytes.restype = i64
         lib.hq_rotate_quant_mxfp4.argtypes = [p, i32, i64, i64, i64, i32, p, p, p]

@@ -179,6 +179,27 @@ def hq_rotate_quant_nvfp4_swizzled(x: torch.Tensor, group: int, amax: torch.Tens
     return q, scales, s_global
 
 
+def hq_rotate_quant_nvfp4_swizzled_ws(x: torch.Tensor, group: int, amax: torch.Tensor,
+                                      q: torch.Tensor | None = None,
+                                      scales: torch.Tensor | None = None,
+                                      s_global: torch.Tensor | None = None,
+                                      workspace: torch.Tensor | None = None,
+                                      stream: torch.cuda.Stream | None = None):
+    """hq_rotate_quant_nvfp4_swizzled with its units of work handed to the warps at run time from
+    the counters in ``workspace`` (as hq_rotate_quant_nvfp4_ws; default: the one this binding
+    keeps per device and stream)."""
+    dt, M, K, ldx = _x_args(x)
+    amax = _need(amax, (1,), torch.float32, x.device, "amax")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (hq_swizzled_scales_bytes(M, K),), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    workspace = _workspace(x.device, stream) if workspace is None else _need(
+        workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
+    _call(x.device, "hq_rotate_quant_nvfp4_swizzled_ws", _ptr(x), dt, M, K, ldx, group,
+          _ptr(amax), _ptr(q), _ptr(scales), _ptr(s_global), _ptr(workspace), stream=stream)
+    return q, scales, s_global
+
+
 def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.Tensor,
                                   amax_next: torch.Tensor | None = None,
                                   q: torch.Tensor | None = None,

@@ -333,6 +333,11 @@ hq_status dispatch_quant_group(const hq::Params& p, int group, bool bf16, bool s
 template <int G>
 hq_status dispatch_quant_swizzled(const hq::Params& p, bool bf16, hq_stream s) {
   using hq::k_rotate_quant_nvfp4;
+  if (p.sched != nullptr)  // units handed out at run time
+    return bf16 ? launch(k_rotate_quant_nvfp4<G, true, hq::kLoadTma, false, true, true>, p, s,
+                         ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, true))
+                : launch(k_rotate_quant_nvfp4<G, false, hq::kLoadTma, false, true, true>, p, s,
+                         ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, false));
   if (bf16)
     return launch(k_rotate_quant_nvfp4<G, true, hq::kLoadTma, false, true>, p, s,
                   ring_bytes<HQ_PASS2_STAGES>(hq::kLoadTma, true));
@@ -458,11 +463,13 @@ int64_t hq_swizzled_scales_bytes(int64_t M, int64_t K) {
   return row_tiles * 128 * cols;
 }
 
-hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t M, int64_t K,
-                                         int64_t ldx, int group, const float* amax, uint8_t* q,
-                                         uint8_t* scales, float* s_global, hq_stream stream) {
+hq_status hq_rotate_quant_nvfp4_swizzled_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                            int64_t ldx, int group, const float* amax, uint8_t* q,
+                                            uint8_t* scales, float* s_global, uint32_t* workspace,
+                                            hq_stream stream) {
   hq_status st = check_x(x, dtype, M, K, ldx, group);
   if (st != HQ_OK) return st;
+  if (workspace && !aligned(workspace, 4)) return HQ_ERR_ALIGN;
   if (M == 0 || K == 0) return HQ_OK;
   if (!amax || !q || !scales) return HQ_ERR_NULL;
   if (!aligned(amax, 4) || !aligned(q, 16) || !aligned(scales, 32) ||
@@ -483,12 +490,23 @@ hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t 
   p.div_ncc = make_fast_div(p.n_cc);
   p.n_tiles = n_tiles;
   p.swz_col_tiles = static_cast<uint64_t>((K / 16 + 3) / 4);
+  if (schedulable(p, workspace, false)) {  // every row is its own copy: strided rows too
+    p.sched = workspace + kSchedWord;
+    p.sched_done = workspace + 3;
+  }
   const bool bf16 = dtype == HQ_BF16;
   switch (group) {
     case 0: return dispatch_quant_swizzled<0>(p, bf16, stream);
     case 16: return dispatch_quant_swizzled<16>(p, bf16, stream);
     default: return dispatch_quant_swizzled<256>(p, bf16, stream);
   }
+}
+
+hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                         int64_t ldx, int group, const float* amax, uint8_t* q,
+                                         uint8_t* scales, float* s_global, hq_stream stream) {
+  return hq_rotate_quant_nvfp4_swizzled_ws(x, dtype, M, K, ldx, group, amax, q, scales, s_global,
+                                           nullptr, stream);
 }
 
 hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M, int64_t K,

@@ -821,48 +821,47 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
   }
 }
 
-// Row-group units through the TMA ring: warp w of W takes the units w, w + W, ...,
-// each as its 8 tiles in order, and calls body(tile, lane, valid, t) with the
-// RgTile.  The unit positions (row group, column chunk) of the tile being read
-// and of the tile being fetched advance by W units with one carry, no division.
-template <int G, bool BF16, int STAGES, typename Body, typename Pre = NoPrologue>
+// Row-group units through the TMA ring, each unit as its 8 tiles in order: body(tile, lane,
+// valid, t) is called with the RgTile.  A unit's geometry (row tile, row pair, column chunk)
+// comes from its index by one division, once per unit; a tile adds its row offset.
+// Fixed split (DYN false): warp w of W takes the units w, w + W, ...  Run-time split (DYN):
+// unit u belongs to class u % C (C = kSchedClasses) and warp c of every CTA serves class c,
+// units c + C j: its first j is blockIdx.x, every later one gridDim.x + the value of an
+// atomicAdd on the class counter p.sched[c * kSchedStrideWords], read by lane 0 a unit ahead
+// (as for_each_tile's run-time split; the last warp to run out puts the counters back to 0).
+// Lane 0 keeps the schedule: the unit it fetches tiles from and, once the reader reaches a
+// unit, that unit's index for the other lanes (the fetcher is STAGES < 8 tiles ahead, so at
+// most two units are in flight).
+template <int G, bool BF16, int STAGES, bool DYN = false, typename Body, typename Pre = NoPrologue>
 __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
   using R = Ring<BF16, STAGES>;
+  static_assert(R::kStages < 8, "the fetcher stays within one unit of the reader");
+  constexpr uint32_t kNoUnit = ~0u;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
-  const uint32_t gw = blockIdx.x * kWarpsPerCta + wid;
-  const uint32_t nw = gridDim.x * kWarpsPerCta;
   const uint32_t n_units = static_cast<uint32_t>(p.n_tiles >> 3);  // < 2^29
-  const uint32_t d_rg = fast_div(nw, p.div_ncc);
-  const uint32_t d_cc = nw - d_rg * p.n_cc;
-  struct Pos {
-    uint32_t u, rg, cc;  // unit, its row group (16 per row tile), its column chunk
+  struct Unit {
+    uint32_t rt, k, row0, c0, ncols;
   };
-  auto start = [&]() {
-    Pos s;
-    s.u = gw;
-    s.rg = fast_div(gw, p.div_ncc);
-    s.cc = gw - s.rg * p.n_cc;
+  auto unit_of = [&](uint32_t u) {
+    Unit s;
+    const uint32_t rg = fast_div(u, p.div_ncc);  // row group: 16 per row tile of 128 rows
+    s.rt = rg >> 4;
+    s.k = rg & 15u;
+    s.row0 = s.rt * 128u + 2u * s.k;
+    s.c0 = (u - rg * p.n_cc) * static_cast<uint32_t>(kTileBlocks);
+    const uint32_t left = p.nbr - s.c0;
+    s.ncols = left < kTileBlocks ? left : kTileBlocks;
     return s;
   };
-  auto step = [&](Pos& s) {
-    s.u += nw;
-    s.rg += d_rg;
-    s.cc += d_cc;
-    if (s.cc >= p.n_cc) {
-      s.cc -= p.n_cc;
-      s.rg += 1;
-    }
-  };
-  auto tile_at = [&](const Pos& s, int rs) {
+  auto tile_in = [&](const Unit& s, int rs) {  // rows 2k + {0, 1, 32, 33, 64, 65, 96, 97}
     RgTile g;
-    g.rt = s.rg >> 4;
-    g.k = s.rg & 15u;
+    g.rt = s.rt;
+    g.k = s.k;
     g.rs = rs;
-    g.row = g.rt * 128u + 2u * g.k + static_cast<uint32_t>(rs & 1) + 32u * static_cast<uint32_t>(rs >> 1);
-    g.c0 = s.cc * static_cast<uint32_t>(kTileBlocks);
-    const uint32_t left = p.nbr - g.c0;
-    g.ncols = left < kTileBlocks ? left : kTileBlocks;
+    g.row = s.row0 + static_cast<uint32_t>(rs & 1) + 32u * static_cast<uint32_t>(rs >> 1);
+    g.c0 = s.c0;
+    g.ncols = s.ncols;
     g.present = g.row < p.rows;
     return g;
   };
@@ -886,50 +885,88 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, P
     fence_mbar_init();
   }
   __syncwarp();
-  Pos ip = start();  // the next tile to fetch: unit ip, tile irs
-  int irs = 0;
-  uint64_t issued = 0;
-  for (int s = 0; s < R::kStages && ip.u < n_units; ++s) {
-    if (lane == 0) issue(tile_at(ip, irs), s);
-    ++issued;
-    if (++irs == 8) {
-      irs = 0;
-      step(ip);
+
+  // Lane 0's fetch position: unit fu (kNoUnit: none left), tile frs, and its geometry.
+  const uint32_t cls = static_cast<uint32_t>(wid);
+  unsigned* const counter = p.sched + (DYN ? wid * kSchedStrideWords : 0);
+  uint32_t fu = DYN ? cls + kSchedClasses * blockIdx.x : blockIdx.x * kWarpsPerCta + wid;
+  if (fu >= n_units) fu = kNoUnit;
+  unsigned pend = 0;
+  if constexpr (DYN) {
+    if (lane == 0) {  // the kernel waited for the one before it: the counters are ready
+      if (fu != kNoUnit)
+        pend = atomicAdd(counter, 1u);
+      else
+        sched_retire(p);
     }
   }
+  const uint32_t first = fu;
+  auto next_unit = [&]() {  // lane 0: the unit after fu
+    uint32_t u;
+    if constexpr (DYN) {
+      const uint64_t j = static_cast<uint64_t>(gridDim.x) + pend;
+      u = j < (uint64_t{1} << 29) ? cls + kSchedClasses * static_cast<uint32_t>(j) : kNoUnit;
+      if (u < n_units) {
+        pend = atomicAdd(counter, 1u);  // the one after, read ahead
+      } else {
+        u = kNoUnit;
+        sched_retire(p);
+      }
+    } else {
+      const uint32_t nw = gridDim.x * kWarpsPerCta;
+      u = (n_units - fu > nw) ? fu + nw : kNoUnit;
+    }
+    return u;
+  };
+  Unit fg = unit_of(fu == kNoUnit ? 0u : fu);
+  int frs = 0;
+  uint64_t issued = 0;  // lane 0: tiles handed to TMA
+  auto fetch = [&](int slot) {  // lane 0: issue the next tile, if any, into `slot`
+    if (fu == kNoUnit) return;
+    issue(tile_in(fg, frs), slot);
+    ++issued;
+    if (++frs == 8) {
+      frs = 0;
+      fu = next_unit();
+      if (fu != kNoUnit) fg = unit_of(fu);
+    }
+  };
+  if (lane == 0)
+    for (int s = 0; s < R::kStages; ++s) fetch(s);
   pre();
-  Pos cp = start();  // the tile to read: unit cp, tile crs
+
+  uint32_t cu = bcast0(lane == 0 ? first : 0u) & 0xFFFFFFFFu;  // the unit being read
+  Unit cg;
   int crs = 0;
-  for (uint64_t k = 0; cp.u < n_units; ++k) {
+  for (uint64_t k = 0;; ++k) {
+    if (crs == 0) {
+      if (cu == kNoUnit) break;
+      cg = unit_of(cu);
+    }
     const int slot = static_cast<int>(k % R::kStages);
     const uint32_t parity = static_cast<uint32_t>((k / R::kStages) & 1);
     const bool ok = mbar_wait(bar0 + slot * 8, parity);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
       if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
-      for (uint64_t m = k; m < issued; ++m)
+      const uint64_t n_issued = bcast0(issued);
+      for (uint64_t m = k; m < n_issued; ++m)
         mbar_wait(bar0 + static_cast<int>(m % R::kStages) * 8, static_cast<uint32_t>((m / R::kStages) & 1));
       return;
     }
-    const RgTile g = tile_at(cp, crs);
+    const RgTile g = tile_in(cg, crs);
     bool valid[4];
     Lane4 t;
     load_tile_smem<G, BF16, 0>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
     __syncwarp();  // every lane has read the slot
-    if (ip.u < n_units) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(tile_at(ip, irs), slot);
-      }
-      ++issued;
-      if (++irs == 8) {
-        irs = 0;
-        step(ip);
-      }
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      fetch(slot);
     }
     body(g, lane, valid, t);
     if (++crs == 8) {
       crs = 0;
-      step(cp);
+      // the fetcher is past this unit's end and within the next one (or out of units)
+      cu = static_cast<uint32_t>(bcast0(lane == 0 ? fu : 0u));
     }
   }
 }
@@ -1507,7 +1544,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
     }
   };
   if constexpr (SWZ)
-    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES>(p, tile_body, prologue);
+    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES, DYN>(p, tile_body, prologue);
   else
     for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1, false, GDC, DYN>(p, tile_body, prologue);
   if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
@@ -1522,7 +1559,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_rotate_quant_nvfp4(Params p) {
   // complete (p.x_ready); the row-group loop waits here.
   if constexpr (SWZ) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ>(p, p.amax_in);
+    rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ, false, DYN>(p, p.amax_in);
   } else {
     rotate_quant_tiles<G, BF16, MODE, REDUCE_NEXT, SWZ, true, DYN>(p, p.amax_in);
   }

@@ -112,8 +112,8 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 int64_t ldx, int group, const float* amax, uint8_t* q,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
-/* Size of the workspace of hq_quantize_nvfp4, hq_rotate_quant_nvfp4_ws and
- * hq_rotate_quant_mxfp4_ws, in 32-bit words
+/* Size of the workspace of hq_quantize_nvfp4 and the _ws entry points (hq_rotate_quant_nvfp4_ws,
+ * hq_rotate_quant_nvfp4_swizzled_ws, hq_rotate_quant_mxfp4_ws), in 32-bit words
  * (control words and the counters of the run-time tile schedule, each on its own 128-byte
  * line). */
 #define HQ_QUANTIZE_WORKSPACE_WORDS 288
@@ -184,6 +184,18 @@ HQ_API hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, i
                                                 int64_t K, int64_t ldx, int group,
                                                 const float* amax, uint8_t* q, uint8_t* scales,
                                                 float* s_global, hq_stream stream);
+
+/*
+ * hq_rotate_quant_nvfp4_swizzled_ws -- hq_rotate_quant_nvfp4_swizzled exactly (same arguments,
+ *   same outputs), with its units of work (8 rows x 128 blocks) handed to the warps at run time
+ *   as in hq_rotate_quant_nvfp4_ws (a schedule, not a step of the method).
+ *   workspace : as for hq_rotate_quant_nvfp4_ws.  NULL: hq_rotate_quant_nvfp4_swizzled.
+ */
+HQ_API hq_status hq_rotate_quant_nvfp4_swizzled_ws(const void* x, hq_dtype dtype, int64_t M,
+                                                   int64_t K, int64_t ldx, int group,
+                                                   const float* amax, uint8_t* q,
+                                                   uint8_t* scales, float* s_global,
+                                                   uint32_t* workspace, hq_stream stream);
 
 /* Size in bytes of the swizzled scale buffer for an [M, K] tensor (-1 if M < 0, K < 0,
  * K % 16 != 0, or the size does not fit int64). */

@@ -251,6 +251,15 @@ def test_swizzled_argument_checks_and_size(lib):
     assert sw(a=0) == 1 and sw(q=0) == 1 and sw(s=0) == 1 and sw(x=0) == 1
     assert sw(G=32) == 5 and sw(dt=2) == 4 and sw(K=24, ldx=24) == 2
     assert sw(s=FAKE + 4) == 3 and sw(s=FAKE + 16) == 3   # the swizzled scales are 32-byte aligned
+
+    def sww(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, a=FAKE, q=FAKE, s=FAKE, sg=None, ws=FAKE + 256):
+        return lib.hq_rotate_quant_nvfp4_swizzled_ws(
+            P(x) if x else None, dt, M, K, ldx, G, P(a) if a else None, P(q) if q else None,
+            P(s) if s else None, P(sg) if sg else None, P(ws) if ws else None, None)
+    assert sww(a=0) == 1 and sww(q=0) == 1 and sww(s=0) == 1 and sww(x=0) == 1
+    assert sww(G=32) == 5 and sww(dt=2) == 4 and sww(K=24, ldx=24) == 2
+    assert sww(s=FAKE + 16) == 3 and sww(ws=FAKE + 2) == 3
+    assert sww(M=0) == 0 and sww(M=0, ws=0) == 0
     assert sw(q=FAKE + 8) == 3 and sw(x=FAKE + 8) == 3
     assert sw(M=0) == 0
     # tiles of 128 rows x 4 scale columns, padded

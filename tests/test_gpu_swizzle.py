@@ -1,4 +1,4 @@
-"""Swizzled block scales (hq_rotate_quant_nvfp4_swizzled) against the oracle, and as the input of
+"""Swizzled block scales (hq_rotate_quant_nvfp4_swizzled, _ws) against the oracle, and as the input of
 cuBLASLt's NVFP4 GEMM.
 
 "A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §6 "From interpreter to hardware"
@@ -81,6 +81,39 @@ def test_swizzled_strided_rows(group):
     q, s, sg = run_swizzled(x, group, x_dev=big.cuda()[:, :512])
     oq, os_, _, _ = oracle.quantize(synth.as_oracle_array(x), group)
     assert np.array_equal(q, oq) and np.array_equal(s, oracle.swizzle_scales(os_))
+
+
+# hq_rotate_quant_nvfp4_swizzled_ws: the units (8 rows x 128 blocks) are handed out at run time
+# from 16384 tiles (2048 units) on; below that it is the fixed split.  Twice on one workspace.
+@pytest.mark.parametrize("M,K,group", [(129, 80, 16), (4099, 8192, 16), (2053, 17408, 16), (4099, 8192, 256),
+                                       (2053, 17408, 0)])
+def test_swizzled_with_a_workspace(M, K, group):
+    x = varied(M, K, seed=M + K + group)
+    xd = x.cuda()
+    oq, os_, _, osg = oracle.quantize(synth.as_oracle_array(x), group)
+    amax = hq.hq_rot_amax(xd, group)
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        s = torch.full((hq.hq_swizzled_scales_bytes(M, K),), 0xFF, dtype=torch.uint8, device="cuda")
+        q, s, sg = hq.hq_rotate_quant_nvfp4_swizzled_ws(xd, group, amax, scales=s, workspace=ws)
+        torch.cuda.synchronize()
+        assert not ws.any().item(), "the workspace is not back to 0"
+        assert np.array_equal(q.cpu().numpy(), oq)
+        assert np.array_equal(sg.cpu().numpy().view(np.uint32), np.array([osg], np.float32).view(np.uint32))
+        assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+
+
+def test_swizzled_with_a_workspace_strided_rows():
+    big = varied(4099, 8192 + 64, seed=4)
+    x = big[:, :8192].contiguous()
+    xd = big.cuda()[:, :8192]
+    oq, os_, _, _ = oracle.quantize(synth.as_oracle_array(x), 16)
+    amax = hq.hq_rot_amax(xd, 16)
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    q, s, sg = hq.hq_rotate_quant_nvfp4_swizzled_ws(xd, 16, amax, workspace=ws)
+    torch.cuda.synchronize()
+    assert not ws.any().item()
+    assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
 
 
 def _nvfp4_gemm(qa, sa, qb, sb):
