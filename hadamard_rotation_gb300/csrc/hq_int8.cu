@@ -37,7 +37,7 @@ hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
   return HQ_OK;
 }
 
-// Rows longer than tensor memory can park: one CTA of kI8Threads per SM, each row read twice.
+// Rows longer than the chip can park: one CTA of kI8Threads per SM, each row read twice.
 template <int G, bool BF16>
 hq_status launch_int8_long(const hq::I8Params& p, hq_stream stream) {
   int dev = 0, sms = 0;
@@ -52,10 +52,35 @@ hq_status launch_int8_long(const hq::I8Params& p, hq_stream stream) {
   return HQ_OK;
 }
 
+// Rows of 17 to 59 warp tiles: parked whole on chip (tensor memory and shared memory), one
+// CTA of kI8Threads per SM.
+template <int G, bool BF16>
+hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
+  auto kernel = hq::k_rotate_quant_int8_park<G, BF16>;
+  const int smem_tiles = p.tiles_per_row > hq::kI8ParkTmemTiles ? p.tiles_per_row - hq::kI8ParkTmemTiles : 0;
+  const size_t smem = static_cast<size_t>(smem_tiles) * hq::kI8ParkTileBytes;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  if (smem > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem))) != cudaSuccess)
+    return cuda_fail(e);
+  const unsigned grid = static_cast<unsigned>(p.M < sms ? p.M : sms);
+  kernel<<<grid, hq::kI8Threads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return HQ_OK;
+}
+
 template <int G>
 hq_status dispatch_int8(const hq::I8Params& p, bool bf16, hq_stream s) {
-  if (p.K > hq::kI8MaxK)
+  if (p.tiles_per_row > hq::kI8ParkMaxTiles)
     return bf16 ? launch_int8_long<G, true>(p, s) : launch_int8_long<G, false>(p, s);
+  if (p.K > hq::kI8MaxK)
+    return bf16 ? launch_int8_park<G, true>(p, s) : launch_int8_park<G, false>(p, s);
   const bool full = p.K % hq::kI8TileElems == 0;
   if (bf16)
     return full ? launch_int8<G, true, hq::kLoadTma, true>(p, s)

@@ -12,7 +12,8 @@
 // S = (v0 + v1) + (v2 + v3) (H4 = J - 2P, P the exchange matrix).
 //
 // Work decomposition.  A CTA of 16 warps handles whole rows: a row of K channels
-// is T = ceil(K / 2048) warp tiles (K <= 32768).  The CTA takes rows in blocks of
+// is T = ceil(K / 2048) warp tiles (K <= 32768; longer rows: k_rotate_quant_int8_park and
+// k_rotate_quant_int8_long below).  The CTA takes rows in blocks of
 // B rows, B T tiles numbered row by row, and warp w handles the tiles w, w + 16,
 // ..., L of them.  For G = 64 and 256, which are bound by instruction issue,
 // B = lcm(T, 16) / T and L = lcm(T, 16) / 16, so all 16 warps have work whatever T
@@ -564,7 +565,161 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
 }
 
 // ---------------------------------------------------------------------------
-// Rows longer than tensor memory can park (K > kI8MaxK).  A CTA of 16 warps takes
+// Rows of 17 to 59 warp tiles (32768 < K <= 120832 channels): the whole rotated row
+// stays on chip, tiles 0 .. 31 in tensor memory (two per warp, as above) and tiles
+// 32 .. T-1 in shared memory (8 KB each), so x is read once and every value rotated
+// once.  A CTA of 16 warps takes rows blockIdx.x, blockIdx.x + gridDim.x, ...; warp w
+// takes the tiles w, w + 16, ... of a row.  Walk 1 loads (16-byte vector loads straight
+// into registers), rotates, keeps the tile amax and parks the tile; the CTA meets at a
+// barrier (the row's amax, one word per warp, double-buffered by row parity, so a warp
+// can be at most one row ahead of a reader); walk 2 takes each tile back, quantizes and
+// stores it.  A warp parks and takes back only its own tiles, so the only wait is the
+// CTA barrier and no bound is needed.
+// ---------------------------------------------------------------------------
+constexpr int kI8ParkTmemTiles = 2 * kI8Warps;                          // 32
+constexpr int kI8ParkTileBytes = kI8TileElems * 4;                      // 8 KB of fp32
+constexpr int kI8ParkSmemTiles = 27;                                    // 216 KB
+constexpr int kI8ParkMaxTiles = kI8ParkTmemTiles + kI8ParkSmemTiles;  // 59
+
+template <int G, bool BF16>
+__global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Params p) {
+  constexpr int es = BF16 ? 2 : 4;
+  constexpr int n16 = BF16 ? 2 : 4;  // 16-byte words per block of 16 channels
+  constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int T = p.tiles_per_row;
+  __shared__ float row_max[2][kI8Warps];
+  __shared__ uint32_t tmem_base_slot;
+  extern __shared__ __align__(1024) uint8_t hq_smem[];  // tiles 32 .. T-1 of the row
+
+  if (wid == 0) tmem_alloc_all(smem_addr(&tmem_base_slot));
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem_warp = tmem_base_slot + ((32u * static_cast<uint32_t>(wid & 3)) << 16) +
+                             128u * static_cast<uint32_t>(wid >> 2);
+
+  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0).
+  auto load = [&](int64_t row, int chunk, Lane4& t) {
+    const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
+    const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
+    const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t bl = i8_in_block<G>(lane, j);
+      uint4 w4[n16];
+      const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+#pragma unroll
+      for (int k = 0; k < n16; ++k)
+        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + k) : make_uint4(0u, 0u, 0u, 0u);
+      float f[16];
+      widen<BF16>(w4, f);
+      put_block(t, j, f);
+    }
+    return nvalid;
+  };
+  // Tile `chunk` (the warp's s-th of the row) in its place: TMEM slot s for chunk < 32,
+  // else shared-memory slot chunk - 32, 16 float4 per lane, float4 i of lane l at
+  // 16 (32 i + l) (each warp-wide 16-byte access covers 512 consecutive bytes).
+  auto park = [&](int chunk, int s, const Lane4& t) {
+    uint32_t v[64];
+    lane4_to_words(t, v);
+    if (chunk < kI8ParkTmemTiles) {
+      tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(s), v);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(hq_smem + (chunk - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dst[32 * i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  };
+  auto unpark = [&](int chunk, int s, Lane4& t) {
+    uint32_t v[64];
+    if (chunk < kI8ParkTmemTiles) {
+      tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(s), v);
+      tmem_wait_ld();
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(hq_smem + (chunk - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 w = src[32 * i];
+        v[4 * i] = w.x;
+        v[4 * i + 1] = w.y;
+        v[4 * i + 2] = w.z;
+        v[4 * i + 3] = w.w;
+      }
+    }
+    words_to_lane4(v, t);
+  };
+
+  int64_t n = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++n) {
+    // walk 1: rotate, the tile amax, park
+    float amax = 0.0f;
+    int s = 0;
+    for (int chunk = wid; chunk < T; chunk += kI8Warps, ++s) {
+      Lane4 t;
+      load(row, chunk, t);
+      rotate_regular<G>(t);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
+      park(chunk, s, t);
+    }
+    amax = warp_max_nonneg(amax);
+    if (lane == 0) row_max[n & 1][wid] = amax;
+    tmem_wait_st();  // this thread's parked columns are written before it reads them back
+    __syncthreads();
+    const float row_amax = warp_max_nonneg(lane < kI8Warps ? row_max[n & 1][lane] : 0.0f);
+    const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
+    const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
+    if (threadIdx.x == 0) p.scales[row] = scale;
+    // walk 2: the codes (rint by the magic constant, as in k_rotate_quant_int8)
+    const float2 inv2 = make_float2(inv, inv);
+    const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+    const float2 one2 = make_float2(1.0f, 1.0f);
+    s = 0;
+    for (int chunk = wid; chunk < T; chunk += kI8Warps, ++s) {
+      Lane4 t;
+      unpark(chunk, s, t);
+      const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
+      const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
+      int8_t* qrow = p.q + row * p.K + c0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t bx[16], by[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+          bx[i] = __float_as_uint(w.x);
+          by[i] = __float_as_uint(w.y);
+        }
+        const uint32_t box = i8_out_block<G>(lane, 2 * k);
+        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
+        if (static_cast<int64_t>(box) * 16 < nvalid)
+          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
+                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
+                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
+        if (static_cast<int64_t>(boy) * 16 < nvalid)
+          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
+                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
+                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
+      }
+    }
+  }
+  // Every thread's TMEM traffic is complete before the columns are freed.
+  tmem_wait_st();
+  tmem_wait_ld();
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (wid == 0) {
+    tmem_fence_after_sync();
+    tmem_dealloc_all(tmem_base_slot);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rows longer than the chip can park (K > 120832 channels).  A CTA of 16 warps takes
 // rows blockIdx.x, blockIdx.x + gridDim.x, ...; warp w takes the warp tiles w, w + 16,
 // ... of a row (at least one each, since T > 16).  Each row is read twice: the first
 // walk rotates the tiles and keeps only their amax; the CTA meets at a barrier (the

@@ -274,9 +274,9 @@ HQ_API hq_status hq_dequant_mxfp4(const uint8_t* q, const uint8_t* scales, int64
  *            fixes the rounding.)
  *   scales : fp32 [M], scale = max(amax_row |y|, 1e-12) / 127.
  *   q      : int8 [M, K] row-major, q = clamp(rint(y * (1/scale)), -127, 127) (half to even).
- *   For K <= 32768, x is read once and the rotated row stays on chip (tensor memory); a longer
- *   row is read twice, first for its amax and then to quantize it (the second read mostly
- *   from L2).
+ *   For K <= 120832, x is read once and the rotated row stays on chip until its amax is known
+ *   (tensor memory up to 32768 channels, tensor and shared memory beyond); a longer row is read
+ *   twice, first for its amax and then to quantize it (the second read mostly from L2).
  *
  *   group  : 4, 16, 64, 256 or 1024; K a multiple of the group and of 16 (the kernels move
  *            whole 16-channel blocks), K / 2048 below 2^30.

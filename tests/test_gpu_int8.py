@@ -3,9 +3,9 @@
 "hyperflow_h3_flash_int8.py" (HyperFlow): regular_hadamard, hadamard_factors,
 rotate_quant_kernel, rotate_quant.  Groups 4, 16, 64, 256 and 1024 (the page's group sizes:
 powers of 4).  Shapes cover one and several warp tiles per row (2048 channels each), ragged last
-tiles, 1 to 16 rows per CTA step, rows longer than tensor memory parks (K > 32768: each row
-read twice), both input types, strided rows, zero rows (the 1e-12 floor) and extreme
-magnitudes.
+tiles, 1 to 16 rows per CTA step, rows longer than tensor memory holds (32768 < K <= 120832:
+parked in tensor and shared memory; longer: each row read twice), both input types, strided
+rows, zero rows (the 1e-12 floor) and extreme magnitudes.
 """
 import numpy as np
 import pytest
@@ -56,9 +56,12 @@ SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16),
           (40, 30720, 16),
           # group 4 (one digit), group 1024 (five digits, two of them across lanes)
           (2, 16, 4), (37, 2064, 4), (5, 1024, 1024), (13, 3072, 1024), (8, 32768, 1024),
-          # rows longer than tensor memory parks: 17 warp tiles, a ragged 18th, 32 and 48
+          # rows longer than tensor memory holds, parked in tensor and shared memory: 17 warp
+          # tiles, a ragged 19th, 32, a ragged 49th, 59 (the most parked on chip)
           (3, 34816, 16), (5, 36864 + 1024, 1024), (4, 65536, 256), (2, 98304 + 16, 4),
-          (3, 65536, 64)]
+          (3, 65536, 64), (3, 120832, 16),
+          # longer still, each row read twice: a ragged 60th tile, 60 and 64 tiles
+          (2, 120832 + 16, 16), (2, 122880, 256), (2, 131072, 1024)]
 
 
 @pytest.mark.parametrize("M,K,group", SHAPES)
@@ -75,7 +78,7 @@ def test_int8_strided_rows(group):
 
 @pytest.mark.parametrize("group", [16, 1024])
 def test_int8_long_rows_strided_and_many(group):
-    """Rows of 65536 channels (each read twice), strided, more rows than SMs."""
+    """Rows of 65536 channels (parked on chip), strided, more rows than SMs."""
     big = rand_input(400, 65536 + 1024, torch.bfloat16, seed=7)
     check(big[:, :65536].contiguous(), group, x_dev=big.cuda()[:, :65536])
 
