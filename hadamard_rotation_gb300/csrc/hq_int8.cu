@@ -56,8 +56,10 @@ hq_status launch_int8_long(const hq::I8Params& p, hq_stream stream) {
 // CTA of kI8Threads per SM.
 template <int G, bool BF16>
 hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
-  auto kernel = hq::k_rotate_quant_int8_park<G, BF16>;
-  const int smem_tiles = p.tiles_per_row > hq::kI8ParkTmemTiles ? p.tiles_per_row - hq::kI8ParkTmemTiles : 0;
+  auto kernel = p.rows_per_block > 1 ? hq::k_rotate_quant_int8_park<G, BF16, true>
+                                     : hq::k_rotate_quant_int8_park<G, BF16, false>;
+  const int n_g = p.rows_per_block * p.tiles_per_row;
+  const int smem_tiles = n_g > hq::kI8ParkTmemTiles ? n_g - hq::kI8ParkTmemTiles : 0;
   const size_t smem = static_cast<size_t>(smem_tiles) * hq::kI8ParkTileBytes;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -68,7 +70,8 @@ hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
       (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem))) != cudaSuccess)
     return cuda_fail(e);
-  const unsigned grid = static_cast<unsigned>(p.M < sms ? p.M : sms);
+  const int64_t n_blocks = (p.M + p.rows_per_block - 1) / p.rows_per_block;
+  const unsigned grid = static_cast<unsigned>(n_blocks < sms ? n_blocks : sms);
   kernel<<<grid, hq::kI8Threads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
@@ -147,8 +150,23 @@ hq_status hq_rotate_quant_int8(const void* x, hq_dtype dtype, int64_t M, int64_t
     b = t;
   }
   const int lcm = p.tiles_per_row / a * hq::kI8Warps;
-  if (p.tiles_per_row > hq::kI8Warps) {  // the long-row kernel: one row at a time
+  if (p.tiles_per_row > hq::kI8ParkMaxTiles) {  // the long-row kernel: one row at a time
     p.rows_per_block = 1;
+    p.tiles_per_warp = 0;
+  } else if (p.tiles_per_row > hq::kI8Warps) {
+    // rows parked on chip: B rows per CTA step (B T <= 59), the B whose B T tiles fill the
+    // 16 warps' rounds best (the smaller B on a tie)
+    int best_b = 1, best_used = 0, best_slots = 1;
+    for (int b = 1; b <= hq::kI8ParkMaxRows && b * p.tiles_per_row <= hq::kI8ParkMaxTiles; ++b) {
+      const int used = b * p.tiles_per_row;
+      const int slots = (used + hq::kI8Warps - 1) / hq::kI8Warps * hq::kI8Warps;
+      if (static_cast<int64_t>(used) * best_slots > static_cast<int64_t>(best_used) * slots) {
+        best_b = b;
+        best_used = used;
+        best_slots = slots;
+      }
+    }
+    p.rows_per_block = best_b;
     p.tiles_per_warp = 0;
   } else if (group <= 16) {  // memory-bound: whole rows, one tile per warp (see hq_int8.cuh)
     p.rows_per_block = hq::kI8Warps / p.tiles_per_row;

@@ -566,32 +566,41 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
 
 // ---------------------------------------------------------------------------
 // Rows of 17 to 59 warp tiles (32768 < K <= 120832 channels): the whole rotated row
-// stays on chip, tiles 0 .. 31 in tensor memory (two per warp, as above) and tiles
-// 32 .. T-1 in shared memory (8 KB each), so x is read once and every value rotated
-// once.  A CTA of 16 warps takes rows blockIdx.x, blockIdx.x + gridDim.x, ...; warp w
-// takes the tiles w, w + 16, ... of a row.  Walk 1 loads (16-byte vector loads straight
-// into registers), rotates, keeps the tile amax and parks the tile; the CTA meets at a
-// barrier (the row's amax, one word per warp, double-buffered by row parity, so a warp
-// can be at most one row ahead of a reader); walk 2 takes each tile back, quantizes and
-// stores it.  A warp parks and takes back only its own tiles, so the only wait is the
-// CTA barrier and no bound is needed.
+// stays on chip until its amax is known, so x is read once and every value rotated once.
+// A CTA of 16 warps takes blocks of B rows (B T <= 59; B = 2 or 3 for T <= 24, which
+// evens out the warps' shares), blocks blockIdx.x, blockIdx.x + gridDim.x, ...; the
+// block's tiles g = 0 .. B T - 1 (row g / T, chunk g % T) are dealt round robin, warp w
+// taking g = w, w + 16, ...  Tiles 0 .. 31 of a block park in tensor memory (two per
+// warp, as above), tiles 32 .. in shared memory (8 KB each).  Walk 1 loads (16-byte
+// vector loads straight into registers), rotates, keeps the per-row tile amax and parks
+// the tile; the CTA meets at a barrier (per row and warp one amax word, double-buffered
+// by block parity, so a warp can be at most one block ahead of a reader); walk 2 takes
+// each tile back, quantizes and stores it.  A warp parks and takes back only its own
+// tiles, so the only wait is the CTA barrier and no bound is needed.
 // ---------------------------------------------------------------------------
 constexpr int kI8ParkTmemTiles = 2 * kI8Warps;                          // 32
 constexpr int kI8ParkTileBytes = kI8TileElems * 4;                      // 8 KB of fp32
 constexpr int kI8ParkSmemTiles = 27;                                    // 216 KB
 constexpr int kI8ParkMaxTiles = kI8ParkTmemTiles + kI8ParkSmemTiles;  // 59
+constexpr int kI8ParkMaxRows = 3;                                       // B (T >= 17)
 
-template <int G, bool BF16>
+// MULTI: blocks of B > 1 rows (B = 1 takes a leaner path).
+template <int G, bool BF16, bool MULTI>
 __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Params p) {
+  constexpr int kRows = MULTI ? kI8ParkMaxRows : 1;
   constexpr int es = BF16 ? 2 : 4;
   constexpr int n16 = BF16 ? 2 : 4;  // 16-byte words per block of 16 channels
   constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
-  __shared__ float row_max[2][kI8Warps];
+  const int B = MULTI ? p.rows_per_block : 1;
+  const int n_g = B * T;  // tiles per block
+  // g / T = (g * inv_T) >> 16, exact for g < 64 and 17 <= T <= 59
+  const uint32_t inv_T = (65536u + static_cast<uint32_t>(T) - 1u) / static_cast<uint32_t>(T);
+  __shared__ float row_max[2][kRows][kI8Warps];
   __shared__ uint32_t tmem_base_slot;
-  extern __shared__ __align__(1024) uint8_t hq_smem[];  // tiles 32 .. T-1 of the row
+  extern __shared__ __align__(1024) uint8_t hq_smem[];  // tiles 32 .. n_g - 1 of a block
 
   if (wid == 0) tmem_alloc_all(smem_addr(&tmem_base_slot));
   tmem_fence_before_sync();
@@ -617,29 +626,28 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       widen<BF16>(w4, f);
       put_block(t, j, f);
     }
-    return nvalid;
   };
-  // Tile `chunk` (the warp's s-th of the row) in its place: TMEM slot s for chunk < 32,
-  // else shared-memory slot chunk - 32, 16 float4 per lane, float4 i of lane l at
-  // 16 (32 i + l) (each warp-wide 16-byte access covers 512 consecutive bytes).
-  auto park = [&](int chunk, int s, const Lane4& t) {
+  // Tile g of the block in its place: TMEM slot g / 16 of this warp for g < 32, else
+  // shared-memory slot g - 32, 16 float4 per lane, float4 i of lane l at 16 (32 i + l) (each
+  // warp-wide 16-byte access covers 512 consecutive bytes).
+  auto park = [&](int g, const Lane4& t) {
     uint32_t v[64];
     lane4_to_words(t, v);
-    if (chunk < kI8ParkTmemTiles) {
-      tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(s), v);
+    if (g < kI8ParkTmemTiles) {
+      tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(g >> 4), v);
     } else {
-      uint4* dst = reinterpret_cast<uint4*>(hq_smem + (chunk - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+      uint4* dst = reinterpret_cast<uint4*>(hq_smem + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[32 * i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
   };
-  auto unpark = [&](int chunk, int s, Lane4& t) {
+  auto unpark = [&](int g, Lane4& t) {
     uint32_t v[64];
-    if (chunk < kI8ParkTmemTiles) {
-      tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(s), v);
+    if (g < kI8ParkTmemTiles) {
+      tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(g >> 4), v);
       tmem_wait_ld();
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(hq_smem + (chunk - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+      const uint4* src = reinterpret_cast<const uint4*>(hq_smem + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint4 w = src[32 * i];
@@ -652,39 +660,60 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     words_to_lane4(v, t);
   };
 
+  const int64_t n_blocks = (p.M + B - 1) / B;
   int64_t n = 0;
-  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x, ++n) {
-    // walk 1: rotate, the tile amax, park
-    float amax = 0.0f;
-    int s = 0;
-    for (int chunk = wid; chunk < T; chunk += kI8Warps, ++s) {
-      Lane4 t;
-      load(row, chunk, t);
-      rotate_regular<G>(t);
+  for (int64_t blk = blockIdx.x; blk < n_blocks; blk += gridDim.x, ++n) {
+    const int64_t row0 = blk * B;
+    // walk 1: rotate, the per-row tile amax, park
+    float amax[kRows];
 #pragma unroll
-      for (int k = 0; k < 2; ++k)
-        amax = max3_nan(amax, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
-      park(chunk, s, t);
+    for (int r = 0; r < kRows; ++r) amax[r] = 0.0f;
+    for (int g = wid; g < n_g; g += kI8Warps) {
+      const int b = MULTI ? static_cast<int>((static_cast<uint32_t>(g) * inv_T) >> 16) : 0;
+      if (MULTI && row0 + b >= p.M) break;  // rows past the end: every later g is past it too
+      Lane4 t;
+      load(row0 + b, g - b * T, t);
+      rotate_regular<G>(t);
+      float m = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) m = max3_nan(m, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+        if (r == b) amax[r] = max_nan(amax[r], m);
+      park(g, t);
     }
-    amax = warp_max_nonneg(amax);
-    if (lane == 0) row_max[n & 1][wid] = amax;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const float a = warp_max_nonneg(amax[r]);
+      if (lane == 0) row_max[n & 1][r][wid] = a;
+    }
     tmem_wait_st();  // this thread's parked columns are written before it reads them back
     __syncthreads();
-    const float row_amax = warp_max_nonneg(lane < kI8Warps ? row_max[n & 1][lane] : 0.0f);
-    const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
-    const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
-    if (threadIdx.x == 0) p.scales[row] = scale;
+    float inv[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const float row_amax = warp_max_nonneg(lane < kI8Warps ? row_max[n & 1][r][lane] : 0.0f);
+      const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
+      inv[r] = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
+      if (threadIdx.x == 0 && r < B && row0 + r < p.M) p.scales[row0 + r] = scale;
+    }
     // walk 2: the codes (rint by the magic constant, as in k_rotate_quant_int8)
-    const float2 inv2 = make_float2(inv, inv);
     const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
     const float2 one2 = make_float2(1.0f, 1.0f);
-    s = 0;
-    for (int chunk = wid; chunk < T; chunk += kI8Warps, ++s) {
+    for (int g = wid; g < n_g; g += kI8Warps) {
+      const int b = MULTI ? static_cast<int>((static_cast<uint32_t>(g) * inv_T) >> 16) : 0;
+      if (MULTI && row0 + b >= p.M) break;
+      const int chunk = g - b * T;
+      float inv_b = inv[0];
+#pragma unroll
+      for (int r = 1; r < kRows; ++r)
+        if (r == b) inv_b = inv[r];
+      const float2 inv2 = make_float2(inv_b, inv_b);
       Lane4 t;
-      unpark(chunk, s, t);
+      unpark(g, t);
       const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
       const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
-      int8_t* qrow = p.q + row * p.K + c0;
+      int8_t* qrow = p.q + (row0 + b) * p.K + c0;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         uint32_t bx[16], by[16];

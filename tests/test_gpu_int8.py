@@ -60,6 +60,8 @@ SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16),
           # tiles, a ragged 19th, 32, a ragged 49th, 59 (the most parked on chip)
           (3, 34816, 16), (5, 36864 + 1024, 1024), (4, 65536, 256), (2, 98304 + 16, 4),
           (3, 65536, 64), (3, 120832, 16),
+          # 2 or 3 such rows per CTA step (T <= 24): a partial last block, more blocks than SMs
+          (301, 36864, 256), (500, 40960, 16), (7, 47104 + 64, 64),
           # longer still, each row read twice: a ragged 60th tile, 60 and 64 tiles
           (2, 120832 + 16, 16), (2, 122880, 256), (2, 131072, 1024)]
 
