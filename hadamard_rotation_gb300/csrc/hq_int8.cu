@@ -14,6 +14,10 @@ using hq::cuda_fail;
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Dynamic shared memory the parking kernel may take: the 227 KB a CTA may opt in to, less
+// 2 KB for its static shared memory and the 1 KB alignment of the dynamic part.
+constexpr size_t kI8ParkSmemLimit = 227 * 1024 - 2 * 1024;
+
 // INT8 per-token rotate-quant: one CTA of kI8Threads per SM, looping over row groups.
 template <int G, bool BF16, int MODE, bool FULL>
 hq_status launch_int8(const hq::I8Params& p, hq_stream stream) {
@@ -53,14 +57,13 @@ hq_status launch_int8_long(const hq::I8Params& p, hq_stream stream) {
 }
 
 // Rows of 17 to 59 warp tiles: parked whole on chip (tensor memory and shared memory), one
-// CTA of kI8Threads per SM.
-template <int G, bool BF16>
-hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
-  auto kernel = p.rows_per_block > 1 ? hq::k_rotate_quant_int8_park<G, BF16, true>
-                                     : hq::k_rotate_quant_int8_park<G, BF16, false>;
-  const int n_g = p.rows_per_block * p.tiles_per_row;
-  const int smem_tiles = n_g > hq::kI8ParkTmemTiles ? n_g - hq::kI8ParkTmemTiles : 0;
-  const size_t smem = static_cast<size_t>(smem_tiles) * hq::kI8ParkTileBytes;
+// CTA of kI8Threads per SM; bf16 rows load through a TMA ring of 2 or 1 tiles per warp when
+// shared memory has room for it beside the parked tiles.
+template <int G, bool BF16, int STAGES>
+hq_status launch_int8_park_ring(const hq::I8Params& p, size_t park_bytes, hq_stream stream) {
+  auto kernel = p.rows_per_block > 1 ? hq::k_rotate_quant_int8_park<G, BF16, true, STAGES>
+                                     : hq::k_rotate_quant_int8_park<G, BF16, false, STAGES>;
+  const size_t smem = park_bytes + static_cast<size_t>(hq::i8_park_ring_bytes(STAGES));
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -76,6 +79,20 @@ hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return HQ_OK;
+}
+
+template <int G, bool BF16>
+hq_status launch_int8_park(const hq::I8Params& p, hq_stream stream) {
+  const int n_g = p.rows_per_block * p.tiles_per_row;
+  const int smem_tiles = n_g > hq::kI8ParkTmemTiles ? n_g - hq::kI8ParkTmemTiles : 0;
+  const size_t park = static_cast<size_t>(smem_tiles) * hq::kI8ParkTileBytes;
+  if constexpr (BF16) {
+    if (park + hq::i8_park_ring_bytes(2) <= kI8ParkSmemLimit)
+      return launch_int8_park_ring<G, true, 2>(p, park, stream);
+    if (park + hq::i8_park_ring_bytes(1) <= kI8ParkSmemLimit)
+      return launch_int8_park_ring<G, true, 1>(p, park, stream);
+  }
+  return launch_int8_park_ring<G, BF16, 0>(p, park, stream);
 }
 
 template <int G>

@@ -570,26 +570,38 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
 // A CTA of 16 warps takes blocks of B rows (B T <= 59; B = 2 or 3 for T <= 24, which
 // evens out the warps' shares), blocks blockIdx.x, blockIdx.x + gridDim.x, ...; the
 // block's tiles g = 0 .. B T - 1 (row g / T, chunk g % T) are dealt round robin, warp w
-// taking g = w, w + 16, ...  Tiles 0 .. 31 of a block park in tensor memory (two per
-// warp, as above), tiles 32 .. in shared memory (8 KB each).  Walk 1 loads (16-byte
-// vector loads straight into registers), rotates, keeps the per-row tile amax and parks
-// the tile; the CTA meets at a barrier (per row and warp one amax word, double-buffered
-// by block parity, so a warp can be at most one block ahead of a reader); walk 2 takes
-// each tile back, quantizes and stores it.  A warp parks and takes back only its own
-// tiles, so the only wait is the CTA barrier and no bound is needed.
+// taking g = w, w + 16, ... (its j-th: g = w + 16 j).  Tiles 0 .. 31 of a block park in
+// tensor memory (two per warp, as above), tiles 32 .. in shared memory (8 KB each).
+// Walk 1 loads, rotates, keeps the per-row tile amax and parks the tile; the CTA meets at
+// a barrier (per row and warp one amax word, double-buffered by block parity, so a warp
+// can be at most one block ahead of a reader); walk 2 takes each tile back, quantizes and
+// stores it.
+// Loads: with STAGES > 0 (bf16, when shared memory has room beside the parked tiles) a
+// per-warp TMA ring of STAGES tiles: the warp's first STAGES tiles of a block are copied
+// while the block before is in walk 2 (which reads no x), tile j + STAGES once tile j is
+// parked.  A ring wait is bounded: a warp whose wait runs out records
+// the fault, waits (bounded) for its copies in flight and marks the CTA broken, and
+// every warp leaves after the next barrier.  STAGES = 0: 16-byte vector loads straight
+// into registers.
 // ---------------------------------------------------------------------------
 constexpr int kI8ParkTmemTiles = 2 * kI8Warps;                          // 32
 constexpr int kI8ParkTileBytes = kI8TileElems * 4;                      // 8 KB of fp32
 constexpr int kI8ParkSmemTiles = 27;                                    // 216 KB
 constexpr int kI8ParkMaxTiles = kI8ParkTmemTiles + kI8ParkSmemTiles;  // 59
 constexpr int kI8ParkMaxRows = 3;                                       // B (T >= 17)
+// Shared memory of the ring: STAGES bf16 tiles and as many mbarriers per warp.
+__host__ __device__ constexpr int i8_park_ring_bytes(int stages) {
+  return kI8Warps * stages * (kI8TileElems * 2 + 8);
+}
 
 // MULTI: blocks of B > 1 rows (B = 1 takes a leaner path).
-template <int G, bool BF16, bool MULTI>
+template <int G, bool BF16, bool MULTI, int STAGES>
 __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Params p) {
+  static_assert(STAGES == 0 || BF16, "the ring holds bf16 tiles");
   constexpr int kRows = MULTI ? kI8ParkMaxRows : 1;
   constexpr int es = BF16 ? 2 : 4;
   constexpr int n16 = BF16 ? 2 : 4;  // 16-byte words per block of 16 channels
+  constexpr int kRingTile = kI8TileElems * 2;
   constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -600,32 +612,96 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
   const uint32_t inv_T = (65536u + static_cast<uint32_t>(T) - 1u) / static_cast<uint32_t>(T);
   __shared__ float row_max[2][kRows][kI8Warps];
   __shared__ uint32_t tmem_base_slot;
-  extern __shared__ __align__(1024) uint8_t hq_smem[];  // tiles 32 .. n_g - 1 of a block
+  __shared__ volatile int cta_broken;
+  // [ring: 16 warps x STAGES tiles][ring mbarriers][tiles 32 .. n_g - 1 of a block]
+  extern __shared__ __align__(1024) uint8_t hq_smem[];
+  uint8_t* const park_base = hq_smem + i8_park_ring_bytes(STAGES);
+  uint8_t* const ring = hq_smem + wid * STAGES * kRingTile;
+  const uint32_t bar0 = smem_addr(hq_smem + kI8Warps * STAGES * kRingTile) + wid * STAGES * 8;
 
+  if (threadIdx.x == 0) cta_broken = 0;
+  if constexpr (STAGES > 0) {
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + s * 8, 1);
+      fence_mbar_init();
+    }
+  }
   if (wid == 0) tmem_alloc_all(smem_addr(&tmem_base_slot));
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
   const uint32_t tmem_warp = tmem_base_slot + ((32u * static_cast<uint32_t>(wid & 3)) << 16) +
                              128u * static_cast<uint32_t>(wid >> 2);
+  const int64_t n_blocks = (p.M + B - 1) / B;
+  auto row_of = [&](int g) { return MULTI ? static_cast<int>((static_cast<uint32_t>(g) * inv_T) >> 16) : 0; };
 
-  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0).
-  auto load = [&](int64_t row, int chunk, Lane4& t) {
+  uint32_t k = 0;       // this warp's tiles read from the ring (its position)
+  uint32_t issued = 0;  // lane 0: tiles handed to TMA
+  // lane 0: copy the warp's j-th tile of the block whose first row is row0, if it exists,
+  // into the slot the ring gives it
+#define HQ_I8_PARK_FETCH(row0_, j_)                                                              \
+  do {                                                                                          \
+    const int g_ = wid + kI8Warps * (j_);                                                       \
+    if (g_ < n_g) {                                                                             \
+      const int b_ = row_of(g_);                                                                \
+      if ((row0_) + b_ < p.M) {                                                                 \
+        const int64_t c0_ = static_cast<int64_t>(g_ - b_ * T) * kI8TileElems;                   \
+        const int64_t nv_ = p.K - c0_ < kI8TileElems ? p.K - c0_ : kI8TileElems;                \
+        const int slot_ = static_cast<int>(issued % STAGES);                                    \
+        tma_load(smem_addr(ring + slot_ * kRingTile), p.x + ((row0_) + b_) * p.ldx_bytes + c0_ * es, \
+                 static_cast<uint32_t>(nv_ * es), bar0 + slot_ * 8, l2_stream_policy());        \
+        ++issued;                                                                               \
+      }                                                                                         \
+    }                                                                                           \
+  } while (0)
+  if constexpr (STAGES > 0) {
+    __syncwarp();
+    if (lane == 0 && blockIdx.x < n_blocks)
+      for (int j = 0; j < STAGES; ++j) HQ_I8_PARK_FETCH(static_cast<int64_t>(blockIdx.x) * B, j);
+  }
+
+  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0);
+  // from the ring: false if the wait ran out (the CTA is then broken).
+  auto load = [&](int64_t row0, int j, int64_t row, int chunk, Lane4& t) {
     const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
     const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
-    const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
+    if constexpr (STAGES > 0) {
+      const int slot = static_cast<int>(k % STAGES);
+      const bool ok = mbar_wait(bar0 + slot * 8, (k / STAGES) & 1u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) return false;  // handled after walk 1
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t bl = i8_in_block<G>(lane, j);
-      uint4 w4[n16];
-      const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t bl = i8_in_block<G>(lane, q);
+        uint4 w4[2];
+        if (static_cast<int64_t>(bl) * 16 < nvalid) {
+          const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kRingTile + bl * 32u);
+          w4[0] = src[0];
+          w4[1] = src[1];
+        } else {
+          w4[0] = w4[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        float f[16];
+        widen<true>(w4, f);
+        put_block(t, q, f);
+      }
+      __syncwarp();  // every lane has read the slot (refilled after the tile is parked)
+      ++k;
+    } else {
+      const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
 #pragma unroll
-      for (int k = 0; k < n16; ++k)
-        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + k) : make_uint4(0u, 0u, 0u, 0u);
-      float f[16];
-      widen<BF16>(w4, f);
-      put_block(t, j, f);
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t bl = i8_in_block<G>(lane, q);
+        uint4 w4[n16];
+        const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+#pragma unroll
+        for (int e = 0; e < n16; ++e)
+          w4[e] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + e) : make_uint4(0u, 0u, 0u, 0u);
+        float f[16];
+        widen<BF16>(w4, f);
+        put_block(t, q, f);
+      }
     }
+    return true;
   };
   // Tile g of the block in its place: TMEM slot g / 16 of this warp for g < 32, else
   // shared-memory slot g - 32, 16 float4 per lane, float4 i of lane l at 16 (32 i + l) (each
@@ -636,7 +712,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     if (g < kI8ParkTmemTiles) {
       tmem_st64(tmem_warp + 64u * static_cast<uint32_t>(g >> 4), v);
     } else {
-      uint4* dst = reinterpret_cast<uint4*>(hq_smem + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+      uint4* dst = reinterpret_cast<uint4*>(park_base + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[32 * i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
@@ -647,7 +723,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       tmem_ld64(tmem_warp + 64u * static_cast<uint32_t>(g >> 4), v);
       tmem_wait_ld();
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(hq_smem + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
+      const uint4* src = reinterpret_cast<const uint4*>(park_base + (g - kI8ParkTmemTiles) * kI8ParkTileBytes) + lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint4 w = src[32 * i];
@@ -660,7 +736,6 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     words_to_lane4(v, t);
   };
 
-  const int64_t n_blocks = (p.M + B - 1) / B;
   int64_t n = 0;
   for (int64_t blk = blockIdx.x; blk < n_blocks; blk += gridDim.x, ++n) {
     const int64_t row0 = blk * B;
@@ -668,19 +743,37 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     float amax[kRows];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) amax[r] = 0.0f;
-    for (int g = wid; g < n_g; g += kI8Warps) {
-      const int b = MULTI ? static_cast<int>((static_cast<uint32_t>(g) * inv_T) >> 16) : 0;
+    int j = 0;
+    bool timed_out = false;
+    for (int g = wid; g < n_g; g += kI8Warps, ++j) {
+      const int b = row_of(g);
       if (MULTI && row0 + b >= p.M) break;  // rows past the end: every later g is past it too
       Lane4 t;
-      load(row0 + b, g - b * T, t);
+      if (!load(row0, j, row0 + b, g - b * T, t)) {
+        timed_out = true;
+        break;
+      }
       rotate_regular<G>(t);
       float m = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) m = max3_nan(m, block_absmax<false>(t.P[k]), block_absmax<true>(t.P[k]));
+      for (int q = 0; q < 2; ++q) m = max3_nan(m, block_absmax<false>(t.P[q]), block_absmax<true>(t.P[q]));
 #pragma unroll
       for (int r = 0; r < kRows; ++r)
         if (r == b) amax[r] = max_nan(amax[r], m);
       park(g, t);
+      if constexpr (STAGES > 0) {  // the slot this tile came from takes tile j + STAGES
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          HQ_I8_PARK_FETCH(row0, j + STAGES);
+        }
+      }
+    }
+    if (timed_out) {  // record it, wait (bounded) for this warp's copies still in flight
+      if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+      const uint32_t n_issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
+      for (uint32_t m = k; m < n_issued; ++m)
+        mbar_wait(bar0 + static_cast<int>(m % STAGES) * 8, (m / STAGES) & 1u);
+      cta_broken = 1;
     }
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
@@ -689,6 +782,11 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     }
     tmem_wait_st();  // this thread's parked columns are written before it reads them back
     __syncthreads();
+    if (cta_broken) break;  // the same in every thread after the barrier
+    if constexpr (STAGES > 0) {  // the next block's first tiles, while this one is in walk 2
+      if (lane == 0 && blk + gridDim.x < n_blocks)
+        for (int a = 0; a < STAGES; ++a) HQ_I8_PARK_FETCH((blk + gridDim.x) * B, a);
+    }
     float inv[kRows];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
@@ -701,7 +799,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
     const float2 one2 = make_float2(1.0f, 1.0f);
     for (int g = wid; g < n_g; g += kI8Warps) {
-      const int b = MULTI ? static_cast<int>((static_cast<uint32_t>(g) * inv_T) >> 16) : 0;
+      const int b = row_of(g);
       if (MULTI && row0 + b >= p.M) break;
       const int chunk = g - b * T;
       float inv_b = inv[0];
@@ -715,16 +813,16 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
       int8_t* qrow = p.q + (row0 + b) * p.K + c0;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t bx[16], by[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+          const float2 w = fma2(mul2(t.P[q][i], inv2), one2, magic2);
           bx[i] = __float_as_uint(w.x);
           by[i] = __float_as_uint(w.y);
         }
-        const uint32_t box = i8_out_block<G>(lane, 2 * k);
-        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
+        const uint32_t box = i8_out_block<G>(lane, 2 * q);
+        const uint32_t boy = i8_out_block<G>(lane, 2 * q + 1);
         if (static_cast<int64_t>(box) * 16 < nvalid)
           __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
                  make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
@@ -746,6 +844,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
     tmem_dealloc_all(tmem_base_slot);
   }
 }
+#undef HQ_I8_PARK_FETCH
 
 // ---------------------------------------------------------------------------
 // Rows longer than the chip can park (K > 120832 channels).  A CTA of 16 warps takes
