@@ -17,6 +17,7 @@ from .api import (  # noqa: F401
     hq_rotate_quant_mxfp4_ws,
     hq_rotate_quant_nvfp4,
     hq_rotate_quant_nvfp4_delayed,
+    hq_rotate_quant_nvfp4_delayed_ws,
     hq_rotate_quant_nvfp4_swizzled,
     hq_rotate_quant_nvfp4_swizzled_ws,
     hq_rotate_quant_nvfp4_ws,
@@ -41,6 +42,7 @@ __all__ = [
     "hq_rotate_quant_mxfp4_ws",
     "hq_rotate_quant_nvfp4",
     "hq_rotate_quant_nvfp4_delayed",
+    "hq_rotate_quant_nvfp4_delayed_ws",
     "hq_rotate_quant_nvfp4_swizzled",
     "hq_rotate_quant_nvfp4_swizzled_ws",
     "hq_rotate_quant_nvfp4_ws",

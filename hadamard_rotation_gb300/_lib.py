@@ -58,6 +58,8 @@ def load() -> ctypes.CDLL:
         lib.hq_quantize_nvfp4.restype = i32
         lib.hq_rotate_quant_nvfp4_delayed.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]
         lib.hq_rotate_quant_nvfp4_delayed.restype = i32
+        lib.hq_rotate_quant_nvfp4_delayed_ws.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p, p]
+        lib.hq_rotate_quant_nvfp4_delayed_ws.restype = i32
         lib.hq_rotate_quant_nvfp4_swizzled.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p]
         lib.hq_rotate_quant_nvfp4_swizzled.restype = i32
         lib.hq_rotate_quant_nvfp4_swizzled_ws.argtypes = [p, i32, i64, i64, i64, i32, p, p, p, p, p, p]

@@ -219,6 +219,31 @@ def hq_rotate_quant_nvfp4_delayed(x: torch.Tensor, group: int, amax_prev: torch.
     return q, scales, s_global, amax_next
 
 
+def hq_rotate_quant_nvfp4_delayed_ws(x: torch.Tensor, group: int, amax_prev: torch.Tensor,
+                                     amax_next: torch.Tensor | None = None,
+                                     q: torch.Tensor | None = None,
+                                     scales: torch.Tensor | None = None,
+                                     s_global: torch.Tensor | None = None,
+                                     workspace: torch.Tensor | None = None,
+                                     stream: torch.cuda.Stream | None = None):
+    """hq_rotate_quant_nvfp4_delayed with a workspace (as hq_rotate_quant_nvfp4_ws; default: the
+    one this binding keeps per device and stream): tiles handed out at run time, and the next
+    amax reduced in the workspace instead of after a memset.  Returns (q, scales, s_global,
+    amax_next)."""
+    dt, M, K, ldx = _x_args(x)
+    amax_prev = _need(amax_prev, (1,), torch.float32, x.device, "amax_prev")
+    amax_next = _need(amax_next, (1,), torch.float32, x.device, "amax_next")
+    q = _need(q, (M, K // 2), torch.uint8, x.device, "q")
+    scales = _need(scales, (M, K // 16), torch.uint8, x.device, "scales")
+    s_global = _need(s_global, (1,), torch.float32, x.device, "s_global")
+    workspace = _workspace(x.device, stream) if workspace is None else _need(
+        workspace, (HQ_QUANTIZE_WORKSPACE_WORDS,), torch.int32, x.device, "workspace")
+    _call(x.device, "hq_rotate_quant_nvfp4_delayed_ws", _ptr(x), dt, M, K, ldx, group,
+          _ptr(amax_prev), _ptr(amax_next), _ptr(q), _ptr(scales), _ptr(s_global), _ptr(workspace),
+          stream=stream)
+    return q, scales, s_global, amax_next
+
+
 def hq_rotate_quant_mxfp4(x: torch.Tensor, group: int, q: torch.Tensor | None = None,
                           scales: torch.Tensor | None = None,
                           stream: torch.cuda.Stream | None = None):

@@ -227,9 +227,11 @@ hq_status check_x(const void* x, hq_dtype dt, int64_t M, int64_t K, int64_t ldx,
   return HQ_OK;
 }
 
-// Workspace words (HQ_QUANTIZE_WORKSPACE_WORDS in all): [0] unused, [1] pass 1's amax bits,
-// [2] CTAs of pass 1 done, [3] warps done with the tile counters; then the tile counters of the run-time split from word kSchedWord on, each on
-// its own 128-byte line.  A call that records no fault leaves every word 0.
+// Workspace words (HQ_QUANTIZE_WORKSPACE_WORDS in all): [0] unused, [1] the amax being
+// reduced (pass 1 of hq_quantize_nvfp4, or the next amax of the delayed pass), [2] CTAs of
+// that kernel done, [3] warps done with the tile counters; then the tile counters of the
+// run-time split from word kSchedWord on, each on its own 128-byte line.  A call that records
+// no fault leaves every word 0.
 constexpr int kSchedWord = hq::kSchedStrideWords;
 static_assert(kSchedWord + hq::kSchedClasses * hq::kSchedStrideWords <= HQ_QUANTIZE_WORKSPACE_WORDS,
               "workspace too small for the tile counters");
@@ -304,11 +306,11 @@ template <int G, bool NEXT>
 hq_status dispatch_quant(const hq::Params& p, bool bf16, bool strided, hq_stream s) {
   using hq::k_rotate_quant_nvfp4;
   constexpr int kMode = HQ_PASS2_MODE;
-  if constexpr (!NEXT && kMode == hq::kLoadTma) {
+  if constexpr (kMode == hq::kLoadTma) {
     if (p.sched != nullptr && !strided)  // tiles handed out at run time
-      return bf16 ? launch(k_rotate_quant_nvfp4<G, true, kMode, false, false, true>, p, s,
+      return bf16 ? launch(k_rotate_quant_nvfp4<G, true, kMode, NEXT, false, true>, p, s,
                            ring_bytes<HQ_PASS2_STAGES>(kMode, true), true)
-                  : launch(k_rotate_quant_nvfp4<G, false, kMode, false, false, true>, p, s,
+                  : launch(k_rotate_quant_nvfp4<G, false, kMode, NEXT, false, true>, p, s,
                            ring_bytes<HQ_PASS2_STAGES>(kMode, false), true);
   }
   if (bf16)
@@ -509,14 +511,14 @@ hq_status hq_rotate_quant_nvfp4_swizzled(const void* x, hq_dtype dtype, int64_t 
                                            nullptr, stream);
 }
 
-hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M, int64_t K,
-                                        int64_t ldx, int group, const float* amax_prev,
-                                        float* amax_next, uint8_t* q, uint8_t* scales,
-                                        float* s_global, hq_stream stream) {
+hq_status hq_rotate_quant_nvfp4_delayed_ws(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                           int64_t ldx, int group, const float* amax_prev,
+                                           float* amax_next, uint8_t* q, uint8_t* scales,
+                                           float* s_global, uint32_t* workspace, hq_stream stream) {
   hq_status st = check_x(x, dtype, M, K, ldx, group);
   if (st != HQ_OK) return st;
   if (!amax_next) return HQ_ERR_NULL;
-  if (!aligned(amax_next, 4)) return HQ_ERR_ALIGN;
+  if (!aligned(amax_next, 4) || (workspace && !aligned(workspace, 4))) return HQ_ERR_ALIGN;
   if (M > 0 && K > 0) {
     if (!amax_prev || !q || !scales) return HQ_ERR_NULL;
     if (amax_prev == amax_next) return HQ_ERR_ALIAS;
@@ -524,9 +526,11 @@ hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M
         (s_global && !aligned(s_global, 4)))
       return HQ_ERR_ALIGN;
   }
-  cudaError_t e = cudaMemsetAsync(amax_next, 0, sizeof(float), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (M == 0 || K == 0) return HQ_OK;
+  if (M == 0 || K == 0 || !workspace) {
+    cudaError_t e = cudaMemsetAsync(amax_next, 0, sizeof(float), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (M == 0 || K == 0) return HQ_OK;
+  }
   hq::Params p = base_params(x, dtype, M, K, ldx);
   p.amax_in = amax_prev;
   p.amax_out = amax_next;
@@ -535,11 +539,28 @@ hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M
   p.sglobal_out = s_global;
   const bool bf16 = dtype == HQ_BF16;
   const bool strided = is_strided(M, K, ldx);
+  if (workspace) {  // the next amax reduced into word 1, the last CTA moves it to *amax_next
+    p.amax_out = reinterpret_cast<float*>(workspace + 1);
+    p.sync = workspace;
+    p.amax_copy = amax_next;
+    if (schedulable(p, workspace, strided)) {
+      p.sched = workspace + kSchedWord;
+      p.sched_done = workspace + 3;
+    }
+  }
   switch (group) {
     case 0: return dispatch_quant<0, true>(p, bf16, strided, stream);
     case 16: return dispatch_quant<16, true>(p, bf16, strided, stream);
     default: return dispatch_quant<256, true>(p, bf16, strided, stream);
   }
+}
+
+hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, int64_t M, int64_t K,
+                                        int64_t ldx, int group, const float* amax_prev,
+                                        float* amax_next, uint8_t* q, uint8_t* scales,
+                                        float* s_global, hq_stream stream) {
+  return hq_rotate_quant_nvfp4_delayed_ws(x, dtype, M, K, ldx, group, amax_prev, amax_next, q, scales,
+                                          s_global, nullptr, stream);
 }
 
 hq_status hq_dequant_nvfp4(const uint8_t* q, const uint8_t* scales, const float* s_global,

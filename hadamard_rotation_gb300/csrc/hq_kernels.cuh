@@ -1547,7 +1547,9 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
     for_each_rg_tile<G, BF16, HQ_PASS2_STAGES, DYN>(p, tile_body, prologue);
   else
     for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1, false, GDC, DYN>(p, tile_body, prologue);
-  if constexpr (REDUCE_NEXT) cta_amax_to_global(next_amax, p.amax_out);
+  // with p.sync (a workspace): reduced into the workspace, the last CTA moves it to p.amax_copy
+  if constexpr (REDUCE_NEXT)
+    cta_amax_to_global(next_amax, p.amax_out, p.sync ? p.sync + 2 : nullptr, p.amax_copy);
 }
 
 template <int G, bool BF16, int MODE, bool REDUCE_NEXT, bool SWZ = false, bool DYN = false>

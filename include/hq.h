@@ -113,7 +113,8 @@ HQ_API hq_status hq_rotate_quant_nvfp4(const void* x, hq_dtype dtype, int64_t M,
                                 uint8_t* scales, float* s_global, hq_stream stream);
 
 /* Size of the workspace of hq_quantize_nvfp4 and the _ws entry points (hq_rotate_quant_nvfp4_ws,
- * hq_rotate_quant_nvfp4_swizzled_ws, hq_rotate_quant_mxfp4_ws), in 32-bit words
+ * hq_rotate_quant_nvfp4_swizzled_ws, hq_rotate_quant_nvfp4_delayed_ws, hq_rotate_quant_mxfp4_ws),
+ * in 32-bit words
  * (control words and the counters of the run-time tile schedule, each on its own 128-byte
  * line). */
 #define HQ_QUANTIZE_WORKSPACE_WORDS 288
@@ -223,6 +224,19 @@ HQ_API hq_status hq_rotate_quant_nvfp4_delayed(const void* x, hq_dtype dtype, in
                                                const float* amax_prev, float* amax_next,
                                                uint8_t* q, uint8_t* scales, float* s_global,
                                                hq_stream stream);
+
+/*
+ * hq_rotate_quant_nvfp4_delayed_ws -- hq_rotate_quant_nvfp4_delayed exactly (same arguments, same
+ *   outputs), with a workspace: the tiles of x are handed to the warps at run time as in
+ *   hq_rotate_quant_nvfp4_ws, and *amax_next is reduced in the workspace and written by the
+ *   kernel's last CTA, so no memset runs before it (one launch per call).
+ *   workspace : as for hq_rotate_quant_nvfp4_ws.  NULL: hq_rotate_quant_nvfp4_delayed.
+ */
+HQ_API hq_status hq_rotate_quant_nvfp4_delayed_ws(const void* x, hq_dtype dtype, int64_t M,
+                                                  int64_t K, int64_t ldx, int group,
+                                                  const float* amax_prev, float* amax_next,
+                                                  uint8_t* q, uint8_t* scales, float* s_global,
+                                                  uint32_t* workspace, hq_stream stream);
 
 /*
  * hq_rotate_quant_mxfp4 -- MXFP4 variant: E2M1 codes with one power-of-two (E8M0) scale per 32

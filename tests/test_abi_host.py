@@ -243,6 +243,17 @@ def test_mxfp4_argument_checks(lib):
     assert lib.hq_dequant_mxfp4(P(FAKE), P(FAKE), 4, 64, 0, 1, P(FAKE), None) == 5
 
 
+def test_delayed_ws_argument_checks(lib):
+    def dw(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, ap=FAKE, an=FAKE + 64, q=FAKE, s=FAKE, sg=None, ws=FAKE + 256):
+        return lib.hq_rotate_quant_nvfp4_delayed_ws(
+            P(x) if x else None, dt, M, K, ldx, G, P(ap) if ap else None, P(an) if an else None,
+            P(q) if q else None, P(s) if s else None, P(sg) if sg else None, P(ws) if ws else None, None)
+    assert dw(an=0) == 1 and dw(ap=0) == 1 and dw(q=0) == 1 and dw(x=0) == 1
+    assert dw(an=FAKE) == 8                  # amax_prev and amax_next alias
+    assert dw(G=32) == 5 and dw(dt=2) == 4 and dw(K=24, ldx=24) == 2
+    assert dw(ws=FAKE + 2) == 3 and dw(an=FAKE + 66) == 3
+
+
 def test_swizzled_argument_checks_and_size(lib):
     def sw(x=FAKE, dt=1, M=4, K=64, ldx=64, G=16, a=FAKE, q=FAKE, s=FAKE, sg=None):
         return lib.hq_rotate_quant_nvfp4_swizzled(

@@ -1,4 +1,4 @@
-"""Single-pass, delayed-amax mode (hq_rotate_quant_nvfp4_delayed) against the oracle.
+"""Single-pass, delayed-amax mode (hq_rotate_quant_nvfp4_delayed, _ws) against the oracle.
 
 "A Fused Hadamard + NVFP4 Quantization Kernel in Triton", §2: production stacks may reuse an amax
 from a previous step so that the per-block work is a single pass.  The oracle side is the same
@@ -38,11 +38,18 @@ def rand_input(M, K, dtype, seed):
     return t if dtype == torch.float32 else t.to(dtype)
 
 
-def check(x_host, group, prev, x_dev=None):
+def check(x_host, group, prev, x_dev=None, ws=None):
     x = x_dev if x_dev is not None else x_host.cuda()
     a_prev = torch.tensor([prev], dtype=torch.float32, device=x.device)
-    q, s, sg, a_next = hq.hq_rotate_quant_nvfp4_delayed(x, group, a_prev)
+    if ws is None:
+        q, s, sg, a_next = hq.hq_rotate_quant_nvfp4_delayed(x, group, a_prev)
+    else:
+        a_next = torch.full((1,), 7.0, dtype=torch.float32, device=x.device)  # overwritten
+        q, s, sg, a_next = hq.hq_rotate_quant_nvfp4_delayed_ws(x, group, a_prev, amax_next=a_next,
+                                                               workspace=ws)
     torch.cuda.synchronize()
+    if ws is not None:
+        assert not ws.any().item(), "the workspace is not back to 0"
     xo = synth.as_oracle_array(x_host)
     oq, os_, _, osg = oracle.quantize(xo, group, amax=float(np.float32(prev)))
     oamax, _ = oracle.rot_amax(xo, group)
@@ -112,3 +119,21 @@ def test_delayed_rejects_aliased_amax():
     a = torch.ones(1, device="cuda")
     with pytest.raises(hq.HQError):
         hq.hq_rotate_quant_nvfp4_delayed(x, 16, a, amax_next=a)
+
+
+# hq_rotate_quant_nvfp4_delayed_ws: the next amax reduced in the workspace (no memset), the tiles
+# handed out at run time from 16384 tiles on; twice on one workspace.
+@pytest.mark.parametrize("M,K,group", [(333, 1024, 16), (4099, 8192, 16), (16385, 2048, 256), (2053, 17408, 0)])
+def test_delayed_with_a_workspace(M, K, group):
+    x = rand_input(M, K, torch.bfloat16, seed=M + K + group)
+    xd = x.cuda()
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    true_amax = check(x, group, 1.0, x_dev=xd, ws=ws)
+    check(x, group, true_amax, x_dev=xd, ws=ws)
+    check(x, group, true_amax * 0.3, x_dev=xd, ws=ws)
+
+
+def test_delayed_with_a_workspace_strided_rows():
+    big = rand_input(4099, 8192 + 64, torch.bfloat16, seed=5)
+    ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+    check(big[:, :8192].contiguous(), 16, 2.5, x_dev=big.cuda()[:, :8192], ws=ws)
