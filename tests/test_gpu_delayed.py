@@ -124,8 +124,9 @@ def test_delayed_rejects_aliased_amax():
 # hq_rotate_quant_nvfp4_delayed_ws: the next amax reduced in the workspace (no memset), the tiles
 # handed out at run time from 16384 tiles on; twice on one workspace.
 @pytest.mark.parametrize("M,K,group", [(333, 1024, 16), (4099, 8192, 16), (16385, 2048, 256), (2053, 17408, 0)])
-def test_delayed_with_a_workspace(M, K, group):
-    x = rand_input(M, K, torch.bfloat16, seed=M + K + group)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_delayed_with_a_workspace(M, K, group, dtype):
+    x = rand_input(M, K, dtype, seed=M + K + group)
     xd = x.cuda()
     ws = torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
     true_amax = check(x, group, 1.0, x_dev=xd, ws=ws)

@@ -98,8 +98,9 @@ def new_workspace():
 # (2^21 16-blocks); below that, and for strided rows, it is the fixed split.
 @pytest.mark.parametrize("M,K,group", [(1, 32, 16), (999, 4352, 16), (4099, 8192, 16), (16385, 2048, 256),
                                        (2053, 17408, 0), (4099, 8192, 256)])
-def test_mxfp4_with_a_workspace(M, K, group):
-    x = rand_input(M, K, torch.bfloat16, seed=M + 3 * K + group)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mxfp4_with_a_workspace(M, K, group, dtype):
+    x = rand_input(M, K, dtype, seed=M + 3 * K + group)
     ws = new_workspace()
     for _ in range(2):  # twice on one workspace: the first call leaves it ready for the next
         check(x, group, ws=ws)

@@ -85,10 +85,14 @@ def test_swizzled_strided_rows(group):
 
 # hq_rotate_quant_nvfp4_swizzled_ws: the units (8 rows x 128 blocks) are handed out at run time
 # from 16384 tiles (2048 units) on; below that it is the fixed split.  Twice on one workspace.
-@pytest.mark.parametrize("M,K,group", [(129, 80, 16), (4099, 8192, 16), (2053, 17408, 16), (4099, 8192, 256),
-                                       (2053, 17408, 0)])
-def test_swizzled_with_a_workspace(M, K, group):
-    x = varied(M, K, seed=M + K + group)
+@pytest.mark.parametrize("M,K,group,dtype", [(129, 80, 16, torch.bfloat16), (4099, 8192, 16, torch.bfloat16),
+                                             (2053, 17408, 16, torch.bfloat16), (4099, 8192, 256, torch.bfloat16),
+                                             (2053, 17408, 0, torch.bfloat16), (4099, 8192, 16, torch.float32),
+                                             (2053, 17408, 256, torch.float32)])
+def test_swizzled_with_a_workspace(M, K, group, dtype):
+    if K % max(group, 16):
+        pytest.skip("K not a multiple of the group")
+    x = varied(M, K, seed=M + K + group, dtype=dtype)
     xd = x.cuda()
     oq, os_, _, osg = oracle.quantize(synth.as_oracle_array(x), group)
     amax = hq.hq_rot_amax(xd, group)
