@@ -291,3 +291,35 @@ def test_run_time_schedule_on_two_streams_with_their_own_workspaces():
         oq, os_, _, osg = oracle.quantize(synth.as_oracle_array(x_host), 16)
         assert np.array_equal(q.cpu().numpy(), oq) and np.array_equal(s.cpu().numpy(), os_)
         assert settled(ws)
+
+
+def test_workspace_forms_on_two_streams_with_their_own_workspaces():
+    """The swizzled-scale pass (units handed out at run time), MXFP4 and the delayed pass (tiles
+    handed out at run time) on two streams at the same time, each stream with its own
+    workspace, three rounds: every result exact, every workspace 0."""
+    xs = [rand_input(4099, 8192, torch.bfloat16, seed=71 + i) for i in range(2)]
+    streams = [torch.cuda.Stream() for _ in xs]
+    wss = [torch.zeros(hq.api.HQ_QUANTIZE_WORKSPACE_WORDS, dtype=torch.int32, device="cuda")
+           for _ in xs]
+    xd = [x.cuda() for x in xs]
+    amaxes = [hq.hq_rot_amax(x, 16) for x in xd]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        outs = []
+        for x, st, ws, amax in zip(xd, streams, wss, amaxes):
+            with torch.cuda.stream(st):
+                sw = hq.hq_rotate_quant_nvfp4_swizzled_ws(x, 16, amax, workspace=ws, stream=st)
+                mx = hq.hq_rotate_quant_mxfp4_ws(x, 16, workspace=ws, stream=st)
+                dl = hq.hq_rotate_quant_nvfp4_delayed_ws(x, 16, amax, workspace=ws, stream=st)
+                outs.append((sw, mx, dl))
+        torch.cuda.synchronize()
+        for x_host, (sw, mx, dl), ws in zip(xs, outs, wss):
+            xo = synth.as_oracle_array(x_host)
+            oq, os_, oamax, osg = oracle.quantize(xo, 16)
+            assert np.array_equal(sw[0].cpu().numpy(), oq)
+            assert np.array_equal(sw[1].cpu().numpy(), oracle.swizzle_scales(os_))
+            mq, ms = oracle.quantize_mxfp4(xo, 16)
+            assert np.array_equal(mx[0].cpu().numpy(), mq) and np.array_equal(mx[1].cpu().numpy(), ms)
+            assert np.array_equal(dl[0].cpu().numpy(), oq) and np.array_equal(dl[1].cpu().numpy(), os_)
+            assert f32_bits(dl[3].cpu().numpy())[0] == f32_bits([oamax])[0]
+            assert settled(ws)
