@@ -17,9 +17,9 @@
 // 4 blocks a lane holds depends on the rotation group:
 //   G <= 16 : block 32*j + lane of the tile (j = 0..3);
 //   G == 256: the 4 lanes of a quad hold the 16 blocks of one 256-group.  In the
-//             plain layout (dequant, swizzled scales) block 16*(lane/4) + (lane%4)
+//             plain layout (dequant) block 16*(lane/4) + (lane%4)
 //             + 4*j: index bits 4,5 of the group are the lane bits, bits 6,7 the
-//             register block j.  Pass 1, pass 2 and MXFP4 use exchange layouts
+//             register block j.  Pass 1, pass 2 (all its forms) and MXFP4 use exchange layouts
 //             (slot_block) in which each cross-lane stage moves half of the values.
 // The 64 values sit in float2 pairs (block 0 with block 1, block 2 with block 3)
 // so the butterfly and the division run on the packed fp32x2 pipe of sm_100-
@@ -832,7 +832,8 @@ __device__ __forceinline__ void for_each_tile(const Params& p, Body&& body, Pre&
 // Lane 0 keeps the schedule: the unit it fetches tiles from and, once the reader reaches a
 // unit, that unit's index for the other lanes (the fetcher is STAGES < 8 tiles ahead, so at
 // most two units are in flight).
-template <int G, bool BF16, int STAGES, bool DYN = false, typename Body, typename Pre = NoPrologue>
+template <int G, bool BF16, int STAGES, bool DYN = false, int ORDER = 0, bool S1 = false, typename Body,
+          typename Pre = NoPrologue>
 __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, Pre&& pre = Pre()) {
   using R = Ring<BF16, STAGES>;
   static_assert(R::kStages < 8, "the fetcher stays within one unit of the reader");
@@ -956,7 +957,7 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, P
     const RgTile g = tile_in(cg, crs);
     bool valid[4];
     Lane4 t;
-    load_tile_smem<G, BF16, 0>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
+    load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
     __syncwarp();  // every lane has read the slot
     if (lane == 0) {
       fence_proxy_async_smem();
@@ -1354,13 +1355,13 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
 
   constexpr float c = inv_sqrt_g<G>();
   constexpr float sq = sqrt_g<G>();
-  // Register layout of a tile: the 256-group's exchange form (slot_block order 2),
-  // except for row-group tiles (SWZ), whose scale collection assumes lane_block.
-  constexpr int kOrder = (G == 256 && !SWZ) ? 2 : 0;
+  // Register layout of a tile: the 256-group's exchange form (slot_block order 2), also for
+  // row-group tiles (SWZ), whose scale gather follows out_block.
+  constexpr int kOrder = G == 256 ? 2 : 0;
   // bf16 tiles of the 256-group arrive with the first butterfly stage applied
   // (widen_stage1_bf16).  (For G = 16 the separate widen and packed stage measured
   // faster: 364 against 381 us on bf16 [32768, 28672].)
-  constexpr bool kS1 = BF16 && G == 256 && !SWZ;
+  constexpr bool kS1 = BF16 && G == 256;
 
   // The fast path's divisor pair for each E4M3 block scale, indexed by its byte
   // (0..126; the NaN 0x7F never comes out of the satfinite conversion):
@@ -1510,7 +1511,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (!valid[j]) continue;
-        __stcs(reinterpret_cast<uint2*>(q_tile + lane_block<G>(lane, j) * 8u),
+        __stcs(reinterpret_cast<uint2*>(q_tile + out_block<G, kOrder>(lane, j) * 8u),
                make_uint2(w[j][0] & keep[j], w[j][1] & keep[j]));
       }
       // Scales.  Row r, column c of the scale matrix sits at 512 * (row tile *
@@ -1519,19 +1520,28 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
       // in word 4 (rs & 1) + (rs >> 1).  Lane L collects column group L (columns
       // c0 + 4L .. + 3) of the unit's rows and writes its 32 bytes after the last
       // tile.  Blocks outside the tensor carry scale 0, which the padding must hold.
-      // Column group L sits in lanes 4 (L % 8) + m, slot L / 8 (G <= 16: block 32 j + lane),
-      // or in lanes 4 (L / 4) + m, slot L % 4 (G = 256: block 16 (lane / 4) + lane % 4 + 4 j),
-      // m = 0..3 for its 4 columns.  Each lane packs its 4 slot bytes into one word; lane L
-      // reads the words of its 4 source lanes and keeps byte `want` of each (byte permutes).
+      // G <= 16: column group L sits in lanes 4 (L % 8) + m, slot L / 8 (block 32 j + lane),
+      // m = 0..3 for its 4 columns.  G = 256 (the exchange layout, out_block): with u = L % 4,
+      // its columns 0, 1, 2, 3 sit in lanes 4 (L / 4) + 0, 3, 2, 1, slots u, u ^ 2, u ^ 2, u
+      // (lane (a, b) of the quad holds column a + 2 (a ^ b), slot 2 (u / 2 ^ b) + u % 2).  Each
+      // lane packs its 4 slot bytes into one word; lane L reads the words of its 4 source
+      // lanes and keeps one byte of each (byte permutes).
       const uint32_t all4 = __byte_perm(sb2[0], sb2[1], 0x5410);  // slot j in byte j
       const int src = (G == 256) ? (lane & ~3) : 4 * (lane & 7);
-      const uint32_t want = (G == 256) ? (lane & 3) : (lane >> 3);
-      const uint32_t sel = want | ((want + 4u) << 4);
       const uint32_t r0 = __shfl_sync(0xFFFFFFFFu, all4, src);
       const uint32_t r1 = __shfl_sync(0xFFFFFFFFu, all4, src + 1);
       const uint32_t r2 = __shfl_sync(0xFFFFFFFFu, all4, src + 2);
       const uint32_t r3 = __shfl_sync(0xFFFFFFFFu, all4, src + 3);
-      const uint32_t mine = __byte_perm(__byte_perm(r0, r1, sel), __byte_perm(r2, r3, sel), 0x5410);
+      uint32_t mine;
+      if constexpr (kOrder == 2) {
+        const uint32_t u = lane & 3, v = u ^ 2u;
+        mine = __byte_perm(__byte_perm(r0, r3, u | ((4u + v) << 4)), __byte_perm(r2, r1, v | ((4u + u) << 4)),
+                           0x5410);
+      } else {
+        const uint32_t want = lane >> 3;
+        const uint32_t sel = want | ((want + 4u) << 4);
+        mine = __byte_perm(__byte_perm(r0, r1, sel), __byte_perm(r2, r3, sel), 0x5410);
+      }
 #pragma unroll
       for (int i = 0; i < 7; ++i) swz_acc[i] = swz_acc[i + 1];
       swz_acc[7] = mine;  // swz_acc[rs] holds row rs once rs = 7
@@ -1544,7 +1554,7 @@ __device__ __forceinline__ void rotate_quant_tiles(const Params& p, const float*
     }
   };
   if constexpr (SWZ)
-    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES, DYN>(p, tile_body, prologue);
+    for_each_rg_tile<G, BF16, HQ_PASS2_STAGES, DYN, kOrder, kS1>(p, tile_body, prologue);
   else
     for_each_tile<G, BF16, MODE, HQ_PASS2_STAGES, kOrder, kS1, false, GDC, DYN>(p, tile_body, prologue);
   // with p.sync (a workspace): reduced into the workspace, the last CTA moves it to p.amax_copy
