@@ -957,13 +957,18 @@ __device__ __forceinline__ void for_each_rg_tile(const Params& p, Body&& body, P
     const RgTile g = tile_in(cg, crs);
     bool valid[4];
     Lane4 t;
-    load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
+    // the 256-group's body compiled a second time for whole tiles, as in for_each_tile
+    const bool full = G == 256 && ORDER == 2 && g.present && g.ncols == kTileBlocks;
+    if (full)
+      load_tile_smem<G, BF16, ORDER, S1, true>(ring + slot * R::kTileBytes, 0, kTileBlocks, lane, valid, t);
+    else
+      load_tile_smem<G, BF16, ORDER, S1>(ring + slot * R::kTileBytes, 0, g.present ? g.ncols : 0, lane, valid, t);
     __syncwarp();  // every lane has read the slot
     if (lane == 0) {
       fence_proxy_async_smem();
       fetch(slot);
     }
-    body(g, lane, valid, t);
+    call_body(full, g, lane, valid, t, body);
     if (++crs == 8) {
       crs = 0;
       // the fetcher is past this unit's end and within the next one (or out of units)
