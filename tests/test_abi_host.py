@@ -51,6 +51,37 @@ def test_header_compiles_as_c(tmp_path):
                     str(src), "-o", str(tmp_path / "use.o")], check=True)
 
 
+def test_a_c_program_links_and_calls_the_library(tmp_path, lib):
+    """The boundary from C itself: a C99 program built with gcc against include/hq.h and
+    linked to libhq.so calls entry points whose arguments fail validation (no GPU needed)
+    and reads the status strings."""
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "hq.h"
+int main(void) {
+  float amax;
+  unsigned char q[64], s[16];
+  unsigned int ws[HQ_QUANTIZE_WORKSPACE_WORDS];
+  hq_status a = hq_rot_amax(NULL, HQ_BF16, 4, 64, 64, 16, &amax, NULL, NULL);
+  hq_status b = hq_rotate_quant_nvfp4((const void*)q, HQ_BF16, 4, 64, 64, 32, &amax, q, s, NULL, NULL);
+  hq_status c = hq_quantize_nvfp4((const void*)q, HQ_BF16, 4, 24, 24, 16, &amax, q, s, NULL, ws, NULL);
+  hq_status d = hq_rotate_quant_mxfp4_ws((const void*)q, HQ_BF16, 4, 48, 48, 16, q, s, ws, NULL);
+  hq_status e = hq_rotate_quant_nvfp4_ws((const void*)q, HQ_BF16, 0, 64, 64, 16, &amax, q, s, NULL, ws, NULL);
+  printf("%d %d %d %d %d %d\n", (int)a, (int)b, (int)c, (int)d, (int)e, hq_version());
+  printf("%s\n", hq_status_string(a));
+  return 0;
+}
+""")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(lib._name)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                    "-L", libdir, "-lhq", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0].split() == ["1", "5", "2", "2", "0", "100"]   # NULL x, group 32, K % 16, K % 32, M = 0
+    assert out[1].startswith("HQ_ERR_NULL")
+
+
 def test_version_and_status_strings(lib):
     assert lib.hq_version() >= 100
     for code in range(9):
