@@ -22,7 +22,8 @@
 // divide 16 (finer row blocks balance the grid better).  Within a tile the
 // lane holds 4 blocks of 16 channels (G = 16: blocks 32j + lane; G = 64, 256: the
 // 4 lanes of a quad hold 16 consecutive blocks, lane % 4 being the block's digit
-// 2, in the lane-dependent slot order of i8_d3).  The rotated values never go to
+// 2 and the slot (i8_d3) its digit 3; every other lane holds the two 8-channel halves
+// of its blocks swapped, i8_half).  The rotated values never go to
 // global memory: between the rotation and the quantization, which needs the whole
 // row's amax, they wait in tensor memory (the pipeline note at the kernel), so x
 // is read once.  bf16 rows stream through the per-warp TMA ring.
@@ -31,10 +32,12 @@
 // RN(a_(3-k) - S/2) = -out_k, one FFMA2 per two values and no negation; the sign
 // alternates from step to step (the sum S of negated inputs is exactly -S), so
 // after an odd number of steps (G = 64) the quantizer multiplies by -1/scale.
-// The step on digit 2 (G = 64, 256) runs across the quad as a reduce-scatter and
-// all-gather of S (1.5 shuffles per value); each lane keeps its own input a_c and
-// produces the output of digit value 3 - c, which relabels the lane's block for
-// the stores.  Digit 3 (G = 256) is in-lane, packed two positions per FADD2.
+// The step on digit 2 (G = 64, 256) runs across the quad: the lanes c and c ^ 1 trade
+// one half of their blocks, so that each holds both values of the pair on the other
+// half, and the pair sums are traded with the lanes c ^ 2 (one shuffle per value); a
+// lane then holds, on its half of each block, the outputs of digit values 3 - c and
+// 3 - (c ^ 1), which relabels its registers for the stores.  Digit 3 (G = 256) is
+// in-lane, packed two positions per FADD2.
 #pragma once
 
 #include "hq_kernels.cuh"
@@ -76,19 +79,33 @@ __device__ __forceinline__ void h4_step(float2& a0, float2& a1, float2& a2, floa
 
 // Which digit-3 value (block index bits 2..3 within a 256-group, or which
 // 64-group of the quad for G = 64) register slot j of a lane holds, for G >= 64.
-// Slot j is P[j >> 1], component j & 1.  The map depends on the lane's position in
-// its quad so that the cross-lane step below runs the same instructions on all
-// four lanes: lane bit 0 swaps the two float2 arrays, lane bit 1 swaps .x and .y.
-// In every lane add2(P[0][i], P[1][i]) pairs digit-3 values {0, 1} and {2, 3}.
-// G = 1024 has a second cross-lane step, on digit 4 (the quad within the 1024-group,
-// lane bits 2 and 3); lane bits 2 and 3 then enter the map as well (xor-ed onto bits
-// 0 and 1), so that the lanes l, l ^ 4, l ^ 8 and l ^ 12 stand to one another as the
-// lanes of a quad do.
+// Slot j is P[j >> 1], component j & 1; add2(P[0][i], P[1][i]) pairs digit-3 values
+// {0, 1} and {2, 3}.  For G = 64 and 256 the map is the same in every lane.  G = 1024
+// has a second cross-lane step, on digit 4 (the quad within the 1024-group, lane bits 2
+// and 3), run by i8_cross_step, whose lanes need their own slot orders: lane bit 2 swaps
+// the two float2 arrays, lane bit 3 swaps .x and .y.
 template <int G>
 __device__ __forceinline__ uint32_t i8_d3(int lane, int j) {
   const int k = j >> 1, c = j & 1;
-  const int lb = (G == 1024) ? (lane ^ (lane >> 2)) : lane;
+  const int lb = (G == 1024) ? (lane >> 2) : 0;
   return static_cast<uint32_t>(((c ^ ((lb >> 1) & 1)) << 1) | (k ^ (lb & 1)));
+}
+
+// For G >= 64: 1 if the lane's registers 0..7 of a block hold its channels 8..15 (and
+// registers 8..15 channels 0..7), else 0.  The lanes c and c ^ 1 of a quad differ, c and
+// c ^ 2 agree (the digit-2 step needs that); for G = 64 and 256 the quads with odd index
+// flip it as well, so that the 8 lanes of a quarter warp read the 32 banks once when
+// they load their blocks' first 16 bytes from shared memory.  For G = 1024 the four lanes
+// of a digit-4 step (l, l ^ 4, l ^ 8, l ^ 12) must agree, so it is lane bit 0 alone.
+// G <= 16: 0.
+template <int G>
+__device__ __forceinline__ int i8_half(int lane) {
+  if constexpr (G <= 16)
+    return 0;
+  else if constexpr (G == 1024)
+    return lane & 1;
+  else
+    return (lane ^ (lane >> 2)) & 1;
 }
 
 // Block (of 16 channels, within the warp tile) that slot j of the lane loads.
@@ -104,24 +121,57 @@ __device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
     return static_cast<uint32_t>((lane >> 2) * 16 + (lane & 3) + 4 * i8_d3<G>(lane, j));
 }
 
-// Block that slot j holds after the rotation: each 4-point step leaves, in the
-// register that held input digit value d, the output of digit value 3 - d.
+// Block that slot j holds after the rotation, in registers 0..7 (r = 0) or 8..15
+// (r = 1) of the slot: each in-lane 4-point step leaves, in the register that held
+// input digit value d, the output of digit value 3 - d; after the digit-2 step the
+// lane's registers 0..7 hold digit value 3 - c and registers 8..15 digit value 3 - (c ^ 1)
+// (c = lane % 4), each on the half i8_half of the block.  G <= 16: the whole block, r = 0.
 template <int G>
-__device__ __forceinline__ uint32_t i8_out_block(int lane, int j) {
+__device__ __forceinline__ uint32_t i8_out_block(int lane, int j, int r) {
+  const int d2 = 3 ^ (lane & 3) ^ r;
   if constexpr (G <= 16)
     return static_cast<uint32_t>(32 * j + lane);
   else if constexpr (G == 64)
-    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * i8_d3<G>(lane, j));
+    return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * i8_d3<G>(lane, j));
   else if constexpr (G == 256)
-    return static_cast<uint32_t>((lane >> 2) * 16 + (3 - (lane & 3)) + 4 * (3 - i8_d3<G>(lane, j)));
+    return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * (3 - i8_d3<G>(lane, j)));
   else
-    return static_cast<uint32_t>((lane >> 4) * 64 + (3 - ((lane >> 2) & 3)) * 16 + (3 - (lane & 3)) +
+    return static_cast<uint32_t>((lane >> 4) * 64 + (3 - ((lane >> 2) & 3)) * 16 + d2 +
                                  4 * (3 - i8_d3<G>(lane, j)));
 }
 
+// The digit-2 step (G >= 64): the four values of a position sit in the same register of
+// the lanes of a quad (digit value c = lane % 4), and the lanes c and c ^ 1 hold opposite
+// halves of each block in registers 0..7 (i8_half).  The lanes c and c ^ 1 trade
+// registers 8..15, so each holds v_c and v_(c ^ 1) on its own half; the pair sums are
+// traded with the lanes c ^ 2, and every lane forms S = (v0 + v1) + (v2 + v3) (the two
+// pair sums added in either order, the same value) and the negated outputs
+// fma(S, -1/2, v_c) of digit value 3 - c and fma(S, -1/2, v_(c ^ 1)) of 3 - (c ^ 1).
+// One shuffle per value.
+__device__ __forceinline__ void i8_quad_step(Lane4& t) {
+  const float2 nh = make_float2(-0.5f, -0.5f);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float2 o;  // the pair lane's value on this lane's half
+      o.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][8 + i].x, 1);
+      o.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[k][8 + i].y, 1);
+      const float2 pr = add2(t.P[k][i], o);
+      float2 q;  // the other pair's sum
+      q.x = __shfl_xor_sync(0xFFFFFFFFu, pr.x, 2);
+      q.y = __shfl_xor_sync(0xFFFFFFFFu, pr.y, 2);
+      const float2 s = add2(pr, q);
+      t.P[k][i] = fma2(s, nh, t.P[k][i]);
+      t.P[k][8 + i] = fma2(s, nh, o);
+    }
+  }
+}
+
 // A 4-point step whose four values sit in the lanes l, l ^ M1, l ^ M2, l ^ (M1 | M2) (digit
-// value = the lane's bits at M1 and M2), in the same register slots: the sum
-// S = (v0 + v1) + (v2 + v3) of every position is reduced and scattered in two exchanges
+// value = the lane's bits at M1 and M2; the digit-4 step of G = 1024), in the same
+// register slots: the sum S = (v0 + v1) + (v2 + v3) of every position is reduced and
+// scattered in two exchanges
 // (the lanes with digit values {0, 1} form v0 + v1 and those with {2, 3} form v2 + v3, on
 // half of the positions each, then every lane adds the other pair's sum on a quarter: the
 // slot map i8_d3 gives those halves and quarters their own registers in each lane), and
@@ -171,7 +221,7 @@ __device__ __forceinline__ float rotate_regular(Lane4& t) {
   } else if constexpr (G == 16) {
     return 1.0f;
   } else {
-    i8_cross_step<1, 2>(t);  // digit 2: the four lanes of a quad (lane % 4)
+    i8_quad_step(t);  // digit 2: the four lanes of a quad (lane % 4)
     if constexpr (G == 64) {
       return -1.0f;
     } else {
@@ -198,6 +248,55 @@ __device__ __forceinline__ float rotate_regular(Lane4& t) {
 // Four packed int8 bytes (channel order) from the magic-add results of four channels.
 __device__ __forceinline__ uint32_t pack_i8x4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
+// The codes q = rint(y * inv) of the lane's rotated tile t (inv2 = (inv, inv), inv the
+// signed reciprocal of the row's scale) to the row's chunk qrow: blocks at or past
+// `nvalid` channels are not written (FULL: the caller knows the whole tile lies inside
+// the row).  rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
+// rounds (half to even) to an integer held, two's complement, in the low bits.  The sum
+// is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA 13.0, -O3) fuses a
+// packed multiply whose only use is a packed add into one fused multiply-add even when
+// both carry an explicit .rn, and rint of the unrounded product differs where RN(y * inv)
+// is exactly k + 1/2.  G <= 16: one 16-byte store per block; G >= 64: one 8-byte store per
+// half block (i8_out_block, i8_half).
+template <int G, bool FULL = false>
+__device__ __forceinline__ void i8_store_codes(int8_t* qrow, int lane, const Lane4& t, float2 inv2, int64_t nvalid) {
+  const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+  const float2 one2 = make_float2(1.0f, 1.0f);
+  auto ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < nvalid; };
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint32_t b[2][16];  // slots 2k and 2k + 1
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
+      b[0][i] = __float_as_uint(w.x);
+      b[1][i] = __float_as_uint(w.y);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if constexpr (G <= 16) {
+        const uint32_t bl = i8_out_block<G>(lane, 2 * k + c, 0);
+        if (ok(bl))
+          __stcs(reinterpret_cast<uint4*>(qrow + bl * 16u),
+                 make_uint4(pack_i8x4(b[c][0], b[c][1], b[c][2], b[c][3]),
+                            pack_i8x4(b[c][4], b[c][5], b[c][6], b[c][7]),
+                            pack_i8x4(b[c][8], b[c][9], b[c][10], b[c][11]),
+                            pack_i8x4(b[c][12], b[c][13], b[c][14], b[c][15])));
+      } else {
+        const uint32_t half = 8u * static_cast<uint32_t>(i8_half<G>(lane));
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t bl = i8_out_block<G>(lane, 2 * k + c, r);
+          if (ok(bl))
+            __stcs(reinterpret_cast<uint2*>(qrow + bl * 16u + half),
+                   make_uint2(pack_i8x4(b[c][8 * r], b[c][8 * r + 1], b[c][8 * r + 2], b[c][8 * r + 3]),
+                              pack_i8x4(b[c][8 * r + 4], b[c][8 * r + 5], b[c][8 * r + 6], b[c][8 * r + 7])));
+        }
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -310,6 +409,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
   constexpr int kTileBytes = kI8TileElems * es;
   constexpr int kSets = 4;
   const int lane = threadIdx.x & 31;
+  // the block halves this lane loads swapped (i8_half): in 16-byte words of a block and of its
+  // bf16 copy in shared memory
+  const int hs = i8_half<G>(lane);
+  const int hw = hs * ((BF16 ? 2 : 4) / 2);
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
   const int B = p.rows_per_block;
@@ -452,8 +555,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
             uint4 w4[2];
             if (block_ok(bl)) {
               const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kTileBytes + bl * 32u);
-              w4[0] = src[0];
-              w4[1] = src[1];
+              w4[0] = src[hs];
+              w4[1] = src[hs ^ 1];
             } else {
               w4[0] = w4[1] = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -474,7 +577,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
             uint4 w4[BF16 ? 2 : 4];
 #pragma unroll
             for (int k = 0; k < (BF16 ? 2 : 4); ++k)
-              w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + k)
+              w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + (k ^ hw))
                          : make_uint4(0u, 0u, 0u, 0u);
             float f[16];
             widen<BF16>(w4, f);
@@ -500,7 +603,6 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
       const int64_t jt = it - 1;
       const TileRef r = tile(cb);
       advance(cb);
-      auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < r.nvalid; };
       const bool ok = mbar_wait(smem_addr(&row_bar[r.set][r.b]), static_cast<uint32_t>(r.parity));
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         fail(drained_from);
@@ -519,36 +621,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
         tmem_wait_ld();
         Lane4 t;
         words_to_lane4(v, t);
-        const float2 inv2 = make_float2(inv, inv);
-        // rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
-        // rounds (half to even) to an integer held, two's complement, in the low bits.
-        // The sum is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA
-        // 13.0, -O3) fuses a packed multiply whose only use is a packed add into one
-        // fused multiply-add even when both carry an explicit .rn, and rint of the
-        // unrounded product differs where RN(y * inv) is exactly k + 1/2.
-        const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
-        const float2 one2 = make_float2(1.0f, 1.0f);
         int8_t* qrow = p.q + r.row * p.K + static_cast<int64_t>(r.chunk) * kI8TileElems;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          uint32_t bx[16], by[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
-            bx[i] = __float_as_uint(w.x);
-            by[i] = __float_as_uint(w.y);
-          }
-          const uint32_t box = i8_out_block<G>(lane, 2 * k);
-          const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
-          if (block_ok(box))
-            __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
-                   make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
-                              pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
-          if (block_ok(boy))
-            __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
-                   make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
-                              pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
-        }
+        i8_store_codes<G, FULL>(qrow, lane, t, make_float2(inv, inv), r.nvalid);
       }
     }
   }
@@ -604,6 +678,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
   constexpr int kRingTile = kI8TileElems * 2;
   constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
   const int lane = threadIdx.x & 31;
+  // the block halves this lane loads swapped (i8_half): in 16-byte words of a block and of its
+  // bf16 copy in shared memory
+  const int hs = i8_half<G>(lane);
+  const int hw = hs * ((BF16 ? 2 : 4) / 2);
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
   const int B = MULTI ? p.rows_per_block : 1;
@@ -675,8 +753,8 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
         uint4 w4[2];
         if (static_cast<int64_t>(bl) * 16 < nvalid) {
           const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kRingTile + bl * 32u);
-          w4[0] = src[0];
-          w4[1] = src[1];
+          w4[0] = src[hs];
+          w4[1] = src[hs ^ 1];
         } else {
           w4[0] = w4[1] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -695,7 +773,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
         const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
 #pragma unroll
         for (int e = 0; e < n16; ++e)
-          w4[e] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + e) : make_uint4(0u, 0u, 0u, 0u);
+          w4[e] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + (e ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
         float f[16];
         widen<BF16>(w4, f);
         put_block(t, q, f);
@@ -768,12 +846,14 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
         }
       }
     }
-    if (timed_out) {  // record it, wait (bounded) for this warp's copies still in flight
-      if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
-      const uint32_t n_issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
-      for (uint32_t m = k; m < n_issued; ++m)
-        mbar_wait(bar0 + static_cast<int>(m % STAGES) * 8, (m / STAGES) & 1u);
-      cta_broken = 1;
+    if constexpr (STAGES > 0) {
+      if (timed_out) {  // record it, wait (bounded) for this warp's copies still in flight
+        if (lane == 0) atomicOr(&g_hq_fault, kFaultWaitTimeout);
+        const uint32_t n_issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
+        for (uint32_t m = k; m < n_issued; ++m)
+          mbar_wait(bar0 + static_cast<int>(m % STAGES) * 8, (m / STAGES) & 1u);
+        cta_broken = 1;
+      }
     }
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
@@ -795,9 +875,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       inv[r] = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
       if (threadIdx.x == 0 && r < B && row0 + r < p.M) p.scales[row0 + r] = scale;
     }
-    // walk 2: the codes (rint by the magic constant, as in k_rotate_quant_int8)
-    const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
-    const float2 one2 = make_float2(1.0f, 1.0f);
+    // walk 2: the codes
     for (int g = wid; g < n_g; g += kI8Warps) {
       const int b = row_of(g);
       if (MULTI && row0 + b >= p.M) break;
@@ -811,27 +889,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       unpark(g, t);
       const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
       const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
-      int8_t* qrow = p.q + (row0 + b) * p.K + c0;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t bx[16], by[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 w = fma2(mul2(t.P[q][i], inv2), one2, magic2);
-          bx[i] = __float_as_uint(w.x);
-          by[i] = __float_as_uint(w.y);
-        }
-        const uint32_t box = i8_out_block<G>(lane, 2 * q);
-        const uint32_t boy = i8_out_block<G>(lane, 2 * q + 1);
-        if (static_cast<int64_t>(box) * 16 < nvalid)
-          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
-                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
-                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
-        if (static_cast<int64_t>(boy) * 16 < nvalid)
-          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
-                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
-                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
-      }
+      i8_store_codes<G>(p.q + (row0 + b) * p.K + c0, lane, t, inv2, nvalid);
     }
   }
   // Every thread's TMEM traffic is complete before the columns are freed.
@@ -863,6 +921,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
   constexpr int n16 = BF16 ? 2 : 4;  // 16-byte words per block of 16 channels
   constexpr float kSign = (G == 4 || G == 64 || G == 1024) ? -1.0f : 1.0f;
   const int lane = threadIdx.x & 31;
+  // the block halves this lane loads swapped (i8_half): in 16-byte words of a block and of its
+  // bf16 copy in shared memory
+  const int hs = i8_half<G>(lane);
+  const int hw = hs * ((BF16 ? 2 : 4) / 2);
   const int wid = threadIdx.x >> 5;
   const int T = p.tiles_per_row;
   __shared__ float row_max[2][kI8Warps];
@@ -879,7 +941,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
       const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
 #pragma unroll
       for (int k = 0; k < n16; ++k)
-        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + k) : make_uint4(0u, 0u, 0u, 0u);
+        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + (k ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
       float f[16];
       widen<BF16>(w4, f);
       put_block(t, j, f);
@@ -906,35 +968,13 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
     const float scale = __fdiv_rn(fmaxf(row_amax, 1e-12f), 127.0f);
     const float inv = __fdiv_rn(1.0f, scale) * kSign;  // -inv when the registers hold -y
     if (threadIdx.x == 0) p.scales[row] = scale;
-    // walk 2: the codes (rint by the magic constant, as in k_rotate_quant_int8)
+    // walk 2: the codes
     const float2 inv2 = make_float2(inv, inv);
-    const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
-    const float2 one2 = make_float2(1.0f, 1.0f);
     for (int chunk = wid; chunk < T; chunk += kI8Warps) {
       Lane4 t;
       const int64_t nvalid = load(row, chunk, t);
       rotate_regular<G>(t);
-      int8_t* qrow = p.q + row * p.K + static_cast<int64_t>(chunk) * kI8TileElems;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint32_t bx[16], by[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 w = fma2(mul2(t.P[k][i], inv2), one2, magic2);
-          bx[i] = __float_as_uint(w.x);
-          by[i] = __float_as_uint(w.y);
-        }
-        const uint32_t box = i8_out_block<G>(lane, 2 * k);
-        const uint32_t boy = i8_out_block<G>(lane, 2 * k + 1);
-        if (static_cast<int64_t>(box) * 16 < nvalid)
-          __stcs(reinterpret_cast<uint4*>(qrow + box * 16u),
-                 make_uint4(pack_i8x4(bx[0], bx[1], bx[2], bx[3]), pack_i8x4(bx[4], bx[5], bx[6], bx[7]),
-                            pack_i8x4(bx[8], bx[9], bx[10], bx[11]), pack_i8x4(bx[12], bx[13], bx[14], bx[15])));
-        if (static_cast<int64_t>(boy) * 16 < nvalid)
-          __stcs(reinterpret_cast<uint4*>(qrow + boy * 16u),
-                 make_uint4(pack_i8x4(by[0], by[1], by[2], by[3]), pack_i8x4(by[4], by[5], by[6], by[7]),
-                            pack_i8x4(by[8], by[9], by[10], by[11]), pack_i8x4(by[12], by[13], by[14], by[15])));
-      }
+      i8_store_codes<G>(p.q + row * p.K + static_cast<int64_t>(chunk) * kI8TileElems, lane, t, inv2, nvalid);
     }
   }
 }
