@@ -80,15 +80,13 @@ __device__ __forceinline__ void h4_step(float2& a0, float2& a1, float2& a2, floa
 // Which digit-3 value (block index bits 2..3 within a 256-group, or which
 // 64-group of the quad for G = 64) register slot j of a lane holds, for G >= 64.
 // Slot j is P[j >> 1], component j & 1; add2(P[0][i], P[1][i]) pairs digit-3 values
-// {0, 1} and {2, 3}.  For G = 64 and 256 the map is the same in every lane.  G = 1024
-// has a second cross-lane step, on digit 4 (the quad within the 1024-group, lane bits 2
-// and 3), run by i8_cross_step, whose lanes need their own slot orders: lane bit 2 swaps
-// the two float2 arrays, lane bit 3 swaps .x and .y.
+// {0, 1} and {2, 3}.  For G = 64 and 256 the map is the same in every lane.  For
+// G = 1024 lane bit 2 (the low bit of digit 4) swaps the two float2 arrays, which the
+// digit-4 step (i8_digit4_step) needs.
 template <int G>
 __device__ __forceinline__ uint32_t i8_d3(int lane, int j) {
-  const int k = j >> 1, c = j & 1;
-  const int lb = (G == 1024) ? (lane >> 2) : 0;
-  return static_cast<uint32_t>(((c ^ ((lb >> 1) & 1)) << 1) | (k ^ (lb & 1)));
+  const int lb = (G == 1024) ? ((lane >> 2) & 1) : 0;
+  return static_cast<uint32_t>(((j & 1) << 1) | ((j >> 1) ^ lb));
 }
 
 // For G >= 64: 1 if the lane's registers 0..7 of a block hold its channels 8..15 (and
@@ -125,7 +123,9 @@ __device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
 // (r = 1) of the slot: each in-lane 4-point step leaves, in the register that held
 // input digit value d, the output of digit value 3 - d; after the digit-2 step the
 // lane's registers 0..7 hold digit value 3 - c and registers 8..15 digit value 3 - (c ^ 1)
-// (c = lane % 4), each on the half i8_half of the block.  G <= 16: the whole block, r = 0.
+// (c = lane % 4), each on the half i8_half of the block; after the digit-4 step (G = 1024)
+// P[0] holds digit-4 value 3 - e and P[1] 3 - (e ^ 1) (e = (lane / 4) % 4).  G <= 16: the
+// whole block, r = 0.
 template <int G>
 __device__ __forceinline__ uint32_t i8_out_block(int lane, int j, int r) {
   const int d2 = 3 ^ (lane & 3) ^ r;
@@ -135,9 +135,9 @@ __device__ __forceinline__ uint32_t i8_out_block(int lane, int j, int r) {
     return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * i8_d3<G>(lane, j));
   else if constexpr (G == 256)
     return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * (3 - i8_d3<G>(lane, j)));
-  else
-    return static_cast<uint32_t>((lane >> 4) * 64 + (3 - ((lane >> 2) & 3)) * 16 + d2 +
-                                 4 * (3 - i8_d3<G>(lane, j)));
+  else  // the digit-4 step leaves P[0] and P[1] on the digit-3 values of P[0]
+    return static_cast<uint32_t>((lane >> 4) * 64 + (3 ^ ((lane >> 2) & 3) ^ (j >> 1)) * 16 + d2 +
+                                 4 * (3 - i8_d3<G>(lane, j & 1)));
 }
 
 // The digit-2 step (G >= 64): the four values of a position sit in the same register of
@@ -168,35 +168,27 @@ __device__ __forceinline__ void i8_quad_step(Lane4& t) {
   }
 }
 
-// A 4-point step whose four values sit in the lanes l, l ^ M1, l ^ M2, l ^ (M1 | M2) (digit
-// value = the lane's bits at M1 and M2; the digit-4 step of G = 1024), in the same
-// register slots: the sum S = (v0 + v1) + (v2 + v3) of every position is reduced and
-// scattered in two exchanges
-// (the lanes with digit values {0, 1} form v0 + v1 and those with {2, 3} form v2 + v3, on
-// half of the positions each, then every lane adds the other pair's sum on a quarter: the
-// slot map i8_d3 gives those halves and quarters their own registers in each lane), and
-// gathered back in two more.  Each lane then keeps its own input v_c and produces the
-// negated output of digit value 3 - c.  1.5 shuffles per value.
-template <int M1, int M2>
-__device__ __forceinline__ void i8_cross_step(Lane4& t) {
+// The digit-4 step (G = 1024): the four values of a position sit in the lanes l, l ^ 4,
+// l ^ 8, l ^ 12 (digit value e = (lane / 4) % 4), which agree on what every register holds
+// but for the digit-3 values of the two float2 arrays, swapped by lane bit 2 (i8_d3).  The
+// lanes e and e ^ 1 trade P[1], so each holds v_e and v_(e ^ 1) on the digit-3 values of
+// its own P[0]; the pair sums are traded with the lanes e ^ 2, and every lane forms S and
+// the negated outputs fma(S, -1/2, v_e) of digit value 3 - e (into P[0]) and
+// fma(S, -1/2, v_(e ^ 1)) of 3 - (e ^ 1) (into P[1]).  One shuffle per value.
+__device__ __forceinline__ void i8_digit4_step(Lane4& t) {
   const float2 nh = make_float2(-0.5f, -0.5f);
-  float s[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float2 r;
-    r.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, M1);
-    r.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, M1);
-    const float2 u = add2(t.P[0][i], r);  // the pair sum on this lane's P[0] positions
-    s[i] = __fadd_rn(u.x, __shfl_xor_sync(0xFFFFFFFFu, u.y, M2));
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 s0 = make_float2(s[i], __shfl_xor_sync(0xFFFFFFFFu, s[i], M2));  // S on P[0]
-    float2 s1;                                                                    // S on P[1]
-    s1.x = __shfl_xor_sync(0xFFFFFFFFu, s0.x, M1);
-    s1.y = __shfl_xor_sync(0xFFFFFFFFu, s0.y, M1);
-    t.P[0][i] = fma2(s0, nh, t.P[0][i]);
-    t.P[1][i] = fma2(s1, nh, t.P[1][i]);
+    float2 o;  // the pair lane's value on this lane's P[0] positions
+    o.x = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].x, 4);
+    o.y = __shfl_xor_sync(0xFFFFFFFFu, t.P[1][i].y, 4);
+    const float2 pr = add2(t.P[0][i], o);
+    float2 q;  // the other pair's sum
+    q.x = __shfl_xor_sync(0xFFFFFFFFu, pr.x, 8);
+    q.y = __shfl_xor_sync(0xFFFFFFFFu, pr.y, 8);
+    const float2 s = add2(pr, q);
+    t.P[0][i] = fma2(s, nh, t.P[0][i]);
+    t.P[1][i] = fma2(s, nh, o);
   }
 }
 
@@ -238,7 +230,7 @@ __device__ __forceinline__ float rotate_regular(Lane4& t) {
       if constexpr (G == 256) {
         return 1.0f;
       } else {
-        i8_cross_step<4, 8>(t);  // digit 4: the four quads of a 1024-group ((lane / 4) % 4)
+        i8_digit4_step(t);  // digit 4: the four quads of a 1024-group ((lane / 4) % 4)
         return -1.0f;
       }
     }
