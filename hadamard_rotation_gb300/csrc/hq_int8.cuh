@@ -84,9 +84,9 @@ __device__ __forceinline__ void h4_step(float2& a0, float2& a1, float2& a2, floa
 // G = 1024 lane bit 2 (the low bit of digit 4) swaps the two float2 arrays, which the
 // digit-4 step (i8_digit4_step) needs.
 template <int G>
-__device__ __forceinline__ uint32_t i8_d3(int lane, int j) {
+__device__ __forceinline__ int i8_d3(int lane, int j) {
   const int lb = (G == 1024) ? ((lane >> 2) & 1) : 0;
-  return static_cast<uint32_t>(((j & 1) << 1) | ((j >> 1) ^ lb));
+  return ((j & 1) << 1) | ((j >> 1) ^ lb);
 }
 
 // For G >= 64: 1 if the lane's registers 0..7 of a block hold its channels 8..15 (and
@@ -112,11 +112,11 @@ __device__ __forceinline__ int i8_half(int lane) {
 //   block's digit 2 and the slot's digit-3 value (i8_d3) its digit 3; for G = 1024, q % 4
 //   is digit 4 and q / 4 the 1024-group of the tile.
 template <int G>
-__device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
+__device__ __forceinline__ int i8_in_block(int lane, int j) {
   if constexpr (G <= 16)
-    return static_cast<uint32_t>(32 * j + lane);
+    return 32 * j + lane;
   else
-    return static_cast<uint32_t>((lane >> 2) * 16 + (lane & 3) + 4 * i8_d3<G>(lane, j));
+    return (lane >> 2) * 16 + (lane & 3) + 4 * i8_d3<G>(lane, j);
 }
 
 // Block that slot j holds after the rotation, in registers 0..7 (r = 0) or 8..15
@@ -127,17 +127,16 @@ __device__ __forceinline__ uint32_t i8_in_block(int lane, int j) {
 // P[0] holds digit-4 value 3 - e and P[1] 3 - (e ^ 1) (e = (lane / 4) % 4).  G <= 16: the
 // whole block, r = 0.
 template <int G>
-__device__ __forceinline__ uint32_t i8_out_block(int lane, int j, int r) {
+__device__ __forceinline__ int i8_out_block(int lane, int j, int r) {
   const int d2 = 3 ^ (lane & 3) ^ r;
   if constexpr (G <= 16)
-    return static_cast<uint32_t>(32 * j + lane);
+    return 32 * j + lane;
   else if constexpr (G == 64)
-    return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * i8_d3<G>(lane, j));
+    return (lane >> 2) * 16 + d2 + 4 * i8_d3<G>(lane, j);
   else if constexpr (G == 256)
-    return static_cast<uint32_t>((lane >> 2) * 16 + d2 + 4 * (3 - i8_d3<G>(lane, j)));
+    return (lane >> 2) * 16 + d2 + 4 * (3 - i8_d3<G>(lane, j));
   else  // the digit-4 step leaves P[0] and P[1] on the digit-3 values of P[0]
-    return static_cast<uint32_t>((lane >> 4) * 64 + (3 ^ ((lane >> 2) & 3) ^ (j >> 1)) * 16 + d2 +
-                                 4 * (3 - i8_d3<G>(lane, j & 1)));
+    return (lane >> 4) * 64 + (3 ^ ((lane >> 2) & 3) ^ (j >> 1)) * 16 + d2 + 4 * (3 - i8_d3<G>(lane, j & 1));
 }
 
 // The digit-2 step (G >= 64): the four values of a position sit in the same register of
@@ -242,10 +241,17 @@ __device__ __forceinline__ uint32_t pack_i8x4(uint32_t b0, uint32_t b1, uint32_t
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
+// Channels of warp tile `chunk` inside a row of K channels (at most one tile, 2048).
+__device__ __forceinline__ int i8_chunk_valid(int64_t K, int chunk) {
+  const int64_t rest = K - static_cast<int64_t>(chunk) * kI8TileElems;
+  return rest < kI8TileElems ? static_cast<int>(rest) : kI8TileElems;
+}
+
 // The codes q = rint(y * inv) of the lane's rotated tile t (inv2 = (inv, inv), inv the
 // signed reciprocal of the row's scale) to the row's chunk qrow: blocks at or past
-// `nvalid` channels are not written (FULL: the caller knows the whole tile lies inside
-// the row).  rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
+// `nvalid` (<= 2048) channels are not written (FULL: the caller knows the whole tile lies
+// inside the row).  Block offsets are signed ints, so that the compiler may fold a
+// store's fixed part into its address.  rint by the magic constant 1.5 * 2^23: |y * inv| <= 127 < 2^22, so the sum
 // rounds (half to even) to an integer held, two's complement, in the low bits.  The sum
 // is written fma(p, 1, magic) on the rounded product p: ptxas (CUDA 13.0, -O3) fuses a
 // packed multiply whose only use is a packed add into one fused multiply-add even when
@@ -253,10 +259,10 @@ __device__ __forceinline__ uint32_t pack_i8x4(uint32_t b0, uint32_t b1, uint32_t
 // is exactly k + 1/2.  G <= 16: one 16-byte store per block; G >= 64: one 8-byte store per
 // half block (i8_out_block, i8_half).
 template <int G, bool FULL = false>
-__device__ __forceinline__ void i8_store_codes(int8_t* qrow, int lane, const Lane4& t, float2 inv2, int64_t nvalid) {
+__device__ __forceinline__ void i8_store_codes(int8_t* qrow, int lane, const Lane4& t, float2 inv2, int nvalid) {
   const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
   const float2 one2 = make_float2(1.0f, 1.0f);
-  auto ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < nvalid; };
+  auto ok = [&](int bl) { return FULL || bl * 16 < nvalid; };
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     uint32_t b[2][16];  // slots 2k and 2k + 1
@@ -269,20 +275,20 @@ __device__ __forceinline__ void i8_store_codes(int8_t* qrow, int lane, const Lan
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       if constexpr (G <= 16) {
-        const uint32_t bl = i8_out_block<G>(lane, 2 * k + c, 0);
+        const int bl = i8_out_block<G>(lane, 2 * k + c, 0);
         if (ok(bl))
-          __stcs(reinterpret_cast<uint4*>(qrow + bl * 16u),
+          __stcs(reinterpret_cast<uint4*>(qrow + bl * 16),
                  make_uint4(pack_i8x4(b[c][0], b[c][1], b[c][2], b[c][3]),
                             pack_i8x4(b[c][4], b[c][5], b[c][6], b[c][7]),
                             pack_i8x4(b[c][8], b[c][9], b[c][10], b[c][11]),
                             pack_i8x4(b[c][12], b[c][13], b[c][14], b[c][15])));
       } else {
-        const uint32_t half = 8u * static_cast<uint32_t>(i8_half<G>(lane));
+        const int half = 8 * i8_half<G>(lane);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const uint32_t bl = i8_out_block<G>(lane, 2 * k + c, r);
+          const int bl = i8_out_block<G>(lane, 2 * k + c, r);
           if (ok(bl))
-            __stcs(reinterpret_cast<uint2*>(qrow + bl * 16u + half),
+            __stcs(reinterpret_cast<uint2*>(qrow + (bl * 16 + half)),
                    make_uint2(pack_i8x4(b[c][8 * r], b[c][8 * r + 1], b[c][8 * r + 2], b[c][8 * r + 3]),
                               pack_i8x4(b[c][8 * r + 4], b[c][8 * r + 5], b[c][8 * r + 6], b[c][8 * r + 7])));
         }
@@ -530,7 +536,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
       const TileRef r = tile(ca);
       advance(ca);
       const bool active = r.row < p.M;
-      auto block_ok = [&](uint32_t bl) { return FULL || static_cast<int64_t>(bl) * 16 < r.nvalid; };
+      auto block_ok = [&](int bl) { return FULL || static_cast<int64_t>(bl) * 16 < r.nvalid; };
       Lane4 t;
       float amax = 0.0f;
       if (active) {
@@ -543,10 +549,10 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t bl = i8_in_block<G>(lane, j);
+            const int bl = i8_in_block<G>(lane, j);
             uint4 w4[2];
             if (block_ok(bl)) {
-              const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kTileBytes + bl * 32u);
+              const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kTileBytes + bl * 32);
               w4[0] = src[hs];
               w4[1] = src[hs ^ 1];
             } else {
@@ -564,12 +570,12 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
           const uint8_t* rowp = p.x + r.row * p.ldx_bytes + static_cast<int64_t>(r.chunk) * kI8TileElems * es;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t bl = i8_in_block<G>(lane, j);
+            const int bl = i8_in_block<G>(lane, j);
             const bool ok = block_ok(bl);
             uint4 w4[BF16 ? 2 : 4];
 #pragma unroll
             for (int k = 0; k < (BF16 ? 2 : 4); ++k)
-              w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16u * es) + (k ^ hw))
+              w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(rowp + bl * 16 * es) + (k ^ hw))
                          : make_uint4(0u, 0u, 0u, 0u);
             float f[16];
             widen<BF16>(w4, f);
@@ -614,7 +620,7 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8(I8Params p)
         Lane4 t;
         words_to_lane4(v, t);
         int8_t* qrow = p.q + r.row * p.K + static_cast<int64_t>(r.chunk) * kI8TileElems;
-        i8_store_codes<G, FULL>(qrow, lane, t, make_float2(inv, inv), r.nvalid);
+        i8_store_codes<G, FULL>(qrow, lane, t, make_float2(inv, inv), static_cast<int>(r.nvalid));
       }
     }
   }
@@ -730,21 +736,22 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       for (int j = 0; j < STAGES; ++j) HQ_I8_PARK_FETCH(static_cast<int64_t>(blockIdx.x) * B, j);
   }
 
-  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0);
-  // from the ring: false if the wait ran out (the CTA is then broken).
-  auto load = [&](int64_t row0, int j, int64_t row, int chunk, Lane4& t) {
+  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0;
+  // `full`: the whole tile lies inside the row, and the call is written once with a
+  // literal true and once with false, so each copy is compiled for its case); from the
+  // ring: false if the wait ran out (the CTA is then broken).
+  auto load = [&](int64_t row, int chunk, int nvalid, bool full, Lane4& t) {
     const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
-    const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
     if constexpr (STAGES > 0) {
       const int slot = static_cast<int>(k % STAGES);
       const bool ok = mbar_wait(bar0 + slot * 8, (k / STAGES) & 1u);
       if (!__all_sync(0xFFFFFFFFu, ok)) return false;  // handled after walk 1
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t bl = i8_in_block<G>(lane, q);
+        const int bl = i8_in_block<G>(lane, q);
         uint4 w4[2];
-        if (static_cast<int64_t>(bl) * 16 < nvalid) {
-          const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kRingTile + bl * 32u);
+        if (full || bl * 16 < nvalid) {
+          const uint4* src = reinterpret_cast<const uint4*>(ring + slot * kRingTile + bl * 32);
           w4[0] = src[hs];
           w4[1] = src[hs ^ 1];
         } else {
@@ -760,12 +767,12 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t bl = i8_in_block<G>(lane, q);
+        const int bl = i8_in_block<G>(lane, q);
         uint4 w4[n16];
-        const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+        const bool ok = full || bl * 16 < nvalid;
 #pragma unroll
         for (int e = 0; e < n16; ++e)
-          w4[e] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + (e ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
+          w4[e] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16 * es) + (e ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
         float f[16];
         widen<BF16>(w4, f);
         put_block(t, q, f);
@@ -819,7 +826,15 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       const int b = row_of(g);
       if (MULTI && row0 + b >= p.M) break;  // rows past the end: every later g is past it too
       Lane4 t;
-      if (!load(row0, j, row0 + b, g - b * T, t)) {
+      const int chunk = g - b * T;
+      const int nvalid = i8_chunk_valid(p.K, chunk);
+      bool loaded;
+      if constexpr (STAGES > 0)  // shared-memory reads: the block checks cost little
+        loaded = load(row0 + b, chunk, nvalid, false, t);
+      else
+        loaded = nvalid == kI8TileElems ? load(row0 + b, chunk, nvalid, true, t)
+                                        : load(row0 + b, chunk, nvalid, false, t);
+      if (!loaded) {
         timed_out = true;
         break;
       }
@@ -879,9 +894,12 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_park(I8Para
       const float2 inv2 = make_float2(inv_b, inv_b);
       Lane4 t;
       unpark(g, t);
-      const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
-      const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
-      i8_store_codes<G>(p.q + (row0 + b) * p.K + c0, lane, t, inv2, nvalid);
+      int8_t* const qrow = p.q + (row0 + b) * p.K + static_cast<int64_t>(chunk) * kI8TileElems;
+      const int nvalid = i8_chunk_valid(p.K, chunk);
+      if (nvalid == kI8TileElems)
+        i8_store_codes<G, true>(qrow, lane, t, inv2, nvalid);
+      else
+        i8_store_codes<G, false>(qrow, lane, t, inv2, nvalid);
     }
   }
   // Every thread's TMEM traffic is complete before the columns are freed.
@@ -921,24 +939,23 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
   const int T = p.tiles_per_row;
   __shared__ float row_max[2][kI8Warps];
 
-  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0).
-  auto load = [&](int64_t row, int chunk, Lane4& t) {
+  // The warp tile `chunk` of row `row` into registers (blocks past the row's end read 0;
+  // `full` as in k_rotate_quant_int8_park).
+  auto load = [&](int64_t row, int chunk, int nvalid, bool full, Lane4& t) {
     const int64_t c0 = static_cast<int64_t>(chunk) * kI8TileElems;
-    const int64_t nvalid = p.K - c0 < kI8TileElems ? p.K - c0 : kI8TileElems;
     const uint8_t* src = p.x + row * p.ldx_bytes + c0 * es;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t bl = i8_in_block<G>(lane, j);
+      const int bl = i8_in_block<G>(lane, j);
       uint4 w4[n16];
-      const bool ok = static_cast<int64_t>(bl) * 16 < nvalid;
+      const bool ok = full || bl * 16 < nvalid;
 #pragma unroll
       for (int k = 0; k < n16; ++k)
-        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16u * es) + (k ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
+        w4[k] = ok ? __ldg(reinterpret_cast<const uint4*>(src + bl * 16 * es) + (k ^ hw)) : make_uint4(0u, 0u, 0u, 0u);
       float f[16];
       widen<BF16>(w4, f);
       put_block(t, j, f);
     }
-    return nvalid;
   };
 
   int64_t n = 0;
@@ -947,7 +964,11 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
     float amax = 0.0f;
     for (int chunk = wid; chunk < T; chunk += kI8Warps) {
       Lane4 t;
-      load(row, chunk, t);
+      const int nvalid = i8_chunk_valid(p.K, chunk);
+      if (nvalid == kI8TileElems)
+        load(row, chunk, nvalid, true, t);
+      else
+        load(row, chunk, nvalid, false, t);
       rotate_regular<G>(t);
 #pragma unroll
       for (int k = 0; k < 2; ++k)
@@ -964,9 +985,17 @@ __global__ void __launch_bounds__(kI8Threads, 1) k_rotate_quant_int8_long(I8Para
     const float2 inv2 = make_float2(inv, inv);
     for (int chunk = wid; chunk < T; chunk += kI8Warps) {
       Lane4 t;
-      const int64_t nvalid = load(row, chunk, t);
-      rotate_regular<G>(t);
-      i8_store_codes<G>(p.q + row * p.K + static_cast<int64_t>(chunk) * kI8TileElems, lane, t, inv2, nvalid);
+      int8_t* const qrow = p.q + row * p.K + static_cast<int64_t>(chunk) * kI8TileElems;
+      const int nvalid = i8_chunk_valid(p.K, chunk);
+      if (nvalid == kI8TileElems) {
+        load(row, chunk, nvalid, true, t);
+        rotate_regular<G>(t);
+        i8_store_codes<G, true>(qrow, lane, t, inv2, nvalid);
+      } else {
+        load(row, chunk, nvalid, false, t);
+        rotate_regular<G>(t);
+        i8_store_codes<G, false>(qrow, lane, t, inv2, nvalid);
+      }
     }
   }
 }
