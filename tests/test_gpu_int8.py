@@ -53,7 +53,7 @@ def check(x_host, group, x_dev=None):
 
 SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16), (9, 2304, 256),
           (100, 4096, 64), (7, 32768, 256), (1000, 1024, 16), (301, 3072, 64), (64, 6144, 256),
-          (40, 30720, 16),
+          (40, 30720, 16), (11, 2048 + 192, 64),
           # group 4 (one digit), group 1024 (five digits, two of them across lanes)
           (2, 16, 4), (37, 2064, 4), (5, 1024, 1024), (13, 3072, 1024), (8, 32768, 1024),
           # rows longer than tensor memory holds, parked in tensor and shared memory: 17 warp
@@ -63,7 +63,7 @@ SHAPES = [(1, 16, 16), (3, 48, 16), (17, 64, 64), (5, 256, 256), (33, 2048, 16),
           # 2 or 3 such rows per CTA step (T <= 24): a partial last block, more blocks than SMs
           (301, 36864, 256), (500, 40960, 16), (7, 47104 + 64, 64),
           # longer still, each row read twice: a ragged 60th tile, 60 and 64 tiles
-          (2, 120832 + 16, 16), (2, 122880, 256), (2, 131072, 1024)]
+          (2, 120832 + 16, 16), (2, 122880, 256), (2, 131072, 1024), (2, 122880 + 192, 64)]
 
 
 @pytest.mark.parametrize("M,K,group", SHAPES)
