@@ -2,7 +2,7 @@
 //
 // The second workload of the pages ("hyperflow_h3_flash_int8.py", HyperFlow:
 // regular_hadamard, rotate_quant_kernel):
-//   y     = x . R_G per run of G channels, R_G = kron(H4/2, ..., H4/2), G in {16, 64, 256},
+//   y     = x . R_G per run of G channels, R_G = kron(H4/2, ..., H4/2), G in {4, 16, 64, 256, 1024},
 //           H4 = [[1,1,1,-1],[1,1,-1,1],[1,-1,1,1],[-1,1,1,1]];
 //   scale = max(amax_row |y|, 1e-12) / 127, one fp32 per row;
 //   q     = clamp(rint(y * (1 / scale)), -127, 127), int8.
@@ -36,8 +36,9 @@
 // one half of their blocks, so that each holds both values of the pair on the other
 // half, and the pair sums are traded with the lanes c ^ 2 (one shuffle per value); a
 // lane then holds, on its half of each block, the outputs of digit values 3 - c and
-// 3 - (c ^ 1), which relabels its registers for the stores.  Digit 3 (G = 256) is
-// in-lane, packed two positions per FADD2.
+// 3 - (c ^ 1), which relabels its registers for the stores.  Digit 3 (G >= 256) is
+// in-lane, packed two positions per FADD2; digit 4 (G = 1024) pairs lanes as digit 2 does,
+// on the two float2 arrays instead of the block halves.
 #pragma once
 
 #include "hq_kernels.cuh"
